@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark: FP32 SGEMM TFLOP/s at M = N = K = 4096 on GB300, and its fraction
+of the chip's FP32 FFMA peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--algo ID]
+
+One step is one call of the library (C = alpha*A@B + beta*C) on one batch of
+synthetic inputs (uniform[-1, 1), seed of the workload) already resident in
+HBM.  Three input sets are rotated so that consecutive steps never find their
+operands in L2.  Prints ONE JSON line on rank 0.
+
+Under torchrun (N > 1) every rank multiplies its own copy of the workload on
+its own GPU (independent replicas, no data exchange); the host-side barrier
+and the max over ranks of the timed region give the whole-job number.
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (whole output rows), with the same
+metric and unit.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp32_sgemm_gb300 import inputs  # noqa: E402
+
+FFMA_PER_CLK_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
+PAGES_BEST_TFLOPS = 9.66           # best kernel of the pages at 4096^3 (RTX 3060, "09 Staged")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_ffma_4096_traffic.txt")
+KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_ffma.cuh", "fp32_sgemm_gb300/csrc/ptx.cuh",
+                  "fp32_sgemm_gb300/csrc/sgemm_api.cu", "fp32_sgemm_gb300/csrc/kernel_table.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sgemm_4096", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--algo", type=int, default=0, help="tile configuration (0 = automatic)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES + sorted(
+            os.path.relpath(p, ROOT) for p in
+            __import__("glob").glob(os.path.join(ROOT, "fp32_sgemm_gb300", "csrc", "sgemm_algo*.cu"))):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        fields = {}
+        for line in open(PROFILE_SUMMARY):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm),
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons)}
+
+
+def sm_max_mhz_query(index: int) -> float | None:
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        return float(out.splitlines()[0])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_rows_sample(w, p, seconds: float, steps: int = 1):
+    """Time the oracle on whole output rows of the workload.  Returns
+    (flops_per_step, seconds_per_step, rows, threads) for a sample sized so
+    that `steps` samples take about `seconds` in total."""
+    import oracle
+    threads = oracle.max_threads()
+    probe_rows = max(1, min(w.M, 32))
+    t0 = time.perf_counter()
+    oracle.sgemm_ref(probe_rows, w.N, w.K, w.alpha, p.A[:probe_rows], p.B, w.beta,
+                     p.C0[:probe_rows] if p.C0 is not None else None)
+    rate = probe_rows / max(time.perf_counter() - t0, 1e-6)      # rows per second
+    rows = int(max(1, min(w.M, rate * seconds / max(steps, 1))))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.sgemm_ref(rows, w.N, w.K, w.alpha, p.A[:rows], p.B, w.beta,
+                         p.C0[:rows] if p.C0 is not None else None)
+        times.append(time.perf_counter() - t0)
+    return 2.0 * rows * w.N * w.K, times, rows, threads
+
+
+def run_reference(args, w, rank: int, world: int):
+    if rank != 0:
+        return
+    p = inputs.workload_problem(w, "uniform")
+    steps = max(1, args.steps)
+    warm = max(0, args.warmup)
+    budget = 120.0        # seconds for the whole --steps/--warmup run
+    flops, times, rows, threads = oracle_rows_sample(w, p, budget, steps + warm)
+    timed = times[warm:] if len(times) > warm else times
+    t = sum(timed) / len(timed)
+    value = flops / t / 1e12
+    sample = (f"{rows} of {w.M} output rows per step (all {w.N} columns, K={w.K}), "
+              f"fp64 oracle, {threads} threads")
+    line = {
+        "impl": "reference",
+        "metric": "SGEMM TFLOP/s at M=N=K=4096 FP32; % of GB300 FP32 FFMA peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": len(timed),
+        "warmup": warm, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / PAGES_BEST_TFLOPS, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "cpu oracle sample"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, l2_note: str) -> dict:
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+            "beta": w.beta, "seed": w.seed, "layout": "row-major A[M,K] B[K,N] C[M,N]",
+            "inputs": "uniform[-1,1) SplitMix64", "l2": l2_note}
+
+
+# ------------------------------------------------------------------ GPU path
+
+def run_ours(args, w, rank: int, world: int, local_rank: int):
+    import torch
+    import fp32_sgemm_gb300 as sg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    sg.load_library(build_if_missing=True)
+    handle = sg.Handle(dev)
+    handle.set_algo(args.algo)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    l2_bytes = getattr(props, "L2_cache_size", 0) or 0
+
+    p = inputs.workload_problem(w, "uniform")
+    set_bytes = 4 * (p.A.size + p.B.size + w.M * w.N)
+    nsets = 3
+    A0 = torch.from_numpy(p.A).to(dev)
+    B0 = torch.from_numpy(p.B).to(dev)
+    C0 = torch.from_numpy(p.C0).to(dev) if p.C0 is not None else torch.zeros((w.M, w.N), device=dev)
+    sets = [(A0, B0, C0)] + [(A0.clone(), B0.clone(), C0.clone()) for _ in range(nsets - 1)]
+    handle._ensure_workspace(handle.workspace_size(w.M, w.N, w.K, A0.data_ptr(), A0.stride(0),
+                                                   B0.data_ptr(), B0.stride(0)))
+    plan = handle.plan(A0, B0, C0, w.alpha, w.beta)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        A, B, C = sets[i % nsets]
+        handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert handle.device_error() == 0
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    assert handle.device_error() == 0
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    flops = 2.0 * w.M * w.N * w.K
+    ms_per_step = elapsed_ms / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # Roofline of the dominant (main) kernel: FFMA-bound.
+    mean_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    max_mhz = clocks.get("sm_max_mhz") or sm_max_mhz_query(local_rank) or 2070.0
+    peak = sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    sus_mhz = clocks.get("sm_mhz")
+    peak_sus = sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
+    roofline = {
+        "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak, "traffic": profiled_traffic(),
+        "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz (max SM clock)",
+        "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
+        "sustained_sm_mhz": sus_mhz,
+        "kernel_ms_mean": mean_launch_ms, "kernel_ms_min": min(launch_ms),
+        "kernel_ms_median": statistics.median(launch_ms),
+    }
+
+    # End to end through the host-buffer C entry point: pinned host A, B (C),
+    # copies up, product, copy of C down, all inside the timed region.
+    e2e = None
+    if args.e2e_steps > 0:
+        Ah = torch.from_numpy(p.A).pin_memory()
+        Bh = torch.from_numpy(p.B).pin_memory()
+        Ch = (torch.from_numpy(p.C0.copy()) if p.C0 is not None
+              else torch.zeros((w.M, w.N))).pin_memory()
+        ws = torch.empty(sg.host_workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=handle, stream=stream)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=handle, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0.0 else 0))
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N,
+               "ms_per_step": e_ms, "steps": args.e2e_steps,
+               "path": "sgemmHostEx: pinned host A,B -> device, SGEMM, C -> pinned host"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        c_flops, c_times, rows, threads = oracle_rows_sample(w, p, args.cpu_seconds, 1)
+        cpu = {"value": c_flops / c_times[0] / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{rows} of {w.M} output rows (all {w.N} columns, K={w.K}) "
+                         f"in {c_times[0]:.1f} s, fp64 C oracle"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "SGEMM TFLOP/s at M=N=K=4096 FP32; % of GB300 FP32 FFMA peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / PAGES_BEST_TFLOPS,
+        "vs_baseline_ref": "9.66 TFLOP/s: the pages' best kernel at 4096^3 on an RTX 3060",
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(
+            w, f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB "
+               f"(> {l2_bytes / 1e6:.0f} MB L2)"),
+            algo=args.algo, tile=f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+            stages=plan["stages"], ctas=plan["ctas"], parallelism=f"replicas x{world}"),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * plan["launches"],
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    w = inputs.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,57 @@
+// Registry of compiled main-kernel instantiations.  Each sgemm_algo*.cu
+// translation unit instantiates one tile configuration (all four
+// beta == 0 / beta != 0 x vector / scalar epilogue variants) so that the
+// configurations compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "sgemm_ffma.cuh"
+
+namespace sg {
+
+constexpr int kMaxDevices = 64;
+
+struct KernelEntry {
+    const void *fn;
+    int threads;
+    int smem;
+    int bm, bn, bk, stages;
+    int occupancy[kMaxDevices];   // CTAs per SM, 0 = not yet queried
+};
+
+// Variant index: (beta != 0) * 2 + (scalar epilogue).
+template <class Cfg, bool BZ, bool CV>
+KernelEntry make_entry() {
+    KernelEntry e{};
+    e.fn = reinterpret_cast<const void *>(&sgemm_ffma_tma_kernel<Cfg, BZ, CV>);
+    e.threads = Cfg::THREADS;
+    e.smem = Cfg::SMEM_BYTES;
+    e.bm = Cfg::BM;
+    e.bn = Cfg::BN;
+    e.bk = Cfg::BK;
+    e.stages = Cfg::STAGES;
+    return e;
+}
+
+template <class Cfg>
+void fill_variants(KernelEntry *v) {
+    v[0] = make_entry<Cfg, true, true>();
+    v[1] = make_entry<Cfg, true, false>();
+    v[2] = make_entry<Cfg, false, true>();
+    v[3] = make_entry<Cfg, false, false>();
+}
+
+constexpr int kNumAlgos = 4;
+void fill_algo1(KernelEntry *v);
+void fill_algo2(KernelEntry *v);
+void fill_algo3(KernelEntry *v);
+void fill_algo4(KernelEntry *v);
+
+// Auxiliary kernels (sgemm_aux.cu).
+void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, cudaStream_t s);
+void launch_pack_rows(const float *src, int64_t ld_src, float *dst, int64_t ld_dst,
+                      int rows, int cols, cudaStream_t s);
+void launch_wait_selftest(uint32_t *err, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace sg

@@ -1,0 +1,484 @@
+// C ABI of the GB300 FP32 SGEMM library (declared in include/sgemm_gb300.h).
+//
+// Host side of the hot path: argument validation, BLAS quick returns, the
+// choice between reading A/B in place through TMA or repacking them into the
+// caller's workspace first, tensor-map encoding, tile-configuration choice
+// and the persistent launch.  The launch shape follows the pages' host
+// launcher (a grid of output tiles, one kernel instantiation per beta == 0 /
+// beta != 0; "The Final Kernel", maxxfuu article4/page14, launch_sgemm_final),
+// made persistent: at most one CTA per SM slot, tiles taken round robin.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sgemm_gb300.h"
+#include "kernel_table.h"
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr uint64_t kMinTimeoutNs = 1000000ull;
+
+using sg::KernelEntry;
+using sg::kMaxDevices;
+using sg::kNumAlgos;
+
+KernelEntry g_kernels[kNumAlgos][4];
+std::once_flag g_kernels_once;
+std::mutex g_occ_mutex;
+
+void init_kernel_table() {
+    sg::fill_algo1(g_kernels[0]);
+    sg::fill_algo2(g_kernels[1]);
+    sg::fill_algo3(g_kernels[2]);
+    sg::fill_algo4(g_kernels[3]);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+}  // namespace
+
+struct sgemmContext {
+    int device = -1;
+    int sm_count = 0;
+    uint32_t *d_err = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    uint64_t timeout_ns = kDefaultTimeoutNs;
+    int algo = 0;
+};
+
+namespace {
+
+sgemmHandle_t g_default[kMaxDevices] = {};
+std::mutex g_default_mutex;
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t x, int64_t a) { return (x + a - 1) / a; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxBytes = int64_t(1) << 40;
+
+// Validation shared by every entry point.  Pure host logic: no CUDA calls.
+sgemmStatus_t validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                       const void *B, int64_t ldb, const void *C, int64_t ldc,
+                       bool need_ab) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_STATUS_INVALID_VALUE;
+    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) ||
+        ldc < std::max<int64_t>(1, N))
+        return SGEMM_STATUS_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_STATUS_SUCCESS;
+    if (C == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    if (need_ab && K > 0 && (A == nullptr || B == nullptr)) return SGEMM_STATUS_INVALID_VALUE;
+    if (!aligned(C, 4)) return SGEMM_STATUS_MISALIGNED;
+    if (need_ab && K > 0 && (!aligned(A, 4) || !aligned(B, 4))) return SGEMM_STATUS_MISALIGNED;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
+    if (lda > kMaxBytes / 4 || ldb > kMaxBytes / 4 || ldc > kMaxBytes / 4)
+        return SGEMM_STATUS_NOT_SUPPORTED;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+inline bool tma_ok(const void *p, int64_t ld) { return aligned(p, 16) && (ld % 4) == 0; }
+
+struct Plan {
+    sgemmPlan_t pub{};
+    int algo_index = -1;   // row of g_kernels
+    int variant = 0;       // column of g_kernels
+    int64_t lda_p = 0, ldb_p = 0;
+    size_t ws_a = 0, ws_b = 0;
+    int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 8;
+};
+
+int choose_algo(const sgemmContext *h, int64_t M, int64_t N, int64_t K) {
+    if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
+    (void)M; (void)N; (void)K;
+    return 0;
+}
+
+int occupancy_for(const sgemmContext *h, KernelEntry &e) {
+    std::lock_guard<std::mutex> lk(g_occ_mutex);
+    int &occ = e.occupancy[h->device];
+    if (occ == 0) {
+        if (cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e.smem) != cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, e.fn, e.threads, e.smem) != cudaSuccess || n < 1)
+            return -1;
+        occ = n;
+    }
+    return occ;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Host-only part of the plan (no CUDA calls).
+sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                        const float *C, int64_t ldc, Plan &pl) {
+    pl = Plan{};
+    if (M == 0 || N == 0) return SGEMM_STATUS_SUCCESS;
+    if (K == 0 || alpha == 0.0f) {
+        pl.pub.kind = 2;
+        pl.pub.launches = 1;
+        return SGEMM_STATUS_SUCCESS;
+    }
+    std::call_once(g_kernels_once, init_kernel_table);
+    pl.pub.kind = 1;
+    pl.pub.packs_a = tma_ok(A, lda) ? 0 : 1;
+    pl.pub.packs_b = tma_ok(B, ldb) ? 0 : 1;
+    pl.pub.vector_epilogue = tma_ok(C, ldc) ? 1 : 0;
+    pl.lda_p = pl.pub.packs_a ? round_up(K, 4) : lda;
+    pl.ldb_p = pl.pub.packs_b ? round_up(N, 4) : ldb;
+    pl.ws_a = pl.pub.packs_a ? align256(size_t(M) * size_t(pl.lda_p) * 4) : 0;
+    pl.ws_b = pl.pub.packs_b ? align256(size_t(K) * size_t(pl.ldb_p) * 4) : 0;
+    pl.algo_index = choose_algo(h, M, N, K);
+    pl.variant = (beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
+    const KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
+    pl.tiles_m = int(ceil_div(M, e.bm));
+    pl.tiles_n = int(ceil_div(N, e.bn));
+    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n;
+    if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
+    pl.num_tiles = int(tiles);
+    pl.pub.tile_m = e.bm;
+    pl.pub.tile_n = e.bn;
+    pl.pub.tile_k = e.bk;
+    pl.pub.stages = e.stages;
+    pl.pub.launches = 1 + pl.pub.packs_a + pl.pub.packs_b;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t encode_2d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer,
+                        int64_t ld, int box_inner, int box_outer, CUtensorMapSwizzle swz) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return SGEMM_STATUS_LAUNCH_FAILED;
+    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+    cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+CUtensorMapSwizzle swizzle_for_bk(int bk) {
+    return bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+sgemmStatus_t launch_pack(const float *src, int64_t ld_src, float *dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, cudaStream_t stream) {
+    sg::launch_pack_rows(src, ld_src, dst, ld_dst, int(rows), int(cols), stream);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                  int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                  cudaStream_t stream) {
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    Plan pl;
+    st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (cur != h->device) return SGEMM_STATUS_INVALID_VALUE;
+
+    if (pl.pub.kind == 2) {
+        sg::launch_scale_c(int(M), int(N), beta, C, ldc, stream);
+        return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+    }
+
+    const float *Ause = A, *Buse = B;
+    if (pl.pub.packs_a || pl.pub.packs_b) {
+        if (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b) return SGEMM_STATUS_WORKSPACE_REQUIRED;
+        char *ws = static_cast<char *>(h->ws);
+        if (pl.pub.packs_a) {
+            float *Ap = reinterpret_cast<float *>(ws);
+            st = launch_pack(A, lda, Ap, pl.lda_p, M, K, stream);
+            if (st != SGEMM_STATUS_SUCCESS) return st;
+            Ause = Ap;
+        }
+        if (pl.pub.packs_b) {
+            float *Bp = reinterpret_cast<float *>(ws + pl.ws_a);
+            st = launch_pack(B, ldb, Bp, pl.ldb_p, K, N, stream);
+            if (st != SGEMM_STATUS_SUCCESS) return st;
+            Buse = Bp;
+        }
+    }
+
+    KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
+    const int occ = occupancy_for(h, e);
+    if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
+
+    CUtensorMap tmA, tmB;
+    st = encode_2d(&tmA, Ause, K, M, pl.lda_p, e.bk, e.bm, swizzle_for_bk(e.bk));
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    st = encode_2d(&tmB, Buse, N, K, pl.ldb_p, e.bn, e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+
+    sg::GemmArgs args{};
+    args.M = int(M);
+    args.N = int(N);
+    args.K = int(K);
+    args.alpha = alpha;
+    args.beta = beta;
+    args.C = C;
+    args.ldc = ldc;
+    args.tiles_m = pl.tiles_m;
+    args.tiles_n = pl.tiles_n;
+    args.num_tiles = pl.num_tiles;
+    args.k_blocks = int(ceil_div(K, e.bk));
+    args.group_m = pl.group_m;
+    args.err = h->d_err;
+    args.timeout_ns = h->timeout_ns;
+
+    const int ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+    void *kargs[] = {&tmA, &tmB, &args};
+    cudaError_t err = cudaLaunchKernel(e.fn, dim3(ctas), dim3(e.threads), kargs, size_t(e.smem), stream);
+    return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sgemmGetStatusString(sgemmStatus_t s) {
+    switch (s) {
+        case SGEMM_STATUS_SUCCESS: return "SGEMM_STATUS_SUCCESS";
+        case SGEMM_STATUS_INVALID_VALUE: return "SGEMM_STATUS_INVALID_VALUE";
+        case SGEMM_STATUS_MISALIGNED: return "SGEMM_STATUS_MISALIGNED";
+        case SGEMM_STATUS_ARCH_MISMATCH: return "SGEMM_STATUS_ARCH_MISMATCH";
+        case SGEMM_STATUS_WORKSPACE_REQUIRED: return "SGEMM_STATUS_WORKSPACE_REQUIRED";
+        case SGEMM_STATUS_LAUNCH_FAILED: return "SGEMM_STATUS_LAUNCH_FAILED";
+        case SGEMM_STATUS_DEVICE_TIMEOUT: return "SGEMM_STATUS_DEVICE_TIMEOUT";
+        case SGEMM_STATUS_NOT_SUPPORTED: return "SGEMM_STATUS_NOT_SUPPORTED";
+        case SGEMM_STATUS_INTERNAL_ERROR: return "SGEMM_STATUS_INTERNAL_ERROR";
+    }
+    return "SGEMM_STATUS_UNKNOWN";
+}
+
+sgemmStatus_t sgemmGetVersion(int *version) {
+    if (version == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *version = kVersion;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmCreate(sgemmHandle_t *handle) {
+    if (handle == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *handle = nullptr;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    if (major != 10 || minor != 3) return SGEMM_STATUS_ARCH_MISMATCH;
+    auto *h = new (std::nothrow) sgemmContext();
+    if (h == nullptr) return SGEMM_STATUS_INTERNAL_ERROR;
+    h->device = dev;
+    h->sm_count = sms;
+    if (cudaMalloc(&h->d_err, sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(h->d_err);
+        delete h;
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    }
+    *handle = h;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmDestroy(sgemmHandle_t h) {
+    if (h == nullptr) return SGEMM_STATUS_SUCCESS;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    cudaFree(h->d_err);
+    if (prev >= 0) cudaSetDevice(prev);
+    delete h;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle) {
+    if (handle == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    std::lock_guard<std::mutex> lk(g_default_mutex);
+    if (g_default[dev] == nullptr) {
+        sgemmStatus_t st = sgemmCreate(&g_default[dev]);
+        if (st != SGEMM_STATUS_SUCCESS) return st;
+    }
+    *handle = g_default[dev];
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t h, int64_t M, int64_t N, int64_t K,
+                                    const float *A, int64_t lda, const float *B, int64_t ldb,
+                                    size_t *bytes) {
+    if (bytes == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *bytes = 0;
+    const float dummy_c = 0.f;
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, &dummy_c, std::max<int64_t>(1, N), true);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0 || K == 0) return st;
+    Plan pl;
+    st = make_plan(h, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, std::max<int64_t>(1, N), pl);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    *bytes = pl.ws_a + pl.ws_b;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetWorkspace(sgemmHandle_t h, void *ptr, size_t bytes) {
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    if (ptr != nullptr && !aligned(ptr, 256)) return SGEMM_STATUS_MISALIGNED;
+    h->ws = ptr;
+    h->ws_bytes = ptr ? bytes : 0;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmEx(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                      const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                      float *C, int64_t ldc, cudaStream_t stream) {
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    return run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+sgemmStatus_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                    const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                    cudaStream_t stream) {
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    sgemmHandle_t h = nullptr;
+    st = sgemmGetDefaultHandle(&h);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    return run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K, size_t *bytes) {
+    if (bytes == nullptr || M < 0 || N < 0 || K < 0) return SGEMM_STATUS_INVALID_VALUE;
+    *bytes = align256(size_t(M) * size_t(round_up(std::max<int64_t>(K, 1), 4)) * 4) +
+             align256(size_t(K) * size_t(round_up(std::max<int64_t>(N, 1), 4)) * 4) +
+             align256(size_t(M) * size_t(round_up(std::max<int64_t>(N, 1), 4)) * 4);
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmHostEx(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                          const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                          float *C, int64_t ldc, void *dws, size_t ws_bytes, cudaStream_t stream) {
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    if (h == nullptr || dws == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    if (!aligned(dws, 256)) return SGEMM_STATUS_MISALIGNED;
+    size_t need = 0;
+    sgemmHostWorkspaceSize(M, N, K, &need);
+    if (ws_bytes < need) return SGEMM_STATUS_WORKSPACE_REQUIRED;
+    const int64_t lda_p = round_up(std::max<int64_t>(K, 1), 4);
+    const int64_t ldb_p = round_up(std::max<int64_t>(N, 1), 4);
+    const int64_t ldc_p = ldb_p;
+    char *base = static_cast<char *>(dws);
+    float *dA = reinterpret_cast<float *>(base);
+    float *dB = reinterpret_cast<float *>(base + align256(size_t(M) * lda_p * 4));
+    float *dC = reinterpret_cast<float *>(base + align256(size_t(M) * lda_p * 4) +
+                                          align256(size_t(K) * ldb_p * 4));
+    const bool use_ab = K > 0 && alpha != 0.0f;
+    if (use_ab) {
+        if (cudaMemcpy2DAsync(dA, lda_p * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaMemcpy2DAsync(dB, ldb_p * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+    }
+    if (beta != 0.0f) {
+        if (cudaMemcpy2DAsync(dC, ldc_p * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+    }
+    st = run(h, M, N, K, alpha, dA, lda_p, dB, ldb_p, beta, dC, ldc_p, stream);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    if (cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_p * 4, N * 4, M, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, float alpha,
+                             const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                             const float *C, int64_t ldc, sgemmPlan_t *plan) {
+    if (plan == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    std::memset(plan, 0, sizeof(*plan));
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    Plan pl;
+    st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    if (pl.pub.kind == 1) {
+        const int occ = occupancy_for(h, g_kernels[pl.algo_index][pl.variant]);
+        if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
+        pl.pub.ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+    }
+    *plan = pl.pub;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
+    if (h == nullptr || algo < 0 || algo > kNumAlgos) return SGEMM_STATUS_INVALID_VALUE;
+    h->algo = algo;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetWaitTimeout(sgemmHandle_t h, uint64_t timeout_ns) {
+    if (h == nullptr || timeout_ns < kMinTimeoutNs) return SGEMM_STATUS_INVALID_VALUE;
+    h->timeout_ns = timeout_ns;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmGetDeviceError(sgemmHandle_t h, int *code) {
+    if (h == nullptr || code == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *code = 0;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    uint32_t word = 0;
+    sgemmStatus_t st = SGEMM_STATUS_SUCCESS;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, h->d_err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess)
+        st = SGEMM_STATUS_LAUNCH_FAILED;
+    if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    *code = int(word);
+    return word == 0 ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_DEVICE_TIMEOUT;
+}
+
+sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t h, uint64_t timeout_ns, cudaStream_t stream) {
+    if (h == nullptr || timeout_ns < kMinTimeoutNs || timeout_ns > 10 * kDefaultTimeoutNs)
+        return SGEMM_STATUS_INVALID_VALUE;
+    sg::launch_wait_selftest(h->d_err, timeout_ns, stream);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+}  // extern "C"

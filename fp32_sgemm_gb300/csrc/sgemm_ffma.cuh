@@ -1,0 +1,300 @@
+// FP32 SGEMM main kernel for sm_103a: C = alpha * A.B + beta * C, row major.
+//
+// Structure (one persistent CTA per SM slot, tiles taken round robin):
+//   * one producer warp: one elected lane streams the K slices of A and B
+//     into an S-stage shared-memory ring with TMA tile loads; each stage has
+//     a "full" mbarrier (TMA transaction bytes) and an "empty" mbarrier (one
+//     arrival per consumer warp).  Out-of-range rows/columns of partial tiles
+//     arrive as zeros (TMA out-of-bounds fill), so M, N, K need not be tile
+//     multiples.
+//   * WARPS_M x WARPS_N consumer warps: each lane keeps an 8 x 16 register
+//     tile of FP32 accumulators and, for every k, forms the outer product of
+//     8 values of A and 16 values of B with packed two-wide FP32 FMAs
+//     (fma.rn.f32x2: each lane issues one instruction per two products).
+//   * epilogue straight from registers: alpha*acc (+ beta*C, and C is not
+//     read when beta == 0), 16-byte stores when C's alignment allows.
+//
+// What the pages contribute, and what changed for this chip:
+//   * the per-thread outer-product register tile and the K loop over staged
+//     shared-memory slices ("2D Register Tiling: The Outer Product",
+//     maxxfuu article4/page8; easonhuang.dev/blog/gpu_matmul, "2D
+//     Blocktiling" and "Kernel 8: Warptiling");
+//   * loading the next slice while this one is computed, one sync per slice
+//     (easonhuang.dev, "Kernel 9 & 10: Staging"; "The Final Kernel",
+//     maxxfuu article4/page14), here as a TMA + mbarrier ring of S stages
+//     instead of register-staged double buffering;
+//   * the thread tile's A values read as 16-byte vectors (the pages transpose
+//     A in shared memory for this; TMA cannot transpose 4-byte elements, so
+//     A stays k-contiguous and each 16-byte read carries 4 consecutive k of
+//     one row, used over 4 k steps); bank conflicts between the rows a warp
+//     reads together are removed by the TMA 32/64/128-byte swizzle instead
+//     of padding, which keeps every vector read 16-byte aligned ("The Final
+//     Kernel", "The Padding Has To Go");
+//   * rows of a lane are interleaved with stride WR and its columns with
+//     stride 4*WC, so that the lanes of a warp read consecutive 16-byte
+//     chunks of B (one wavefront, as in the pages' warptiling argument) and
+//     distinct swizzled chunks of A;
+//   * beta == 0 selects a kernel that never reads C ("The Final Kernel",
+//     "Skipping The Read Of C"); __launch_bounds__(threads, 1) lets the
+//     compiler spend registers on the 128 accumulators ("The Declaration
+//     That Was Worth More Than Any Of It").
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace sg {
+
+struct GemmArgs {
+    int M, N, K;
+    float alpha, beta;
+    float *C;
+    int64_t ldc;
+    int tiles_m, tiles_n, num_tiles;
+    int k_blocks;
+    int group_m;          // rasterisation: tile rows per band
+    uint32_t *err;        // device error word (bounded waits)
+    uint64_t timeout_ns;
+};
+
+template <int KA> struct AVecT;
+template <> struct AVecT<4> { using type = float4; };
+template <> struct AVecT<2> { using type = float2; };
+
+__device__ __forceinline__ float vec_get(const float4 &v, int k) {
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0 ? v.x : v.y; }
+
+template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_,
+          int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4>
+struct FfmaConfig {
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int WR = WR_, WC = 32 / WR_;
+    static constexpr int TM = 8, TN = 16;
+    static constexpr int WTM = WR * TM, WTN = WC * TN;
+    static constexpr int KQ_UNROLL = KQ_UNROLL_;
+    static constexpr int KA = KA_;
+    static constexpr int MIN_CTAS = MIN_CTAS_;
+    static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
+    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    static constexpr int ROW_BYTES_A = BK * 4;                 // one row of the A slice
+    static constexpr int A_STAGE_BYTES = BM * BK * 4;
+    static constexpr int B_STAGE_BYTES = BK * BN * 4;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    // TMA swizzle span equals the A row: 128 B (BK=32), 64 B (BK=16), 32 B (BK=8).
+    static constexpr int SWZ_MASK = ROW_BYTES_A / 16 - 1;      // 7, 3, 1
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+
+    static_assert(BK == 8 || BK == 16 || BK == 32, "A slice row must match a TMA swizzle span");
+    static_assert(WR == 1 || WR == 2 || WR == 4 || WR == 8 || WR == 16 || WR == 32, "WR");
+    static_assert(BM == WARPS_M * WTM && BN == WARPS_N * WTN, "tile / warp grid mismatch");
+    static_assert(WTM * ROW_BYTES_A >= 1024, "warp row block must cover a swizzle period");
+    static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box dimension limit");
+    static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
+    static_assert(KA == 2 || KA == 4, "A vector width");
+    static_assert((BK / KA) % KQ_UNROLL == 0, "unroll must divide the slice");
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int rows = min(tiles_m - first_m, group_m);
+    const int local = t - g * per_group;
+    tm = first_m + local % rows;
+    tn = local / rows;
+}
+
+template <class Cfg, bool BETA_ZERO, bool C_VEC>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
+sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const GemmArgs p)
+{
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, WR = Cfg::WR, WC = Cfg::WC;
+    constexpr int NJ = TN / 4;   // 16-byte column groups per lane
+    constexpr int KA = Cfg::KA;  // k values per vector read of A (4: 16 B, 2: 8 B)
+    using AVec = typename AVecT<KA>::type;
+
+    extern __shared__ unsigned char smem_raw[];
+    // TMA 128-byte swizzle wants 1024-byte aligned destinations.
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sA = smem;
+    unsigned char *sB = smem + STAGES * Cfg::A_STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == Cfg::CONSUMER_WARPS) {
+        // ---------------- producer ----------------
+        if (lane != 0) return;
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                    record_error(p.err, kSiteProducerEmpty);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * BK, tm * BM);
+                tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], tn * BN, kb * BK);
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            // Do not leave the CTA with copies in flight: wait (bounded) for
+            // the most recent loads, which no consumer may ever have taken.
+            const int pending = issued < STAGES ? issued : STAGES;
+            for (int back = 1; back <= pending; ++back) {
+                int s = stage - back;
+                uint32_t ph = phase;
+                if (s < 0) { s += STAGES; ph ^= 1u; }
+                mbar_wait_bounded(&full[s], ph, p.timeout_ns);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int wm = warp / Cfg::WARPS_N;
+    const int wn = warp % Cfg::WARPS_N;
+    const int lr = lane / WC;          // lane row in the warp grid
+    const int lc = lane % WC;          // lane column
+    // Rows of this lane inside the CTA tile: m_i = row0 + WR*i.
+    const int row0 = wm * Cfg::WTM + lr;
+    // Columns: n_j = col0 + 4*WC*j (+0..3).
+    const int col0 = wn * Cfg::WTN + lc * 4;
+    // Swizzle term of row0's A row (rows of other i differ by a constant, see below).
+    const uint32_t a_x0 = ((uint32_t)(lr * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
+    const uint32_t a_row0_off = (uint32_t)row0 * Cfg::ROW_BYTES_A;
+
+    int stage = 0;
+    uint32_t phase = 0;
+
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+
+        float2 acc[TM][TN / 2];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+                record_error(p.err, kSiteConsumerFull);
+                return;
+            }
+            const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
+            const float *Bs = reinterpret_cast<const float *>(sB + stage * Cfg::B_STAGE_BYTES) + col0;
+
+#pragma unroll Cfg::KQ_UNROLL
+            for (int kq = 0; kq < BK / KA; ++kq) {
+                // A: KA consecutive k of each of the lane's 8 rows, one vector
+                // read per row.  Row m_i = row0 + WR*i sits at byte offset
+                // m_i*ROW_BYTES_A; its 16-byte chunk c is stored at chunk
+                // c ^ swz(m_i), and swz(m_i) = a_x0 ^ d_i with d_i a
+                // compile-time constant because lr*ROW_BYTES_A and
+                // WR*i*ROW_BYTES_A occupy disjoint bits.
+                const uint32_t chunk = (uint32_t)(kq * KA) >> 2;
+                const uint32_t within = (uint32_t)(kq * KA * 4) & 15u;
+                const uint32_t kx = chunk ^ a_x0;
+                AVec a[TM];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const uint32_t d_i = ((uint32_t)(WR * i * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
+                    a[i] = *reinterpret_cast<const AVec *>(
+                        As + WR * i * Cfg::ROW_BYTES_A + (((kx ^ d_i) << 4) | within));
+                }
+#pragma unroll
+                for (int kr = 0; kr < KA; ++kr) {
+                    const float *brow = Bs + (kq * KA + kr) * BN;
+                    float4 b[NJ];
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j)
+                        b[j] = *reinterpret_cast<const float4 *>(brow + j * 4 * WC);
+#pragma unroll
+                    for (int i = 0; i < TM; ++i) {
+                        const float av = vec_get(a[i], kr);
+                        const float2 a2 = make_float2(av, av);
+#pragma unroll
+                        for (int j = 0; j < NJ; ++j) {
+                            acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
+                            acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+
+        // ---------------- epilogue ----------------
+        const float alpha = p.alpha;
+        const float beta = p.beta;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int row = tm * BM + row0 + WR * i;
+            if (row >= p.M) continue;
+            float *crow = p.C + (int64_t)row * p.ldc;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int col = tn * BN + col0 + 4 * WC * j;
+                float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+                if (C_VEC && col + 3 < p.N) {
+                    float4 *dst = reinterpret_cast<float4 *>(crow + col);
+                    float4 o;
+                    if constexpr (BETA_ZERO) {
+                        o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                    } else {
+                        const float4 c = *dst;
+                        o = make_float4(fmaf(beta, c.x, alpha * v[0]), fmaf(beta, c.y, alpha * v[1]),
+                                        fmaf(beta, c.z, alpha * v[2]), fmaf(beta, c.w, alpha * v[3]));
+                    }
+                    *dst = o;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (col + q < p.N) {
+                            float *dst = crow + col + q;
+                            if constexpr (BETA_ZERO) *dst = alpha * v[q];
+                            else *dst = fmaf(beta, *dst, alpha * v[q]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+}  // namespace sg

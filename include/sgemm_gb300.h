@@ -1,0 +1,209 @@
+/*
+ * sgemm_gb300.h: C ABI of the FP32 general matrix multiply for NVIDIA GB300
+ * (sm_103a).
+ *
+ *   C = alpha * A . B + beta * C        (FP32 in, FP32 FMA, FP32 out)
+ *
+ * A is M x K, B is K x N, C is M x N, all ROW MAJOR with leading dimensions
+ * (row pitches, in elements) lda >= max(1, K), ldb >= max(1, N),
+ * ldc >= max(1, N).  The operation and its 2MNK FLOP count are the problem
+ * statement of "Matmul I: tiling and shared memory" (notes.ybc.sh cap-07,
+ * section 1); alpha and beta enter in the epilogue as in "2D Register Tiling:
+ * The Outer Product" (maxxfuu article4/page8, "The Kernel"); with beta == 0 C
+ * is not read, as in "The Final Kernel" (maxxfuu article4/page14, "Skipping
+ * The Read Of C").  Those pages give the kernel signature as
+ * (M, N, K, alpha, A, B, beta, C) with the leading dimensions implied by the
+ * shapes; this ABI adds explicit leading dimensions and a stream.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers A, B, C are DEVICE pointers owned by the caller, 4-byte
+ *     aligned.  Unless stated otherwise a call only enqueues work on `stream`
+ *     (0 = legacy default stream) and returns; it neither synchronises nor
+ *     allocates device memory.
+ *   - Quick returns (BLAS conventions; the pages do not discuss them):
+ *       M == 0 or N == 0       -> nothing is done, SUCCESS.
+ *       K == 0 or alpha == 0   -> C = beta * C; A and B are not read.
+ *       beta == 0              -> C is write-only: NaN/Inf already in C never
+ *                                 reach the result.
+ *     Entries of C beyond column N (the ldc padding) are never touched.
+ *   - Results are rounded FP32 sums of FP32 products; the summation order over
+ *     k is fixed for a given shape, so repeated calls give identical bits.
+ *   - Errors are returned, never printed or raised; see sgemmStatus_t.
+ *   - Thread safety: a handle may be used from one host thread at a time.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_API_H__
+typedef struct CUstream_st *cudaStream_t;
+#endif
+
+typedef enum sgemmStatus {
+    SGEMM_STATUS_SUCCESS = 0,
+    SGEMM_STATUS_INVALID_VALUE = 1,      /* bad size, leading dimension, NULL pointer or handle */
+    SGEMM_STATUS_MISALIGNED = 2,         /* A, B or C not 4-byte aligned */
+    SGEMM_STATUS_ARCH_MISMATCH = 3,      /* current device is not compute capability 10.3 */
+    SGEMM_STATUS_WORKSPACE_REQUIRED = 4, /* operands need packing and no (or too small a) workspace is set */
+    SGEMM_STATUS_LAUNCH_FAILED = 5,      /* a CUDA call or kernel launch failed */
+    SGEMM_STATUS_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait expired (sgemmGetDeviceError) */
+    SGEMM_STATUS_NOT_SUPPORTED = 7,      /* sizes beyond what the kernels address (see sgemmEx) */
+    SGEMM_STATUS_INTERNAL_ERROR = 8
+} sgemmStatus_t;
+
+typedef struct sgemmContext *sgemmHandle_t;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *sgemmGetStatusString(sgemmStatus_t status);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+sgemmStatus_t sgemmGetVersion(int *version);
+
+/*
+ * Create a handle bound to the CURRENT device.  Checks that the device is
+ * compute capability 10.3 (ARCH_MISMATCH otherwise), reads its SM count and
+ * allocates the handle's 4-byte device error word: the only device
+ * allocation the library makes, done here and never on the compute path.
+ */
+sgemmStatus_t sgemmCreate(sgemmHandle_t *handle);
+
+/* Release a handle (synchronises its device first).  NULL is a no-op. */
+sgemmStatus_t sgemmDestroy(sgemmHandle_t handle);
+
+/*
+ * Per-device default handle used by sgemm(); created on first use for the
+ * current device and kept until process exit.  Callers may attach a
+ * workspace to it with sgemmSetWorkspace().
+ */
+sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle);
+
+/*
+ * Bytes of device workspace sgemmEx() needs for these operands: 0 when A and
+ * B can be read in place (16-byte aligned base, row pitch a multiple of 16
+ * bytes), else room to repack the operand(s) that cannot into rows padded to
+ * a multiple of 4 floats.  Same validation as sgemmEx().
+ */
+sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t handle, int64_t M, int64_t N,
+                                    int64_t K, const float *A, int64_t lda,
+                                    const float *B, int64_t ldb, size_t *bytes);
+
+/*
+ * Attach caller-owned device memory (256-byte aligned, `bytes` long) as the
+ * handle's workspace; ptr == NULL detaches.  The library reads and writes it
+ * during calls enqueued afterwards; the caller must keep it alive until that
+ * work has finished.
+ */
+sgemmStatus_t sgemmSetWorkspace(sgemmHandle_t handle, void *ptr, size_t bytes);
+
+/*
+ * C = alpha * A . B + beta * C on `stream`, using `handle`'s device,
+ * workspace and error word.  A, B, C: device pointers, row major, leading
+ * dimensions as above.  Returns INVALID_VALUE for negative sizes, leading
+ * dimensions below the minimum, a NULL pointer with nonzero extent, or a
+ * NULL handle; MISALIGNED for pointers that are not 4-byte aligned;
+ * NOT_SUPPORTED for M, N or K >= 2^31 or an operand span of 2^40 bytes or
+ * more; WORKSPACE_REQUIRED when packing is needed (see
+ * sgemmGetWorkspaceSize) and the attached workspace is missing or too small;
+ * LAUNCH_FAILED if a launch is rejected.  Operands may not overlap C.
+ */
+sgemmStatus_t sgemmEx(sgemmHandle_t handle, int64_t M, int64_t N, int64_t K,
+                      float alpha, const float *A, int64_t lda, const float *B,
+                      int64_t ldb, float beta, float *C, int64_t ldc,
+                      cudaStream_t stream);
+
+/* sgemmEx() with the current device's default handle. */
+sgemmStatus_t sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+                    const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace sgemmHostEx() needs: device copies of A, B and C
+ * with rows padded to a multiple of 4 floats.
+ */
+sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K,
+                                     size_t *bytes);
+
+/*
+ * The same product with A, B and C in HOST memory (pinned memory gives full
+ * copy bandwidth; pageable memory works but is staged by the driver).  The
+ * operands are copied into `dev_workspace` (device memory of at least
+ * sgemmHostWorkspaceSize() bytes, owned by the caller), the product runs
+ * there, and the M x N result is copied back into C.  All of it is enqueued
+ * on `stream`; the call returns before the copies finish, so the host
+ * buffers must stay untouched until the stream has been synchronised.
+ * C is read (copied up) only when beta != 0.
+ */
+sgemmStatus_t sgemmHostEx(sgemmHandle_t handle, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float *A_host, int64_t lda,
+                          const float *B_host, int64_t ldb, float beta,
+                          float *C_host, int64_t ldc, void *dev_workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Description of what sgemmEx() would launch for these arguments (no work
+ * is enqueued): the number of kernel launches, the output tile (BM x BN),
+ * the number of CTAs of the main kernel and whether operands are repacked.
+ */
+typedef struct sgemmPlan {
+    int launches;       /* kernels one call enqueues (0 for M == 0 or N == 0) */
+    int tile_m, tile_n; /* output tile of the main kernel (0 if none) */
+    int tile_k;         /* K slice staged per pipeline step */
+    int stages;         /* shared-memory pipeline depth */
+    int ctas;           /* CTAs of the main kernel (persistent grid) */
+    int packs_a, packs_b; /* 1 if the operand is repacked into the workspace */
+    int vector_epilogue;  /* 1 if C is written with 16-byte stores */
+    int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0) */
+} sgemmPlan_t;
+
+sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
+                             int64_t K, float alpha, const float *A,
+                             int64_t lda, const float *B, int64_t ldb,
+                             float beta, const float *C, int64_t ldc,
+                             sgemmPlan_t *plan);
+
+/*
+ * Pin the main kernel's tile configuration for calls on this handle:
+ * 0 = automatic choice by shape (default); 1..4 = a fixed configuration
+ * (1: 128x128x32 tile, 4 stages, 4 compute warps; 2: same tile, 3 stages,
+ * two CTAs per SM; 3: 128x256x32, 8 compute warps; 4: 128x128x16, 6 stages).
+ * Every configuration computes the same result up to summation order.
+ */
+sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
+
+/*
+ * Limit, in nanoseconds, on every wait a kernel of this handle performs
+ * (default 2e9, minimum 1e6).  A wait that runs out records an error in the
+ * handle's error word and lets the kernel return instead of hanging.
+ */
+sgemmStatus_t sgemmSetWaitTimeout(sgemmHandle_t handle, uint64_t timeout_ns);
+
+/*
+ * Synchronise the handle's device, read and clear its error word.  *code is
+ * 0 when no kernel recorded an error; otherwise the return value is
+ * DEVICE_TIMEOUT and *code holds the raw word: bits 24..31 say which wait
+ * expired (1 consumer data wait, 2 producer slot wait, 3 self test), bits
+ * 0..23 the CTA index.
+ */
+sgemmStatus_t sgemmGetDeviceError(sgemmHandle_t handle, int *code);
+
+/*
+ * Health check of the bounded-wait machinery: enqueue one single-CTA kernel
+ * that waits on a shared-memory barrier no one ever arrives on, with limit
+ * timeout_ns.  The wait must run out and record code 3 in the error word;
+ * the kernel then returns normally, so the context stays usable.
+ */
+sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
+                                       uint64_t timeout_ns,
+                                       cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -1,0 +1,309 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Uniform inputs must satisfy |C_gpu - C_ref| <= 1e-3 + 1e-3*|C_ref|
+elementwise; integer-valued inputs in {-4..4} must match bit for bit (every
+FP32 partial sum is exact, so any summation order gives the oracle's value).
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from fp32_sgemm_gb300 import inputs
+from conftest import fp32_tolerance
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp32_sgemm_gb300 as m
+    m.build()
+    return m
+
+
+@pytest.fixture(scope="module")
+def handle(sg):
+    return sg.Handle()
+
+
+def _to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _gpu(sg, handle, p, C_init=None, algo=0):
+    """Run the problem on the GPU; returns the full [M, ldc] C buffer on the host."""
+    A = _to_dev(p.A)[:, : p.K] if p.K > 0 else torch.zeros((p.M, 0), device="cuda")
+    B = _to_dev(p.B)[:, : p.N]
+    if C_init is None:
+        C_init = p.C0 if p.C0 is not None else np.full((p.M, p.N), np.nan, np.float32)
+    Cbuf = _to_dev(C_init)
+    C = Cbuf[:, : p.N]
+    handle.set_algo(algo)
+    handle.gemm(A, B, C, p.alpha, p.beta)
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    return Cbuf.cpu().numpy()
+
+
+def _assert_close(got, ref):
+    err = np.abs(got.astype(np.float64) - ref)
+    tol = fp32_tolerance(ref)
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{int(bad.sum())} entries out of tolerance; worst ratio "
+                           f"{float(np.nanmax(err / tol)):.3g}")
+    return float(np.max(err / tol)) if err.size else 0.0
+
+
+def _ref(p, threads=0):
+    return oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0, threads=threads)
+
+
+FULL = ["sgemm_128", "sgemm_1024", "sgemm_4096", "sgemm_4095x4097x1023"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_uniform_full(sg, handle, name):
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_problem(w, "uniform")
+    got = _gpu(sg, handle, p)[:, : p.N]
+    ratio = _assert_close(got, _ref(p))
+    assert ratio < 0.5
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_integer_twin_bit_exact(sg, handle, name):
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_problem(w, "integer")
+    got = _gpu(sg, handle, p)[:, : p.N]
+    np.testing.assert_array_equal(got.astype(np.float64), _ref(p))
+
+
+def _sampled_8192(sg, handle, kind):
+    w = inputs.WORKLOADS["sgemm_8192"]
+    p = inputs.workload_problem(w, kind)
+    A = _to_dev(p.A)
+    B = _to_dev(p.B)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    handle.set_algo(0)
+    handle.gemm(A, B, C, w.alpha, w.beta)
+    rows, cols = inputs.sample_entries(w.M, w.N, w.samples, w.seed)
+    got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+    assert handle.device_error() == 0
+    ref = oracle.sgemm_ref_entries(w.K, w.alpha, p.A, p.B, rows, cols, w.beta, p.C0)
+    return got, ref
+
+
+def test_workload_8192_sampled_uniform(sg, handle):
+    got, ref = _sampled_8192(sg, handle, "uniform")
+    _assert_close(got, ref)
+
+
+def test_workload_8192_sampled_integer_bit_exact(sg, handle):
+    got, ref = _sampled_8192(sg, handle, "integer")
+    np.testing.assert_array_equal(got.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("algo", [1, 2, 3, 4])
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
+def test_every_tile_configuration(sg, handle, algo, shape):
+    M, N, K = shape
+    p = inputs.make_problem(M, N, K, seed=40 + algo, alpha=0.5, beta=0.25)
+    _assert_close(_gpu(sg, handle, p, algo=algo)[:, :N], _ref(p))
+    q = inputs.make_problem(M, N, K, seed=1040 + algo, kind="integer", alpha=0.5, beta=0.25)
+    np.testing.assert_array_equal(_gpu(sg, handle, q, algo=algo)[:, :N].astype(np.float64), _ref(q))
+
+
+_SMALL = [1, 2, 3, 5, 8, 9]
+_EDGES = [15, 16, 17, 31, 32, 33, 127, 128, 129]
+
+
+def test_tiny_shapes_integer_exact(sg, handle):
+    for M, N, K in itertools.product(_SMALL, _SMALL, _SMALL):
+        p = inputs.make_problem(M, N, K, seed=M * 97 + N * 13 + K, kind="integer",
+                                alpha=1.0, beta=0.5, with_c=True,
+                                lda=K + (M % 3), ldb=N + (K % 2), ldc=N + 1)
+        got = _gpu(sg, handle, p)
+        np.testing.assert_array_equal(got[:, :N].astype(np.float64), _ref(p),
+                                      err_msg=f"shape {(M, N, K)}")
+        assert np.isnan(got[:, N:]).all(), "ldc padding was written"
+
+
+def test_edge_shapes_uniform(sg, handle):
+    for M, N, K in itertools.product(_EDGES[::2], _EDGES[1::2], _EDGES):
+        p = inputs.make_problem(M, N, K, seed=M + 7 * N + 11 * K, alpha=-1.25, beta=0.75)
+        _assert_close(_gpu(sg, handle, p)[:, :N], _ref(p))
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
+    (255, 257, 129, 132, 260, 264),       # 16-byte pitches, ragged sizes
+    (257, 255, 131, 131, 255, 255),       # odd pitches: A and B repacked, scalar C
+    (130, 126, 64, 68, 127, 129),         # A in place, B repacked, scalar C
+    (129, 131, 513, 515, 132, 136),       # A repacked, B in place, vector C
+])
+def test_leading_dimensions_and_packing(sg, handle, M, N, K, lda, ldb, ldc):
+    p = inputs.make_problem(M, N, K, seed=M * N, alpha=1.5, beta=-0.5, lda=lda, ldb=ldb, ldc=ldc)
+    got = _gpu(sg, handle, p)
+    _assert_close(got[:, :N], _ref(p))
+    assert np.isnan(got[:, N:]).all()
+    q = inputs.make_problem(M, N, K, seed=M * N + 1, kind="integer", alpha=1.5, beta=-0.5,
+                            lda=lda, ldb=ldb, ldc=ldc)
+    np.testing.assert_array_equal(_gpu(sg, handle, q)[:, :N].astype(np.float64), _ref(q))
+
+
+def test_unaligned_base_pointers(sg, handle):
+    # Views that start one float into their buffers: 4-byte but not 16-byte
+    # aligned, so A and B are repacked and C is written with scalar stores.
+    M, N, K = 200, 190, 170
+    p = inputs.make_problem(M, N, K, seed=77, alpha=1.0, beta=1.0)
+    Ab = torch.zeros(M * K + 1, device="cuda")
+    Bb = torch.zeros(K * N + 1, device="cuda")
+    Cb = torch.zeros(M * N + 1, device="cuda")
+    A = Ab[1:].view(M, K); A.copy_(torch.from_numpy(p.A))
+    B = Bb[1:].view(K, N); B.copy_(torch.from_numpy(p.B))
+    C = Cb[1:].view(M, N); C.copy_(torch.from_numpy(p.C0))
+    plan = handle.plan(A, B, C, 1.0, 1.0)
+    assert plan["packs_a"] == 1 and plan["packs_b"] == 1 and plan["vector_epilogue"] == 0
+    handle.set_algo(0)
+    handle.gemm(A, B, C, 1.0, 1.0)
+    _assert_close(C.cpu().numpy(), _ref(p))
+    assert float(Cb[0]) == 0.0
+
+
+def test_beta_zero_never_reads_c(sg, handle):
+    p = inputs.make_problem(300, 260, 100, seed=5)
+    got = _gpu(sg, handle, p, C_init=np.full((300, 260), np.nan, np.float32))
+    assert np.isfinite(got).all()
+    _assert_close(got, _ref(p))
+
+
+def test_alpha_zero_and_k_zero(sg, handle):
+    p = inputs.make_problem(70, 90, 30, seed=6, alpha=0.0, beta=-2.0)
+    A = torch.full((70, 30), float("nan"), device="cuda")
+    B = torch.full((30, 90), float("nan"), device="cuda")
+    C = _to_dev(p.C0)
+    handle.gemm(A, B, C, 0.0, -2.0)
+    np.testing.assert_array_equal(C.cpu().numpy(), -2.0 * p.C0)
+    C = _to_dev(p.C0)
+    handle.gemm(torch.zeros((70, 0), device="cuda"), torch.zeros((0, 90), device="cuda"), C, 3.0, 0.0)
+    np.testing.assert_array_equal(C.cpu().numpy(), np.zeros((70, 90), np.float32))
+
+
+def test_empty_output_untouched(sg, handle):
+    C = torch.full((0, 5), 1.0, device="cuda")
+    handle.gemm(torch.zeros((0, 3), device="cuda"), torch.zeros((3, 5), device="cuda"), C)
+    C = torch.full((4, 0), 1.0, device="cuda")
+    handle.gemm(torch.zeros((4, 3), device="cuda"), torch.zeros((3, 0), device="cuda"), C)
+    torch.cuda.synchronize()
+
+
+def test_guard_bands_untouched(sg, handle):
+    # C lives inside a larger canary-filled buffer: rows above/below, columns
+    # past N (ldc padding) must keep their exact bit patterns.
+    M, N, K, ldc = 257, 250, 96, 260
+    canary = np.frombuffer(np.uint32(0x7FC0BEEF).tobytes() * ((M + 8) * ldc),
+                           dtype=np.float32).reshape(M + 8, ldc).copy()
+    p = inputs.make_problem(M, N, K, seed=8, alpha=1.0, beta=0.5, with_c=True)
+    canary[4:4 + M, :N] = p.C0[:, :N]
+    buf = _to_dev(canary)
+    C = buf[4:4 + M, :N]
+    handle.set_algo(0)
+    handle.gemm(_to_dev(p.A), _to_dev(p.B), C, 1.0, 0.5)
+    out = buf.cpu().numpy()
+    mask = np.ones(out.shape, bool)
+    mask[4:4 + M, :N] = False
+    assert (out.view(np.uint32)[mask] == 0x7FC0BEEF).all()
+    _assert_close(out[4:4 + M, :N], _ref(p))
+
+
+def test_identity_and_permutation_exact(sg, handle):
+    n, N = 384, 200
+    p = inputs.make_problem(n, N, n, seed=9)
+    eye = np.eye(n, dtype=np.float32)
+    C = torch.empty((n, N), device="cuda")
+    handle.gemm(_to_dev(eye), _to_dev(p.B), C)
+    np.testing.assert_array_equal(C.cpu().numpy(), p.B)
+    perm = np.random.default_rng(1).permutation(n)
+    P = np.zeros((n, n), np.float32)
+    P[np.arange(n), perm] = 1.0
+    handle.gemm(_to_dev(P), _to_dev(p.B), C)
+    np.testing.assert_array_equal(C.cpu().numpy(), p.B[perm])
+
+
+def test_repeated_calls_bitwise_identical(sg, handle):
+    p = inputs.make_problem(1024, 1024, 1024, seed=10)
+    A, B = _to_dev(p.A), _to_dev(p.B)
+    handle.set_algo(0)
+    first = torch.empty((1024, 1024), device="cuda")
+    handle.gemm(A, B, first)
+    C = torch.empty_like(first)
+    for _ in range(30):
+        handle.gemm(A, B, C)
+        assert torch.equal(C.view(torch.int32), first.view(torch.int32))
+
+
+def test_non_default_stream(sg, handle):
+    p = inputs.make_problem(512, 384, 256, seed=11, beta=1.0)
+    s = torch.cuda.Stream()
+    A, B, C = _to_dev(p.A), _to_dev(p.B), _to_dev(p.C0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        handle.gemm(A, B, C, 1.0, 1.0, stream=s)
+    s.synchronize()
+    _assert_close(C.cpu().numpy(), _ref(p))
+
+
+def test_default_handle_entry_point(sg):
+    p = inputs.make_problem(640, 320, 200, seed=12)
+    C = sg.sgemm(_to_dev(p.A), _to_dev(p.B))
+    torch.cuda.synchronize()
+    _assert_close(C.cpu().numpy(), _ref(p))
+
+
+def test_workspace_required_without_workspace(sg):
+    import ctypes
+    lib = sg.load_library()
+    h = sg.Handle()
+    A = torch.zeros(100 * 33, device="cuda")
+    B = torch.zeros(33 * 64, device="cuda")
+    C = torch.zeros(100 * 64, device="cuda")
+    st = lib.sgemmEx(h.ptr, 100, 64, 33, 1.0, A.data_ptr(), 33, B.data_ptr(), 64, 0.0,
+                     C.data_ptr(), 64, None)
+    assert st == sg.Status.WORKSPACE_REQUIRED
+    n = ctypes.c_size_t()
+    assert lib.sgemmGetWorkspaceSize(h.ptr, 100, 64, 33, A.data_ptr(), 33, B.data_ptr(), 64,
+                                     ctypes.byref(n)) == 0
+    assert n.value == (100 * 36 * 4 + 255) // 256 * 256
+    h.close()
+
+
+def test_host_buffer_entry_point(sg, handle):
+    M, N, K = 1000, 777, 333
+    p = inputs.make_problem(M, N, K, seed=13, alpha=0.5, beta=0.25)
+    A = torch.from_numpy(p.A).pin_memory()
+    B = torch.from_numpy(p.B).pin_memory()
+    C = torch.from_numpy(p.C0.copy()).pin_memory()
+    ws = torch.empty(sg.host_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    sg.sgemm_host(A, B, C, 0.5, 0.25, workspace=ws, handle=handle)
+    torch.cuda.synchronize()
+    _assert_close(C.numpy(), _ref(p))
+
+
+def test_bounded_wait_self_test_reports_timeout(sg):
+    h = sg.Handle()
+    assert h.device_error() == 0
+    h.selftest_wait_timeout(50_000_000)          # 50 ms, nothing ever arrives
+    code = h.device_error()
+    assert code >> 24 == 3
+    assert h.device_error() == 0                 # reading cleared it
+    # The context is still usable afterwards.
+    p = inputs.make_problem(256, 256, 256, seed=14, kind="integer")
+    C = torch.empty((256, 256), device="cuda")
+    h.gemm(_to_dev(p.A), _to_dev(p.B), C)
+    np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), _ref(p))
+    h.close()
