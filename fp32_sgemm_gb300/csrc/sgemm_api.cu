@@ -38,6 +38,10 @@ void init_kernel_table() {
     sg::fill_algo2(g_kernels[1]);
     sg::fill_algo3(g_kernels[2]);
     sg::fill_algo4(g_kernels[3]);
+    sg::fill_algo5(g_kernels[4]);
+    sg::fill_algo6(g_kernels[5]);
+    sg::fill_algo7(g_kernels[6]);
+    sg::fill_algo8(g_kernels[7]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

@@ -69,8 +69,19 @@ __device__ __forceinline__ float vec_get(const float4 &v, int k) {
 }
 __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0 ? v.x : v.y; }
 
+// Tile configuration.
+//   BM x BN output tile, BK-wide K slices, STAGES-deep shared-memory ring;
+//   WARPS_M x WARPS_N consumer warps, each lane an 8 x 16 register tile
+//   (lane grid WR x (32/WR) inside a warp);
+//   KA: k values per vector read of A (4 -> 16 B, 2 -> 8 B);
+//   PRODUCER_WARP: 1 = a dedicated TMA warp, 0 = thread 0 of the first
+//   consumer warp issues the loads (no extra warp, so two CTAs fit per SM);
+//   PIPE: 1 = fragments of the next k are read while this k's FMAs run
+//   (explicit register double buffering), 0 = left to the compiler;
+//   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2).
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_,
-          int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4>
+          int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4, int PRODUCER_WARP_ = 1,
+          int PIPE_ = 0>
 struct FfmaConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -78,10 +89,12 @@ struct FfmaConfig {
     static constexpr int TM = 8, TN = 16;
     static constexpr int WTM = WR * TM, WTN = WC * TN;
     static constexpr int KQ_UNROLL = KQ_UNROLL_;
-    static constexpr int KA = KA_;
     static constexpr int MIN_CTAS = MIN_CTAS_;
+    static constexpr int KA = KA_;
+    static constexpr bool PRODUCER_WARP = PRODUCER_WARP_ != 0;
+    static constexpr bool PIPE = PIPE_ != 0;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    static constexpr int THREADS = (CONSUMER_WARPS + (PRODUCER_WARP ? 1 : 0)) * 32;
     static constexpr int ROW_BYTES_A = BK * 4;                 // one row of the A slice
     static constexpr int A_STAGE_BYTES = BM * BK * 4;
     static constexpr int B_STAGE_BYTES = BK * BN * 4;
@@ -89,6 +102,7 @@ struct FfmaConfig {
     // TMA swizzle span equals the A row: 128 B (BK=32), 64 B (BK=16), 32 B (BK=8).
     static constexpr int SWZ_MASK = ROW_BYTES_A / 16 - 1;      // 7, 3, 1
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+    static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
 
     static_assert(BK == 8 || BK == 16 || BK == 32, "A slice row must match a TMA swizzle span");
     static_assert(WR == 1 || WR == 2 || WR == 4 || WR == 8 || WR == 16 || WR == 32, "WR");
@@ -97,7 +111,9 @@ struct FfmaConfig {
     static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box dimension limit");
     static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(KA == 2 || KA == 4, "A vector width");
-    static_assert((BK / KA) % KQ_UNROLL == 0, "unroll must divide the slice");
+    static_assert(NKQ % KQ_UNROLL == 0, "unroll must divide the slice");
+    static_assert(!PIPE || KQ_UNROLL % 2 == 0, "pipelined fragments alternate two buffers");
+    static_assert(STAGES >= 2, "ring depth");
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
@@ -111,6 +127,41 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = local / rows;
 }
 
+// The sequence of K slices a CTA loads: all slices of its tiles, in order.
+// Slice number g (counted from 0 across tiles) goes to stage g % STAGES and
+// completes phase (g / STAGES) & 1 of that stage's barriers.
+struct SliceCursor {
+    int t, kb;       // tile and K slice of the next load
+    int g;           // its slice number
+};
+
+template <class Cfg>
+__device__ __forceinline__ bool issue_slice(SliceCursor &c, const GemmArgs &p,
+                                            const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                            unsigned char *sA, unsigned char *sB,
+                                            uint64_t *full, uint64_t *empty) {
+    const int stage = c.g % Cfg::STAGES;
+    const uint32_t phase = (uint32_t)(c.g / Cfg::STAGES) & 1u;
+    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) return false;
+    int tm, tn;
+    tile_coords(c.t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+    tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, tmA, &full[stage], c.kb * Cfg::BK, tm * Cfg::BM);
+    tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, tmB, &full[stage], tn * Cfg::BN, c.kb * Cfg::BK);
+    ++c.g;
+    if (++c.kb == p.k_blocks) { c.kb = 0; c.t += gridDim.x; }
+    return true;
+}
+
+// Wait (bounded) until slices [from, to) have landed, so that a CTA that
+// gives up never exits with its own TMA copies still in flight.
+template <class Cfg>
+__device__ __forceinline__ void drain_slices(int from, int to, uint64_t *full, uint64_t timeout_ns) {
+    if (from < to - Cfg::STAGES) from = to - Cfg::STAGES;
+    for (int g = from; g < to; ++g)
+        mbar_wait_bounded(&full[g % Cfg::STAGES], (uint32_t)(g / Cfg::STAGES) & 1u, timeout_ns);
+}
+
 template <class Cfg, bool BETA_ZERO, bool C_VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -121,12 +172,14 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int TM = Cfg::TM, TN = Cfg::TN, WR = Cfg::WR, WC = Cfg::WC;
     constexpr int NJ = TN / 4;   // 16-byte column groups per lane
     constexpr int KA = Cfg::KA;  // k values per vector read of A (4: 16 B, 2: 8 B)
+    constexpr int NKQ = Cfg::NKQ;
     using AVec = typename AVecT<KA>::type;
 
     extern __shared__ unsigned char smem_raw[];
-    // TMA 128-byte swizzle wants 1024-byte aligned destinations.
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // TMA 128-byte swizzle wants 1024-byte aligned destinations.  Offsetting
+    // the __shared__ array itself keeps the pointer in the shared window.
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    unsigned char *smem = smem_raw + pad;
     unsigned char *sA = smem;
     unsigned char *sB = smem + STAGES * Cfg::A_STAGE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
@@ -144,46 +197,44 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     __syncthreads();
 
-    if (warp == Cfg::CONSUMER_WARPS) {
-        // ---------------- producer ----------------
-        if (lane != 0) return;
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+    const int slices_total = [&] {
+        const int my_tiles = p.num_tiles > (int)blockIdx.x
+                                 ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        return my_tiles * p.k_blocks;
+    }();
+
+    if constexpr (Cfg::PRODUCER_WARP) {
+        if (warp == Cfg::CONSUMER_WARPS) {
+            // ---------------- dedicated producer warp ----------------
+            if (lane != 0) return;
+            prefetch_tensormap(&tmA);
+            prefetch_tensormap(&tmB);
+            SliceCursor cur{(int)blockIdx.x, 0, 0};
+            while (cur.g < slices_total) {
+                if (!issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
-                    ok = false;
-                    break;
+                    // No consumer may ever take the most recent slices.
+                    drain_slices<Cfg>(0, cur.g, full, p.timeout_ns);
+                    return;
                 }
-                mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, &tmA, &full[stage], kb * BK, tm * BM);
-                tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, &tmB, &full[stage], tn * BN, kb * BK);
-                ++issued;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            return;
         }
-        if (!ok) {
-            // Do not leave the CTA with copies in flight: wait (bounded) for
-            // the most recent loads, which no consumer may ever have taken.
-            const int pending = issued < STAGES ? issued : STAGES;
-            for (int back = 1; back <= pending; ++back) {
-                int s = stage - back;
-                uint32_t ph = phase;
-                if (s < 0) { s += STAGES; ph ^= 1u; }
-                mbar_wait_bounded(&full[s], ph, p.timeout_ns);
-            }
-        }
-        return;
     }
 
     // ---------------- consumers ----------------
+    // Inline producer: thread 0 issues the first STAGES slices up front, then
+    // after consuming slice g (g >= 1) refills the stage of slice g - 1, which
+    // every warp has released by the time thread 0 is done with slice g.
+    const bool producer = !Cfg::PRODUCER_WARP && threadIdx.x == 0;
+    SliceCursor cur{(int)blockIdx.x, 0, 0};
+    if (producer) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        while (cur.g < slices_total && cur.g < STAGES)
+            issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty);   // fresh stages: never waits
+    }
+
     const int wm = warp / Cfg::WARPS_N;
     const int wn = warp % Cfg::WARPS_N;
     const int lr = lane / WC;          // lane row in the warp grid
@@ -192,71 +243,117 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     const int row0 = wm * Cfg::WTM + lr;
     // Columns: n_j = col0 + 4*WC*j (+0..3).
     const int col0 = wn * Cfg::WTN + lc * 4;
-    // Swizzle term of row0's A row (rows of other i differ by a constant, see below).
+    // Swizzle term of row0's A row; rows of other i differ by a compile-time
+    // constant d_i because lr*ROW_BYTES_A and WR*i*ROW_BYTES_A occupy disjoint bits.
     const uint32_t a_x0 = ((uint32_t)(lr * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
     const uint32_t a_row0_off = (uint32_t)row0 * Cfg::ROW_BYTES_A;
 
-    int stage = 0;
-    uint32_t phase = 0;
+    // A: KA consecutive k of each of the lane's 8 rows, one vector read per
+    // row.  Row m_i's 16-byte chunk c is stored at chunk c ^ swz(m_i).
+    auto load_a = [&](const unsigned char *As, int kq, AVec (&a)[TM]) {
+        const uint32_t chunk = (uint32_t)(kq * KA) >> 2;
+        const uint32_t within = (uint32_t)(kq * KA * 4) & 15u;
+        const uint32_t kx = chunk ^ a_x0;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const uint32_t d_i = ((uint32_t)(WR * i * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
+            a[i] = *reinterpret_cast<const AVec *>(
+                As + WR * i * Cfg::ROW_BYTES_A + (((kx ^ d_i) << 4) | within));
+        }
+    };
+    // B: 16 values of row k, in 4 groups of 4 consecutive columns.
+    auto load_b = [&](const float *Bs, int k, float4 (&b)[NJ]) {
+        const float *brow = Bs + k * BN;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4 *>(brow + j * 4 * WC);
+    };
 
+    float2 acc[TM][TN / 2];
+    auto fma_k = [&](const AVec (&a)[TM], int kr, const float4 (&b)[NJ]) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const float av = vec_get(a[i], kr);
+            const float2 a2 = make_float2(av, av);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
+                acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
+            }
+        }
+    };
+
+    int g = 0;   // slice number being consumed
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         int tm, tn;
         tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
 
-        float2 acc[TM][TN / 2];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+            const int stage = g % STAGES;
+            if (!mbar_wait_bounded(&full[stage], (uint32_t)(g / STAGES) & 1u, p.timeout_ns)) {
                 record_error(p.err, kSiteConsumerFull);
+                if (producer) drain_slices<Cfg>(g, cur.g, full, p.timeout_ns);
                 return;
             }
             const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
             const float *Bs = reinterpret_cast<const float *>(sB + stage * Cfg::B_STAGE_BYTES) + col0;
 
-#pragma unroll Cfg::KQ_UNROLL
-            for (int kq = 0; kq < BK / KA; ++kq) {
-                // A: KA consecutive k of each of the lane's 8 rows, one vector
-                // read per row.  Row m_i = row0 + WR*i sits at byte offset
-                // m_i*ROW_BYTES_A; its 16-byte chunk c is stored at chunk
-                // c ^ swz(m_i), and swz(m_i) = a_x0 ^ d_i with d_i a
-                // compile-time constant because lr*ROW_BYTES_A and
-                // WR*i*ROW_BYTES_A occupy disjoint bits.
-                const uint32_t chunk = (uint32_t)(kq * KA) >> 2;
-                const uint32_t within = (uint32_t)(kq * KA * 4) & 15u;
-                const uint32_t kx = chunk ^ a_x0;
-                AVec a[TM];
+            if constexpr (Cfg::PIPE) {
+                // Register double buffering: while the FMAs of k run, the B
+                // values of k+1 (and, one k ahead of need, the next A group)
+                // are read into the other buffer.  Loop iterations cover
+                // KQ_UNROLL groups so the buffer roles are compile-time.
+                AVec a0[TM], a1[TM];
+                float4 b0[NJ], b1[NJ];
+                load_a(As, 0, a0);
+                load_b(Bs, 0, b0);
+                constexpr int KSTEPS = Cfg::KQ_UNROLL * KA;
+#pragma unroll 1
+                for (int kq0 = 0; kq0 < NKQ; kq0 += Cfg::KQ_UNROLL) {
+                    const bool more = kq0 + Cfg::KQ_UNROLL < NKQ;
 #pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const uint32_t d_i = ((uint32_t)(WR * i * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
-                    a[i] = *reinterpret_cast<const AVec *>(
-                        As + WR * i * Cfg::ROW_BYTES_A + (((kx ^ d_i) << 4) | within));
-                }
+                    for (int u = 0; u < Cfg::KQ_UNROLL; ++u) {
+                        AVec (&ac)[TM] = (u & 1) ? a1 : a0;
+                        AVec (&an)[TM] = (u & 1) ? a0 : a1;
 #pragma unroll
-                for (int kr = 0; kr < KA; ++kr) {
-                    const float *brow = Bs + (kq * KA + kr) * BN;
-                    float4 b[NJ];
-#pragma unroll
-                    for (int j = 0; j < NJ; ++j)
-                        b[j] = *reinterpret_cast<const float4 *>(brow + j * 4 * WC);
-#pragma unroll
-                    for (int i = 0; i < TM; ++i) {
-                        const float av = vec_get(a[i], kr);
-                        const float2 a2 = make_float2(av, av);
-#pragma unroll
-                        for (int j = 0; j < NJ; ++j) {
-                            acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
-                            acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
+                        for (int kr = 0; kr < KA; ++kr) {
+                            const int ks = u * KA + kr;                 // k step inside the iteration
+                            float4 (&bc)[NJ] = (ks & 1) ? b1 : b0;
+                            float4 (&bn)[NJ] = (ks & 1) ? b0 : b1;
+                            const bool last = ks == KSTEPS - 1;
+                            if (!last || more) load_b(Bs, kq0 * KA + ks + 1, bn);
+                            if (kr == KA - 2 && (u + 1 < Cfg::KQ_UNROLL || more))
+                                load_a(As, kq0 + u + 1, an);
+                            fma_k(ac, kr, bc);
                         }
+                    }
+                }
+            } else {
+#pragma unroll Cfg::KQ_UNROLL
+                for (int kq = 0; kq < NKQ; ++kq) {
+                    AVec a[TM];
+                    load_a(As, kq, a);
+#pragma unroll
+                    for (int kr = 0; kr < KA; ++kr) {
+                        float4 b[NJ];
+                        load_b(Bs, kq * KA + kr, b);
+                        fma_k(a, kr, b);
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (producer && g >= 1 && cur.g < slices_total) {
+                if (!issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty)) {
+                    record_error(p.err, kSiteProducerEmpty);
+                    drain_slices<Cfg>(g + 1, cur.g, full, p.timeout_ns);
+                    return;
+                }
+            }
         }
 
         // ---------------- epilogue ----------------

@@ -169,10 +169,11 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
 
 /*
  * Pin the main kernel's tile configuration for calls on this handle:
- * 0 = automatic choice by shape (default); 1..4 = a fixed configuration
- * (1: 128x128x32 tile, 4 stages, 4 compute warps; 2: same tile, 3 stages,
- * two CTAs per SM; 3: 128x256x32, 8 compute warps; 4: 128x128x16, 6 stages).
- * Every configuration computes the same result up to summation order.
+ * 0 = automatic choice by shape (default); 1..8 = a fixed configuration of
+ * the 128 x 128 output tile (K slice 16 or 32, 3 or 4 pipeline stages, a
+ * dedicated TMA warp or TMA issued by a compute thread, one or two CTAs per
+ * SM; see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  Every configuration
+ * computes the same result up to summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
 
