@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sgemm_4096", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--algo", type=int, default=0, help="tile configuration (0 = automatic)")
+    ap.add_argument("--schedule", type=int, default=0,
+                    help="0 automatic, 1 whole tiles per CTA, 2 stream-K")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -224,6 +226,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     sg.load_library(build_if_missing=True)
     handle = sg.Handle(dev)
     handle.set_algo(args.algo)
+    handle.set_schedule(args.schedule)
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     l2_bytes = getattr(props, "L2_cache_size", 0) or 0
@@ -351,7 +354,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "config": dict(workload_config(
             w, f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB "
                f"(> {l2_bytes / 1e6:.0f} MB L2)"),
-            algo=args.algo, tile=f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+            algo=args.algo, schedule="stream-K" if plan["stream_k"] else "whole tiles",
+            tile=f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
             stages=plan["stages"], ctas=plan["ctas"], parallelism=f"replicas x{world}"),
         "roofline": roofline,
         "cpu_baseline": cpu,

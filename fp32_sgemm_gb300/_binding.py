@@ -43,7 +43,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("tile_k", ctypes.c_int), ("stages", ctypes.c_int), ("ctas", ctypes.c_int),
                 ("packs_a", ctypes.c_int), ("packs_b", ctypes.c_int),
-                ("vector_epilogue", ctypes.c_int), ("kind", ctypes.c_int)]
+                ("vector_epilogue", ctypes.c_int), ("kind", ctypes.c_int),
+                ("stream_k", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -67,6 +68,7 @@ SIGNATURES = {
     "sgemmQueryPlan": (_st, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                              ctypes.POINTER(Plan)]),
     "sgemmSetAlgo": (_st, [_vp, ctypes.c_int]),
+    "sgemmSetSchedule": (_st, [_vp, ctypes.c_int]),
     "sgemmSetWaitTimeout": (_st, [_vp, ctypes.c_uint64]),
     "sgemmGetDeviceError": (_st, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "sgemmSelfTestWaitTimeout": (_st, [_vp, ctypes.c_uint64, _vp]),
@@ -184,6 +186,10 @@ class Handle:
 
     def set_algo(self, algo: int):
         _check(self._lib.sgemmSetAlgo(self._h, int(algo)), "sgemmSetAlgo")
+
+    def set_schedule(self, schedule: int):
+        """0 automatic, 1 whole tiles per CTA, 2 stream-K when it applies."""
+        _check(self._lib.sgemmSetSchedule(self._h, int(schedule)), "sgemmSetSchedule")
 
     def set_wait_timeout(self, ns: int):
         _check(self._lib.sgemmSetWaitTimeout(self._h, int(ns)), "sgemmSetWaitTimeout")

@@ -66,8 +66,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Global-memory flag used between CTAs: release store / acquire load at GPU scope.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait for a global flag to become nonzero (the CTAs involved are
+// all resident: the persistent grid never exceeds one wave).
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *p, uint64_t timeout_ns) {
+    if (ld_acquire_gpu(p) != 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) != 0) return true;
+        if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return false;
+}
+
 // Error word layout: bits 24..31 = which wait expired, bits 0..23 = CTA index.
-enum WaitSite : uint32_t { kSiteConsumerFull = 1, kSiteProducerEmpty = 2, kSiteSelfTest = 3 };
+enum WaitSite : uint32_t {
+    kSiteConsumerFull = 1, kSiteProducerEmpty = 2, kSiteSelfTest = 3,
+    kSiteStreamKFlag = 4, kSiteCtaSync = 5
+};
 
 __device__ __forceinline__ void record_error(uint32_t *err, uint32_t site) {
     if (err != nullptr)

@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -69,6 +70,7 @@ struct sgemmContext {
     size_t ws_bytes = 0;
     uint64_t timeout_ns = kDefaultTimeoutNs;
     int algo = 0;
+    int schedule = 0;   // 0 automatic, 1 whole tiles only, 2 stream-K whenever it applies
 };
 
 namespace {
@@ -109,8 +111,11 @@ struct Plan {
     int algo_index = -1;   // row of g_kernels
     int variant = 0;       // column of g_kernels
     int64_t lda_p = 0, ldb_p = 0;
-    size_t ws_a = 0, ws_b = 0;
+    size_t ws_a = 0, ws_b = 0;      // repacked A / B
+    size_t ws_flags = 0, ws_partials = 0;   // stream-K scratch (0 when not used)
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 8;
+    int k_blocks = 0;
+    int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
 };
 
 int choose_algo(const sgemmContext *h, int64_t M, int64_t N, int64_t K) {
@@ -135,7 +140,9 @@ int occupancy_for(const sgemmContext *h, KernelEntry &e) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Host-only part of the plan (no CUDA calls).
+// Plan of one call: repacking, kernel variant, grid and stream-K split.
+// Queries the kernel's occupancy once per device (a CUDA call); everything
+// else is host arithmetic.
 sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
                         const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                         const float *C, int64_t ldc, Plan &pl) {
@@ -157,12 +164,29 @@ sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, 
     pl.ws_b = pl.pub.packs_b ? align256(size_t(K) * size_t(pl.ldb_p) * 4) : 0;
     pl.algo_index = choose_algo(h, M, N, K);
     pl.variant = (beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
-    const KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
+    KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
     pl.tiles_m = int(ceil_div(M, e.bm));
     pl.tiles_n = int(ceil_div(N, e.bn));
     const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n;
     if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.num_tiles = int(tiles);
+    pl.k_blocks = int(ceil_div(K, e.bk));
+    const int occ = occupancy_for(h, e);
+    if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
+    const int64_t slots = int64_t(h->sm_count) * occ;
+    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, slots));
+    // Whole tiles leave the SMs unevenly loaded when the tile count is not a
+    // multiple of the SM count (the last wave is partial).  Stream-K gives
+    // every resident CTA the same number of (tile, K slice) units instead.
+    const double per_sm = double(pl.num_tiles) / h->sm_count;
+    const double dp_eff = per_sm / std::ceil(per_sm);
+    const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
+    const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
+    if (want_sk && pl.k_blocks >= 2 && units >= slots && units < kMaxDim) {
+        pl.sk_ctas = int(slots);
+        pl.ws_flags = align256(size_t(slots) * 4);
+        pl.ws_partials = size_t(slots) * size_t(e.bm) * size_t(e.bn) * 4;
+    }
     pl.pub.tile_m = e.bm;
     pl.pub.tile_n = e.bn;
     pl.pub.tile_k = e.bk;
@@ -216,6 +240,9 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
     }
 
     const float *Ause = A, *Buse = B;
+    // Stream-K scratch is optional: without room for it, whole tiles are used.
+    const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
+                        h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
     if (pl.pub.packs_a || pl.pub.packs_b) {
         if (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b) return SGEMM_STATUS_WORKSPACE_REQUIRED;
         char *ws = static_cast<char *>(h->ws);
@@ -234,8 +261,6 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
     }
 
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
-    const int occ = occupancy_for(h, e);
-    if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
 
     CUtensorMap tmA, tmB;
     st = encode_2d(&tmA, Ause, K, M, pl.lda_p, e.bk, e.bm, swizzle_for_bk(e.bk));
@@ -254,12 +279,22 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
     args.tiles_m = pl.tiles_m;
     args.tiles_n = pl.tiles_n;
     args.num_tiles = pl.num_tiles;
-    args.k_blocks = int(ceil_div(K, e.bk));
+    args.k_blocks = pl.k_blocks;
     args.group_m = pl.group_m;
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
-
-    const int ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+    int ctas = pl.dp_ctas;
+    if (use_sk) {
+        char *ws = static_cast<char *>(h->ws) + pl.ws_a + pl.ws_b;
+        args.stream_k = 1;
+        args.flags = reinterpret_cast<uint32_t *>(ws);
+        args.partials = reinterpret_cast<float *>(ws + pl.ws_flags);
+        ctas = pl.sk_ctas;
+        // Flags start at zero for every launch (set by the CTA that stores a
+        // partial tile, read by the CTA that finishes that tile).
+        if (cudaMemsetAsync(args.flags, 0, size_t(ctas) * 4, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+    }
     void *kargs[] = {&tmA, &tmB, &args};
     cudaError_t err = cudaLaunchKernel(e.fn, dim3(ctas), dim3(e.threads), kargs, size_t(e.smem), stream);
     return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
@@ -353,7 +388,7 @@ sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t h, int64_t M, int64_t N, int64
     Plan pl;
     st = make_plan(h, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, std::max<int64_t>(1, N), pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = pl.ws_a + pl.ws_b;
+    *bytes = pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
     return SGEMM_STATUS_SUCCESS;
 }
 
@@ -440,9 +475,10 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
     st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
     if (pl.pub.kind == 1) {
-        const int occ = occupancy_for(h, g_kernels[pl.algo_index][pl.variant]);
-        if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
-        pl.pub.ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+        const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
+                            h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
+        pl.pub.ctas = use_sk ? pl.sk_ctas : pl.dp_ctas;
+        pl.pub.stream_k = use_sk ? 1 : 0;
     }
     *plan = pl.pub;
     return SGEMM_STATUS_SUCCESS;
@@ -451,6 +487,12 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
     if (h == nullptr || algo < 0 || algo > kNumAlgos) return SGEMM_STATUS_INVALID_VALUE;
     h->algo = algo;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetSchedule(sgemmHandle_t h, int schedule) {
+    if (h == nullptr || schedule < 0 || schedule > 2) return SGEMM_STATUS_INVALID_VALUE;
+    h->schedule = schedule;
     return SGEMM_STATUS_SUCCESS;
 }
 

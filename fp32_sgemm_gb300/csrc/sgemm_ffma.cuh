@@ -56,6 +56,9 @@ struct GemmArgs {
     int tiles_m, tiles_n, num_tiles;
     int k_blocks;
     int group_m;          // rasterisation: tile rows per band
+    int stream_k;         // 0: whole tiles round robin; 1: equal shares of (tile, slice) units
+    float *partials;      // stream-K: one BM x BN partial tile per CTA
+    uint32_t *flags;      // stream-K: one ready flag per CTA, zeroed before the launch
     uint32_t *err;        // device error word (bounded waits)
     uint64_t timeout_ns;
 };
@@ -101,7 +104,7 @@ struct FfmaConfig {
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     // TMA swizzle span equals the A row: 128 B (BK=32), 64 B (BK=16), 32 B (BK=8).
     static constexpr int SWZ_MASK = ROW_BYTES_A / 16 - 1;      // 7, 3, 1
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 128 + 1024;
     static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
 
     static_assert(BK == 8 || BK == 16 || BK == 32, "A slice row must match a TMA swizzle span");
@@ -127,29 +130,135 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = local / rows;
 }
 
-// The sequence of K slices a CTA loads: all slices of its tiles, in order.
-// Slice number g (counted from 0 across tiles) goes to stage g % STAGES and
-// completes phase (g / STAGES) & 1 of that stage's barriers.
-struct SliceCursor {
-    int t, kb;       // tile and K slice of the next load
-    int g;           // its slice number
+// Work of one CTA, as segments: a run of K slices [kb0, kb1) of tile t.
+//   stream_k == 0: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//   stream_k == 1: the W = num_tiles * k_blocks (tile, slice) units, tile
+//     major, are cut into gridDim.x equal contiguous ranges, one per CTA
+//     ("stream-K" decomposition), so every CTA does the same number of FMAs.
+//     A tile cut between CTAs is finished by the CTA holding its first
+//     slice (the last segment of that CTA); the others store partial sums.
+struct Segment {
+    int t, kb0, kb1;
 };
 
+// Units are counted in 32 bits: the host enables stream-K only when
+// num_tiles * k_blocks < 2^31.
+struct WorkIter {
+    int u, u_end;   // stream-K units
+    int t;          // round-robin tile
+
+    __device__ __forceinline__ void begin(const GemmArgs &p) {
+        if (p.stream_k) {
+            const int64_t W = (int64_t)p.num_tiles * p.k_blocks;
+            u = (int)((int64_t)blockIdx.x * W / gridDim.x);
+            u_end = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x);
+            t = 0;
+        } else {
+            u = u_end = 0;
+            t = blockIdx.x;
+        }
+    }
+    __device__ __forceinline__ bool get(const GemmArgs &p, Segment &s) const {
+        if (p.stream_k) {
+            if (u >= u_end) return false;
+            s.t = u / p.k_blocks;
+            s.kb0 = u - s.t * p.k_blocks;
+            s.kb1 = min(p.k_blocks, s.kb0 + (u_end - u));
+            return true;
+        }
+        if (t >= p.num_tiles) return false;
+        s.t = t;
+        s.kb0 = 0;
+        s.kb1 = p.k_blocks;
+        return true;
+    }
+    __device__ __forceinline__ void advance(const GemmArgs &p, const Segment &s) {
+        if (p.stream_k) u += s.kb1 - s.kb0;
+        else t += gridDim.x;
+    }
+};
+
+// Stream-K: the CTA whose unit range contains unit u.
+__device__ __forceinline__ int cta_of_unit(int u, const GemmArgs &p) {
+    const int64_t W = (int64_t)p.num_tiles * p.k_blocks;
+    return (int)(((int64_t)(u + 1) * gridDim.x - 1) / W);
+}
+
+// The sequence of K slices a CTA loads, in consumption order.  Slice number
+// g (counted from 0 across segments) goes to stage g % STAGES and completes
+// phase (g / STAGES) & 1 of that stage's barriers.  Only the issuing thread
+// uses the cursor; it lives in shared memory and is read and written once
+// per issued slice, so that it holds no registers across the FMA loop.
+struct SliceCursor {
+    WorkIter it;
+    Segment seg;
+    int valid;
+    int kb, tm, tn;
+    int stage;
+    uint32_t phase;
+    int issued;
+};
+constexpr int kCursorWords = sizeof(SliceCursor) / 4;
+static_assert(sizeof(SliceCursor) % 4 == 0, "cursor is a block of 32-bit words");
+
+__device__ __forceinline__ SliceCursor cursor_load(const SliceCursor *sc) {
+    SliceCursor c;
+    const volatile int *src = reinterpret_cast<const volatile int *>(sc);
+    int *dst = reinterpret_cast<int *>(&c);
+#pragma unroll
+    for (int i = 0; i < kCursorWords; ++i) dst[i] = src[i];
+    return c;
+}
+
+__device__ __forceinline__ void cursor_store(SliceCursor *sc, const SliceCursor &c) {
+    volatile int *dst = reinterpret_cast<volatile int *>(sc);
+    const int *src = reinterpret_cast<const int *>(&c);
+#pragma unroll
+    for (int i = 0; i < kCursorWords; ++i) dst[i] = src[i];
+}
+
+__device__ __forceinline__ void cursor_begin(SliceCursor *sc, const GemmArgs &p) {
+    SliceCursor c;
+    c.it.begin(p);
+    c.valid = c.it.get(p, c.seg) ? 1 : 0;
+    c.kb = c.seg.kb0;
+    c.tm = c.tn = 0;
+    if (c.valid) tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.tm, c.tn);
+    c.stage = 0;
+    c.phase = 0;
+    c.issued = 0;
+    cursor_store(sc, c);
+}
+
+__device__ __forceinline__ bool cursor_valid(const SliceCursor *sc) {
+    return reinterpret_cast<const volatile SliceCursor *>(sc)->valid != 0;
+}
+__device__ __forceinline__ int cursor_issued(const SliceCursor *sc) {
+    return reinterpret_cast<const volatile SliceCursor *>(sc)->issued;
+}
+
+// Issue the cursor's next slice (waiting, bounded, for its stage to be free).
 template <class Cfg>
-__device__ __forceinline__ bool issue_slice(SliceCursor &c, const GemmArgs &p,
-                                            const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                            unsigned char *sA, unsigned char *sB,
-                                            uint64_t *full, uint64_t *empty) {
-    const int stage = c.g % Cfg::STAGES;
-    const uint32_t phase = (uint32_t)(c.g / Cfg::STAGES) & 1u;
-    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) return false;
-    int tm, tn;
-    tile_coords(c.t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-    tma_load_2d(sA + stage * Cfg::A_STAGE_BYTES, tmA, &full[stage], c.kb * Cfg::BK, tm * Cfg::BM);
-    tma_load_2d(sB + stage * Cfg::B_STAGE_BYTES, tmB, &full[stage], tn * Cfg::BN, c.kb * Cfg::BK);
-    ++c.g;
-    if (++c.kb == p.k_blocks) { c.kb = 0; c.t += gridDim.x; }
+__device__ __noinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
+                                         const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                         unsigned char *sA, unsigned char *sB,
+                                         uint64_t *full, uint64_t *empty) {
+    SliceCursor c = cursor_load(sc);
+    if (!mbar_wait_bounded(&empty[c.stage], c.phase ^ 1u, p.timeout_ns)) return false;
+    mbar_arrive_expect_tx(&full[c.stage], Cfg::STAGE_BYTES);
+    tma_load_2d(sA + c.stage * Cfg::A_STAGE_BYTES, tmA, &full[c.stage], c.kb * Cfg::BK, c.tm * Cfg::BM);
+    tma_load_2d(sB + c.stage * Cfg::B_STAGE_BYTES, tmB, &full[c.stage], c.tn * Cfg::BN, c.kb * Cfg::BK);
+    ++c.issued;
+    if (++c.stage == Cfg::STAGES) { c.stage = 0; c.phase ^= 1u; }
+    if (++c.kb == c.seg.kb1) {
+        c.it.advance(p, c.seg);
+        c.valid = c.it.get(p, c.seg) ? 1 : 0;
+        if (c.valid) {
+            c.kb = c.seg.kb0;
+            tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.tm, c.tn);
+        }
+    }
+    cursor_store(sc, c);
     return true;
 }
 
@@ -173,6 +282,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int NJ = TN / 4;   // 16-byte column groups per lane
     constexpr int KA = Cfg::KA;  // k values per vector read of A (4: 16 B, 2: 8 B)
     constexpr int NKQ = Cfg::NKQ;
+    constexpr int CONSUMER_THREADS = Cfg::CONSUMER_WARPS * 32;
     using AVec = typename AVecT<KA>::type;
 
     extern __shared__ unsigned char smem_raw[];
@@ -184,6 +294,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     unsigned char *sB = smem + STAGES * Cfg::A_STAGE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
+    uint64_t *cta_bar = empty + STAGES;   // consumer-warp rendezvous (stream-K fixup)
+    SliceCursor *cursor = reinterpret_cast<SliceCursor *>(cta_bar + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -193,15 +305,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
+        mbar_init(cta_bar, Cfg::CONSUMER_WARPS);
         fence_barrier_init();
     }
     __syncthreads();
-
-    const int slices_total = [&] {
-        const int my_tiles = p.num_tiles > (int)blockIdx.x
-                                 ? (p.num_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        return my_tiles * p.k_blocks;
-    }();
 
     if constexpr (Cfg::PRODUCER_WARP) {
         if (warp == Cfg::CONSUMER_WARPS) {
@@ -209,12 +316,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             if (lane != 0) return;
             prefetch_tensormap(&tmA);
             prefetch_tensormap(&tmB);
-            SliceCursor cur{(int)blockIdx.x, 0, 0};
-            while (cur.g < slices_total) {
-                if (!issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty)) {
+            cursor_begin(cursor, p);
+            while (cursor_valid(cursor)) {
+                if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
                     // No consumer may ever take the most recent slices.
-                    drain_slices<Cfg>(0, cur.g, full, p.timeout_ns);
+                    drain_slices<Cfg>(0, cursor_issued(cursor), full, p.timeout_ns);
                     return;
                 }
             }
@@ -227,12 +334,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     // after consuming slice g (g >= 1) refills the stage of slice g - 1, which
     // every warp has released by the time thread 0 is done with slice g.
     const bool producer = !Cfg::PRODUCER_WARP && threadIdx.x == 0;
-    SliceCursor cur{(int)blockIdx.x, 0, 0};
     if (producer) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        while (cur.g < slices_total && cur.g < STAGES)
-            issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty);   // fresh stages: never waits
+        cursor_begin(cursor, p);
+        while (cursor_valid(cursor) && cursor_issued(cursor) < STAGES)
+            issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty);   // fresh stages: never waits
     }
 
     const int wm = warp / Cfg::WARPS_N;
@@ -282,21 +389,35 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     };
 
-    int g = 0;   // slice number being consumed
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    // Rendezvous of the consumer warps (bounded; used around the stream-K
+    // partial-sum exchange).
+    uint32_t cta_phase = 0;
+    auto consumer_sync = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cta_bar);
+        if (!mbar_wait_bounded(cta_bar, cta_phase, p.timeout_ns)) record_error(p.err, kSiteCtaSync);
+        cta_phase ^= 1u;
+    };
+
+    WorkIter it;
+    it.begin(p);
+    Segment seg;
+    int g = 0;             // slice number being consumed
+    int stage = 0;
+    uint32_t phase = 0;
+    while (it.get(p, seg)) {
         int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
 
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
-            const int stage = g % STAGES;
-            if (!mbar_wait_bounded(&full[stage], (uint32_t)(g / STAGES) & 1u, p.timeout_ns)) {
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++g) {
+            if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
                 record_error(p.err, kSiteConsumerFull);
-                if (producer) drain_slices<Cfg>(g, cur.g, full, p.timeout_ns);
+                if (producer) drain_slices<Cfg>(g, cursor_issued(cursor), full, p.timeout_ns);
                 return;
             }
             const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
@@ -347,11 +468,60 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (producer && g >= 1 && cur.g < slices_total) {
-                if (!issue_slice<Cfg>(cur, p, &tmA, &tmB, sA, sB, full, empty)) {
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (producer && g >= 1 && cursor_valid(cursor)) {
+                if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
-                    drain_slices<Cfg>(g + 1, cur.g, full, p.timeout_ns);
+                    drain_slices<Cfg>(g + 1, cursor_issued(cursor), full, p.timeout_ns);
                     return;
+                }
+            }
+        }
+
+        // ---------------- stream-K fixup ----------------
+        if (seg.kb0 != 0 || seg.kb1 != p.k_blocks) {
+            float4 *mine = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * (BM * BN));
+            if (seg.kb0 != 0) {
+                // Not the first slice of the tile: hand the partial sums to
+                // the CTA that finishes it, then go on with the next segment.
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j)
+                        __stcg(&mine[(i * NJ + j) * CONSUMER_THREADS + threadIdx.x],
+                               make_float4(acc[i][2 * j].x, acc[i][2 * j].y,
+                                           acc[i][2 * j + 1].x, acc[i][2 * j + 1].y));
+                __threadfence();
+                consumer_sync();
+                if (threadIdx.x == 0) st_release_gpu(&p.flags[blockIdx.x], 1u);
+                it.advance(p, seg);
+                continue;
+            }
+            // First slice of a tile cut between CTAs: add the partial sums of
+            // the CTAs holding its other slices, in CTA order (deterministic).
+            const int tile_u0 = seg.t * p.k_blocks;
+            const int c_first = cta_of_unit(tile_u0 + seg.kb1, p);
+            const int c_last = cta_of_unit(tile_u0 + p.k_blocks - 1, p);
+            if (threadIdx.x == 0) {
+                for (int c = c_first; c <= c_last; ++c)
+                    if (!flag_wait_bounded(&p.flags[c], p.timeout_ns)) record_error(p.err, kSiteStreamKFlag);
+            }
+            consumer_sync();
+            for (int c = c_first; c <= c_last; ++c) {
+                const float4 *other = reinterpret_cast<const float4 *>(p.partials + (size_t)c * (BM * BN));
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        const float4 v = __ldcg(&other[(i * NJ + j) * CONSUMER_THREADS + threadIdx.x]);
+                        acc[i][2 * j].x += v.x;
+                        acc[i][2 * j].y += v.y;
+                        acc[i][2 * j + 1].x += v.z;
+                        acc[i][2 * j + 1].y += v.w;
+                    }
+                    // Keep the compiler from hoisting all 32 loads at once:
+                    // registers are already full with the accumulators.
+                    asm volatile("" ::: "memory");
                 }
             }
         }
@@ -391,6 +561,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
             }
         }
+        it.advance(p, seg);
     }
 }
 

@@ -84,10 +84,16 @@ sgemmStatus_t sgemmDestroy(sgemmHandle_t handle);
 sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle);
 
 /*
- * Bytes of device workspace sgemmEx() needs for these operands: 0 when A and
- * B can be read in place (16-byte aligned base, row pitch a multiple of 16
- * bytes), else room to repack the operand(s) that cannot into rows padded to
- * a multiple of 4 floats.  Same validation as sgemmEx().
+ * Bytes of device workspace sgemmEx() can use for these operands:
+ *   - room to repack A and/or B when an operand cannot be read in place (base
+ *     not 16-byte aligned or row pitch not a multiple of 16 bytes) into rows
+ *     padded to a multiple of 4 floats: REQUIRED for such operands;
+ *   - stream-K scratch (one ready flag and one BM x BN FP32 partial tile per
+ *     resident CTA) when the output tiles do not divide evenly over the SMs:
+ *     OPTIONAL; with less workspace the call runs whole tiles per CTA instead
+ *     (same result up to summation order, less even load).
+ * Same validation as sgemmEx().  Calls that share a workspace must be
+ * ordered on one stream.
  */
 sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t handle, int64_t M, int64_t N,
                                     int64_t K, const float *A, int64_t lda,
@@ -159,6 +165,7 @@ typedef struct sgemmPlan {
     int packs_a, packs_b; /* 1 if the operand is repacked into the workspace */
     int vector_epilogue;  /* 1 if C is written with 16-byte stores */
     int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0) */
+    int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
 } sgemmPlan_t;
 
 sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
@@ -176,6 +183,17 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * computes the same result up to summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
+
+/*
+ * How output tiles are shared among the persistent CTAs of the main kernel:
+ * 0 = automatic (default): stream-K when whole tiles would leave the SMs
+ *     unevenly loaded and the workspace has room for its scratch;
+ * 1 = whole tiles only, round robin;
+ * 2 = stream-K whenever the workspace has room (every CTA gets the same
+ *     number of (tile, K slice) units; tiles cut between CTAs are summed in
+ *     a fixed order, so results stay deterministic).
+ */
+sgemmStatus_t sgemmSetSchedule(sgemmHandle_t handle, int schedule);
 
 /*
  * Limit, in nanoseconds, on every wait a kernel of this handle performs

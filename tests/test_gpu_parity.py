@@ -36,7 +36,7 @@ def _to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _gpu(sg, handle, p, C_init=None, algo=0):
+def _gpu(sg, handle, p, C_init=None, algo=0, schedule=0):
     """Run the problem on the GPU; returns the full [M, ldc] C buffer on the host."""
     A = _to_dev(p.A)[:, : p.K] if p.K > 0 else torch.zeros((p.M, 0), device="cuda")
     B = _to_dev(p.B)[:, : p.N]
@@ -45,8 +45,10 @@ def _gpu(sg, handle, p, C_init=None, algo=0):
     Cbuf = _to_dev(C_init)
     C = Cbuf[:, : p.N]
     handle.set_algo(algo)
+    handle.set_schedule(schedule)
     handle.gemm(A, B, C, p.alpha, p.beta)
     torch.cuda.synchronize()
+    handle.set_schedule(0)
     assert handle.device_error() == 0
     return Cbuf.cpu().numpy()
 
@@ -117,6 +119,50 @@ def test_every_tile_configuration(sg, handle, algo, shape):
     _assert_close(_gpu(sg, handle, p, algo=algo)[:, :N], _ref(p))
     q = inputs.make_problem(M, N, K, seed=1040 + algo, kind="integer", alpha=0.5, beta=0.25)
     np.testing.assert_array_equal(_gpu(sg, handle, q, algo=algo)[:, :N].astype(np.float64), _ref(q))
+
+
+@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("algo", [1, 3, 5, 8])
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263), (1500, 700, 2000),
+                                   (257, 255, 4000)])
+def test_schedules(sg, handle, schedule, algo, shape):
+    # schedule 1: whole tiles per CTA; schedule 2: stream-K, where tiles are
+    # cut between CTAs (here up to ~5 CTAs per tile) and summed in a fixup.
+    M, N, K = shape
+    p = inputs.make_problem(M, N, K, seed=M + N + K + algo, alpha=0.75, beta=-0.5)
+    _assert_close(_gpu(sg, handle, p, algo=algo, schedule=schedule)[:, :N], _ref(p))
+    q = inputs.make_problem(M, N, K, seed=M + N + K + algo + 1000, kind="integer",
+                            alpha=0.75, beta=-0.5)
+    np.testing.assert_array_equal(
+        _gpu(sg, handle, q, algo=algo, schedule=schedule)[:, :N].astype(np.float64), _ref(q))
+
+
+def test_stream_k_chosen_for_uneven_tiles_and_deterministic(sg, handle):
+    M = N = K = 4096
+    p = inputs.make_problem(512, 512, 512, seed=3)   # content irrelevant for the plan
+    A = torch.empty((M, K), device="cuda")
+    B = torch.empty((K, N), device="cuda")
+    C = torch.empty((M, N), device="cuda")
+    handle.set_algo(0)
+    handle.set_schedule(0)
+    handle._ensure_workspace(handle.workspace_size(M, N, K, A.data_ptr(), K, B.data_ptr(), N))
+    plan = handle.plan(A, B, C)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["stream_k"] == (1 if (M // 128) * (N // 128) % sms else 0)
+    # Stream-K sums the partial tiles in a fixed order: repeated calls agree bitwise.
+    M, N, K = 1024, 1024, 1024
+    p = inputs.make_problem(M, N, K, seed=21)
+    A, B = _to_dev(p.A), _to_dev(p.B)
+    handle.set_schedule(2)
+    first = torch.empty((M, N), device="cuda")
+    handle.gemm(A, B, first)
+    C = torch.empty_like(first)
+    for _ in range(20):
+        handle.gemm(A, B, C)
+        assert torch.equal(C.view(torch.int32), first.view(torch.int32))
+    handle.set_schedule(0)
+    assert handle.device_error() == 0
+    _assert_close(first.cpu().numpy(), _ref(p))
 
 
 _SMALL = [1, 2, 3, 5, 8, 9]
