@@ -42,7 +42,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 8;
+constexpr int kNumAlgos = 10;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -51,6 +51,8 @@ void fill_algo5(KernelEntry *v);
 void fill_algo6(KernelEntry *v);
 void fill_algo7(KernelEntry *v);
 void fill_algo8(KernelEntry *v);
+void fill_algo9(KernelEntry *v);
+void fill_algo10(KernelEntry *v);
 
 // Auxiliary kernels (sgemm_aux.cu).
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, cudaStream_t s);

@@ -43,6 +43,8 @@ void init_kernel_table() {
     sg::fill_algo6(g_kernels[5]);
     sg::fill_algo7(g_kernels[6]);
     sg::fill_algo8(g_kernels[7]);
+    sg::fill_algo9(g_kernels[8]);
+    sg::fill_algo10(g_kernels[9]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

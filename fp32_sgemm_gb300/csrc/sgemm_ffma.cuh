@@ -239,7 +239,7 @@ __device__ __forceinline__ int cursor_issued(const SliceCursor *sc) {
 
 // Issue the cursor's next slice (waiting, bounded, for its stage to be free).
 template <class Cfg>
-__device__ __noinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
+__device__ __forceinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
                                          const CUtensorMap *tmA, const CUtensorMap *tmB,
                                          unsigned char *sA, unsigned char *sB,
                                          uint64_t *full, uint64_t *empty) {
