@@ -72,6 +72,7 @@ SIGNATURES = {
     "sgemmSetWaitTimeout": (_st, [_vp, ctypes.c_uint64]),
     "sgemmGetDeviceError": (_st, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "sgemmSelfTestWaitTimeout": (_st, [_vp, ctypes.c_uint64, _vp]),
+    "sgemmNoAlloc": (_st, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
 }
 
 _lock = threading.Lock()

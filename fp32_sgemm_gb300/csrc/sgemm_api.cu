@@ -530,3 +530,89 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t h, uint64_t timeout_ns, cud
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (sgemmNoAlloc).
+//
+// For callers that may not allocate device memory at all: code running where
+// the allocator is off limits (inside a memory pool or allocator hook, under
+// a framework that owns every byte of device memory, or in a process whose
+// memory budget is fixed up front).  Its scratch (error word, stream-K flags
+// and partial tiles, repacked operands) lives in one file-scope device array
+// that every GPU loading this library holds until the process exits.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
+constexpr size_t kStaticErrBytes = 256;                     // error word, padded
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_sgemm_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+struct StaticScratchSlot {
+    std::once_flag once;
+    sgemmStatus_t status = SGEMM_STATUS_INTERNAL_ERROR;
+    unsigned char *ptr = nullptr;   // device address of g_sgemm_static_scratch
+    int sm_count = 0;
+};
+StaticScratchSlot g_static_slots[kMaxDevices];
+
+// Once per device, with that device current: the array's device address (in
+// host code its name is only a host-side stand-in), the SM count and the
+// architecture check.
+void setup_static_scratch(StaticScratchSlot &slot, int dev) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        slot.status = SGEMM_STATUS_LAUNCH_FAILED;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        slot.status = SGEMM_STATUS_ARCH_MISMATCH;
+        return;
+    }
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_sgemm_static_scratch) != cudaSuccess || ptr == nullptr) {
+        slot.status = SGEMM_STATUS_LAUNCH_FAILED;
+        return;
+    }
+    slot.ptr = static_cast<unsigned char *>(ptr);
+    slot.sm_count = sms;
+    slot.status = SGEMM_STATUS_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                                      float beta, float *C, int64_t ldc, cudaStream_t stream) {
+    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
+    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    StaticScratchSlot &slot = g_static_slots[dev];
+    std::call_once(slot.once, [&slot, dev] { setup_static_scratch(slot, dev); });
+    if (slot.status != SGEMM_STATUS_SUCCESS) return slot.status;
+
+    // A context on the stack whose error word and workspace are carved out
+    // of the static array.
+    sgemmContext ctx;
+    ctx.device = dev;
+    ctx.sm_count = slot.sm_count;
+    ctx.d_err = reinterpret_cast<uint32_t *>(slot.ptr);
+    ctx.ws = slot.ptr + kStaticErrBytes;
+    ctx.ws_bytes = kStaticScratchBytes - kStaticErrBytes;
+
+    Plan pl;
+    st = make_plan(&ctx, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    // Operands that must be repacked have to fit in the static array;
+    // stream-K scratch is used only when it fits as well.
+    if (pl.ws_a + pl.ws_b > ctx.ws_bytes) return SGEMM_STATUS_NOT_SUPPORTED;
+    return run(&ctx, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}

@@ -221,6 +221,42 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
                                        uint64_t timeout_ns,
                                        cudaStream_t stream);
 
+/*
+ * sgemmNoAlloc: the same product as sgemm(), for callers that cannot
+ * allocate device memory at all -- code running where the allocator is off
+ * limits (inside an allocator hook or memory pool, under a framework that
+ * owns all device memory, or with a device-memory budget fixed up front).
+ * The paper (the SGEMM pages this library follows) has no counterpart of it.
+ *
+ * It calls no cudaMalloc, cudaFree or allocating library routine.  Its
+ * scratch (error word, stream-K flags and partial tiles, repacked operands)
+ * lives in one file-scope device array of SGEMM_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) that every GPU loading this library holds until process exit.
+ * The caller passes A, B and C as for sgemm().
+ *   - The first call on a device does one-time set-up on the current device
+ *     (looks up the array's device address, reads the SM count, checks the
+ *     architecture, queries kernel occupancy).  Make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array per device and the array keeps the
+ *     last call's contents; what must start at zero (the stream-K flags) is
+ *     cleared on the stream before each launch.  Calls whose work overlaps
+ *     on the GPU (different streams, or different host threads without
+ *     ordering) race on the array: order them on one stream.
+ *   - Operands that need repacking (base not 16-byte aligned or row pitch not
+ *     a multiple of 4 floats) must fit in the array: M * round_up(K, 4) and
+ *     K * round_up(N, 4) floats together at most 32 MiB minus 256 bytes;
+ *     larger ones return SGEMM_STATUS_NOT_SUPPORTED before anything is
+ *     enqueued.  Stream-K is used only when its scratch fits as well.
+ *   - A bounded-wait timeout inside this path is recorded in the array's own
+ *     error word, which no entry point reads back.
+ * Other status codes as for sgemm().
+ */
+#define SGEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alpha,
+                           const float *A, int64_t lda, const float *B,
+                           int64_t ldb, float beta, float *C, int64_t ldc,
+                           cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
