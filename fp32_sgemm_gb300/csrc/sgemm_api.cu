@@ -118,12 +118,18 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 8;
     int k_blocks = 0;
     int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
+    int sk_tile0 = 0;               // first tile of the stream-K part
 };
+
+// Configuration 10 (BK = 32, 3 stages, TMA issued by a compute thread, two
+// CTAs per SM, double-buffered 8-byte A and 16-byte B fragments) measured
+// fastest at 1024^3 to 8192^3; it is the automatic choice for every shape.
+constexpr int kDefaultAlgo = 10;
 
 int choose_algo(const sgemmContext *h, int64_t M, int64_t N, int64_t K) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
     (void)M; (void)N; (void)K;
-    return 0;
+    return kDefaultAlgo - 1;
 }
 
 int occupancy_for(const sgemmContext *h, KernelEntry &e) {
@@ -185,6 +191,11 @@ sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, 
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
     const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
     if (want_sk && pl.k_blocks >= 2 && units >= slots && units < kMaxDim) {
+        // All but the last full wave of tiles run whole (their concurrent
+        // tiles form a compact band, friendly to L2); the last wave plus the
+        // remainder is split evenly in (tile, K slice) units.
+        const int64_t waves = pl.num_tiles / slots;
+        pl.sk_tile0 = waves >= 2 ? int((waves - 1) * slots) : 0;
         pl.sk_ctas = int(slots);
         pl.ws_flags = align256(size_t(slots) * 4);
         pl.ws_partials = size_t(slots) * size_t(e.bm) * size_t(e.bn) * 4;
@@ -286,9 +297,10 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
     int ctas = pl.dp_ctas;
+    args.sk_tile0 = pl.num_tiles;
     if (use_sk) {
         char *ws = static_cast<char *>(h->ws) + pl.ws_a + pl.ws_b;
-        args.stream_k = 1;
+        args.sk_tile0 = pl.sk_tile0;
         args.flags = reinterpret_cast<uint32_t *>(ws);
         args.partials = reinterpret_cast<float *>(ws + pl.ws_flags);
         ctas = pl.sk_ctas;

@@ -56,7 +56,7 @@ struct GemmArgs {
     int tiles_m, tiles_n, num_tiles;
     int k_blocks;
     int group_m;          // rasterisation: tile rows per band
-    int stream_k;         // 0: whole tiles round robin; 1: equal shares of (tile, slice) units
+    int sk_tile0;         // tiles [0, sk_tile0) whole, round robin; [sk_tile0, num_tiles) stream-K
     float *partials;      // stream-K: one BM x BN partial tile per CTA
     uint32_t *flags;      // stream-K: one ready flag per CTA, zeroed before the launch
     uint32_t *err;        // device error word (bounded waits)
@@ -131,57 +131,54 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 }
 
 // Work of one CTA, as segments: a run of K slices [kb0, kb1) of tile t.
-//   stream_k == 0: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-//   stream_k == 1: the W = num_tiles * k_blocks (tile, slice) units, tile
-//     major, are cut into gridDim.x equal contiguous ranges, one per CTA
-//     ("stream-K" decomposition), so every CTA does the same number of FMAs.
-//     A tile cut between CTAs is finished by the CTA holding its first
-//     slice (the last segment of that CTA); the others store partial sums.
+//   Tiles [0, sk_tile0): whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//     (consecutive tile numbers run concurrently, a compact band of C).
+//   Tiles [sk_tile0, num_tiles): their (tile, slice) units, tile major, are
+//     cut into gridDim.x equal contiguous ranges, one per CTA ("stream-K"),
+//     so every CTA ends up with the same number of FMAs.  A tile cut between
+//     CTAs is finished by the CTA holding its first slice (the last segment
+//     of that CTA); the others store partial sums.
+// Units are counted in 32 bits: the host enables stream-K only when
+// num_tiles * k_blocks < 2^31.
 struct Segment {
     int t, kb0, kb1;
 };
 
-// Units are counted in 32 bits: the host enables stream-K only when
-// num_tiles * k_blocks < 2^31.
 struct WorkIter {
-    int u, u_end;   // stream-K units
-    int t;          // round-robin tile
+    int t;          // next whole tile
+    int u, u_end;   // stream-K units (absolute: tile * k_blocks + slice)
 
     __device__ __forceinline__ void begin(const GemmArgs &p) {
-        if (p.stream_k) {
-            const int64_t W = (int64_t)p.num_tiles * p.k_blocks;
-            u = (int)((int64_t)blockIdx.x * W / gridDim.x);
-            u_end = (int)((int64_t)(blockIdx.x + 1) * W / gridDim.x);
-            t = 0;
-        } else {
-            u = u_end = 0;
-            t = blockIdx.x;
-        }
+        t = blockIdx.x;
+        const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
+        const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
+        u = (int)(base + (int64_t)blockIdx.x * W / gridDim.x);
+        u_end = (int)(base + (int64_t)(blockIdx.x + 1) * W / gridDim.x);
     }
     __device__ __forceinline__ bool get(const GemmArgs &p, Segment &s) const {
-        if (p.stream_k) {
-            if (u >= u_end) return false;
-            s.t = u / p.k_blocks;
-            s.kb0 = u - s.t * p.k_blocks;
-            s.kb1 = min(p.k_blocks, s.kb0 + (u_end - u));
+        if (t < p.sk_tile0) {
+            s.t = t;
+            s.kb0 = 0;
+            s.kb1 = p.k_blocks;
             return true;
         }
-        if (t >= p.num_tiles) return false;
-        s.t = t;
-        s.kb0 = 0;
-        s.kb1 = p.k_blocks;
+        if (u >= u_end) return false;
+        s.t = u / p.k_blocks;
+        s.kb0 = u - s.t * p.k_blocks;
+        s.kb1 = min(p.k_blocks, s.kb0 + (u_end - u));
         return true;
     }
     __device__ __forceinline__ void advance(const GemmArgs &p, const Segment &s) {
-        if (p.stream_k) u += s.kb1 - s.kb0;
-        else t += gridDim.x;
+        if (t < p.sk_tile0) t += gridDim.x;
+        else u += s.kb1 - s.kb0;
     }
 };
 
 // Stream-K: the CTA whose unit range contains unit u.
 __device__ __forceinline__ int cta_of_unit(int u, const GemmArgs &p) {
-    const int64_t W = (int64_t)p.num_tiles * p.k_blocks;
-    return (int)(((int64_t)(u + 1) * gridDim.x - 1) / W);
+    const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
+    const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
+    return (int)((((int64_t)u - base + 1) * gridDim.x - 1) / W);
 }
 
 // The sequence of K slices a CTA loads, in consumption order.  Slice number
