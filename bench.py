@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sgemm_4096", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--algo", type=int, default=0, help="tile configuration (0 = automatic)")
+    ap.add_argument("--math", type=int, default=0,
+                    help="0 FP32 FFMA (CUDA cores), 1 error-compensated 3xTF32 (tensor cores)")
     ap.add_argument("--schedule", type=int, default=0,
                     help="0 automatic, 1 whole tiles per CTA, 2 stream-K")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -227,6 +229,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     handle = sg.Handle(dev)
     handle.set_algo(args.algo)
     handle.set_schedule(args.schedule)
+    handle.set_math_mode(args.math)
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     l2_bytes = getattr(props, "L2_cache_size", 0) or 0

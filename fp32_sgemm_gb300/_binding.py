@@ -69,6 +69,7 @@ SIGNATURES = {
                              ctypes.POINTER(Plan)]),
     "sgemmSetAlgo": (_st, [_vp, ctypes.c_int]),
     "sgemmSetSchedule": (_st, [_vp, ctypes.c_int]),
+    "sgemmSetMathMode": (_st, [_vp, ctypes.c_int]),
     "sgemmSetWaitTimeout": (_st, [_vp, ctypes.c_uint64]),
     "sgemmGetDeviceError": (_st, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "sgemmSelfTestWaitTimeout": (_st, [_vp, ctypes.c_uint64, _vp]),
@@ -187,6 +188,10 @@ class Handle:
 
     def set_algo(self, algo: int):
         _check(self._lib.sgemmSetAlgo(self._h, int(algo)), "sgemmSetAlgo")
+
+    def set_math_mode(self, mode: int):
+        """0 FP32 FFMA (default), 1 error-compensated 3xTF32 on the tensor cores."""
+        _check(self._lib.sgemmSetMathMode(self._h, int(mode)), "sgemmSetMathMode")
 
     def set_schedule(self, schedule: int):
         """0 automatic, 1 whole tiles per CTA, 2 stream-K when it applies."""

@@ -54,6 +54,28 @@ void fill_algo8(KernelEntry *v);
 void fill_algo9(KernelEntry *v);
 void fill_algo10(KernelEntry *v);
 
+// Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
+struct Tf32x3Args {
+    int M, N, K;
+    float alpha, beta;
+    float *C;
+    int64_t ldc;
+    int tiles_m, tiles_n, num_tiles;
+    int k_blocks;
+    int group_m;
+    uint32_t *err;
+    uint64_t timeout_ns;
+};
+struct Tf32x3Info {
+    const void *fn[4];   // variant index as for the FFMA kernels
+    int threads, smem, bm, bn, bk, stages;
+};
+Tf32x3Info tf32x3_info();
+void launch_split_rows(const float *A, int64_t lda, float *hi, float *lo, int64_t ldh, int rows,
+                       int cols, cudaStream_t s);
+void launch_split_transpose(const float *B, int64_t ldb, float *hiT, float *loT, int64_t ldh,
+                            int K, int N, cudaStream_t s);
+
 // Auxiliary kernels (sgemm_aux.cu).
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, cudaStream_t s);
 void launch_pack_rows(const float *src, int64_t ld_src, float *dst, int64_t ld_dst,

@@ -73,6 +73,7 @@ struct sgemmContext {
     uint64_t timeout_ns = kDefaultTimeoutNs;
     int algo = 0;
     int schedule = 0;   // 0 automatic, 1 whole tiles only, 2 stream-K whenever it applies
+    int math = 0;       // 0 FP32 FFMA, 1 error-compensated 3xTF32 on the tensor cores
 };
 
 namespace {
@@ -119,6 +120,8 @@ struct Plan {
     int k_blocks = 0;
     int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
     int sk_tile0 = 0;               // first tile of the stream-K part
+    int64_t kp = 0;                 // 3xTF32: row pitch of the split operands
+    size_t ws_split = 0;            // 3xTF32: A_hi, A_lo, B_hi^T, B_lo^T
 };
 
 // Configuration 10 (BK = 32, 3 stages, TMA issued by a compute thread, two
@@ -148,6 +151,54 @@ int occupancy_for(const sgemmContext *h, KernelEntry &e) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// 3xTF32 plan: operands are always split into the workspace (TF32 hi and lo
+// parts, B transposed), so any pitch and alignment of A and B is accepted.
+sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, int64_t M, int64_t N, int64_t K,
+                               const float *C, int64_t ldc, float beta, Plan &pl) {
+    const sg::Tf32x3Info info = sg::tf32x3_info();
+    pl.pub.kind = 3;
+    pl.pub.vector_epilogue = tma_ok(C, ldc) ? 1 : 0;
+    pl.variant = (beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
+    pl.kp = round_up(K, 4);
+    if (ceil_div(K, 32) > 65535) return SGEMM_STATUS_NOT_SUPPORTED;   // split grid
+    pl.ws_split = 2 * align256(size_t(M) * size_t(pl.kp) * 4) + 2 * align256(size_t(N) * size_t(pl.kp) * 4);
+    pl.tiles_m = int(ceil_div(M, info.bm));
+    pl.tiles_n = int(ceil_div(N, info.bn));
+    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n;
+    if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
+    pl.num_tiles = int(tiles);
+    pl.k_blocks = int(ceil_div(K, info.bk));
+    static std::mutex occ_mutex;
+    static int occ_cache[kMaxDevices][4] = {};
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> lk(occ_mutex);
+        int &o = occ_cache[h->device][pl.variant];
+        if (o == 0) {
+            const void *fn = info.fn[pl.variant];
+            int n = 0;
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, info.threads, info.smem) != cudaSuccess ||
+                n < 1)
+                return SGEMM_STATUS_LAUNCH_FAILED;
+            o = n;
+        }
+        occ = o;
+    }
+    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+    pl.pub.tile_m = info.bm;
+    pl.pub.tile_n = info.bn;
+    pl.pub.tile_k = info.bk;
+    pl.pub.stages = info.stages;
+    pl.pub.packs_a = 1;
+    pl.pub.packs_b = 1;
+    pl.pub.launches = 3;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t encode_2d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer,
+                        int64_t ld, int box_inner, int box_outer, CUtensorMapSwizzle swz);
+
 // Plan of one call: repacking, kernel variant, grid and stream-K split.
 // Queries the kernel's occupancy once per device (a CUDA call); everything
 // else is host arithmetic.
@@ -162,6 +213,7 @@ sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, 
         return SGEMM_STATUS_SUCCESS;
     }
     std::call_once(g_kernels_once, init_kernel_table);
+    if (h->math == 1) return make_plan_tf32x3(h, M, N, K, C, ldc, beta, pl);
     pl.pub.kind = 1;
     pl.pub.packs_a = tma_ok(A, lda) ? 0 : 1;
     pl.pub.packs_b = tma_ok(B, ldb) ? 0 : 1;
@@ -233,6 +285,51 @@ sgemmStatus_t launch_pack(const float *src, int64_t ld_src, float *dst, int64_t 
     return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
+sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float beta, float *C, int64_t ldc, cudaStream_t stream) {
+    if (h->ws == nullptr || h->ws_bytes < pl.ws_split) return SGEMM_STATUS_WORKSPACE_REQUIRED;
+    const sg::Tf32x3Info info = sg::tf32x3_info();
+    char *ws = static_cast<char *>(h->ws);
+    const size_t a_bytes = align256(size_t(M) * size_t(pl.kp) * 4);
+    const size_t b_bytes = align256(size_t(N) * size_t(pl.kp) * 4);
+    float *a_hi = reinterpret_cast<float *>(ws);
+    float *a_lo = reinterpret_cast<float *>(ws + a_bytes);
+    float *b_hi = reinterpret_cast<float *>(ws + 2 * a_bytes);
+    float *b_lo = reinterpret_cast<float *>(ws + 2 * a_bytes + b_bytes);
+    sg::launch_split_rows(A, lda, a_hi, a_lo, pl.kp, int(M), int(K), stream);
+    sg::launch_split_transpose(B, ldb, b_hi, b_lo, pl.kp, int(K), int(N), stream);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+
+    CUtensorMap tm[4];
+    const float *ptrs[4] = {a_hi, a_lo, b_hi, b_lo};
+    for (int i = 0; i < 4; ++i) {
+        const bool is_a = i < 2;
+        sgemmStatus_t st = encode_2d(&tm[i], ptrs[i], K, is_a ? M : N, pl.kp, info.bk,
+                                     is_a ? info.bm : info.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != SGEMM_STATUS_SUCCESS) return st;
+    }
+    sg::Tf32x3Args args{};
+    args.M = int(M);
+    args.N = int(N);
+    args.K = int(K);
+    args.alpha = alpha;
+    args.beta = beta;
+    args.C = C;
+    args.ldc = ldc;
+    args.tiles_m = pl.tiles_m;
+    args.tiles_n = pl.tiles_n;
+    args.num_tiles = pl.num_tiles;
+    args.k_blocks = pl.k_blocks;
+    args.group_m = pl.group_m;
+    args.err = h->d_err;
+    args.timeout_ns = h->timeout_ns;
+    void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
+    cudaError_t err = cudaLaunchKernel(info.fn[pl.variant], dim3(pl.dp_ctas), dim3(info.threads),
+                                       kargs, size_t(info.smem), stream);
+    return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
 sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                   int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                   cudaStream_t stream) {
@@ -251,6 +348,8 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
         sg::launch_scale_c(int(M), int(N), beta, C, ldc, stream);
         return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
     }
+
+    if (pl.pub.kind == 3) return run_tf32x3(h, pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 
     const float *Ause = A, *Buse = B;
     // Stream-K scratch is optional: without room for it, whole tiles are used.
@@ -402,7 +501,7 @@ sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t h, int64_t M, int64_t N, int64
     Plan pl;
     st = make_plan(h, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, std::max<int64_t>(1, N), pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
+    *bytes = pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials + pl.ws_split;
     return SGEMM_STATUS_SUCCESS;
 }
 
@@ -488,6 +587,7 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
     Plan pl;
     st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
+    if (pl.pub.kind == 3) pl.pub.ctas = pl.dp_ctas;
     if (pl.pub.kind == 1) {
         const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
                             h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
@@ -501,6 +601,12 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
     if (h == nullptr || algo < 0 || algo > kNumAlgos) return SGEMM_STATUS_INVALID_VALUE;
     h->algo = algo;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetMathMode(sgemmHandle_t h, int mode) {
+    if (h == nullptr || mode < 0 || mode > 1) return SGEMM_STATUS_INVALID_VALUE;
+    h->math = mode;
     return SGEMM_STATUS_SUCCESS;
 }
 

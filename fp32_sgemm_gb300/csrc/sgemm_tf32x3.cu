@@ -1,0 +1,340 @@
+// FP32 SGEMM on the 5th-generation tensor cores, error-compensated 3xTF32:
+//
+//   x = x_hi + x_lo,  x_hi = tf32(x), x_lo = tf32(x - x_hi)   (round to nearest)
+//   A.B ~= A_hi.B_hi + A_hi.B_lo + A_lo.B_hi                  (FP32 accumulation)
+//
+// The dropped term A_lo.B_lo and the rounding of x_lo leave a relative
+// error per product near 2^-21, far inside the FP32 acceptance bound, while
+// the products run at tensor-core rate.  TF32 is only mentioned on the pages
+// as a different contest ("Matmul I", section 1; "The Final Kernel", "What
+// Could Be Improved"); the splitting is the error-compensated TF32 method of
+// Ootomo & Yokota (2022).  Integer-valued inputs up to 2^11 in magnitude are
+// exact in TF32 (x_lo = 0), so those products stay bit exact.
+//
+// Two kernels:
+//   * split: A -> A_hi, A_lo (row major, K contiguous) and B -> B_hi^T, B_lo^T
+//     (N x K, K contiguous), so both tensor-core operands are K-major and can
+//     be staged with TMA's 128-byte swizzle, the layout the MMA descriptors
+//     name;
+//   * main: persistent CTAs of 6 warps.  Warp 0 lane 0 streams the four
+//     operand tiles of each 32-wide K slice into a shared-memory ring (TMA);
+//     warp 1 lane 0 issues tcgen05.mma (M=128, N=BN, K=8, kind::tf32) into a
+//     double-buffered TMEM accumulator; warps 2..5 read the accumulator back
+//     (tcgen05.ld, each warp its 32-lane quarter of TMEM) and write C =
+//     alpha*acc (+ beta*C) while the next tile is multiplied.
+// Every wait is bounded; a CTA that gives up records the error, lets its own
+// TMA copies and MMAs finish, and releases its TMEM before returning.
+#include <algorithm>
+
+#include "kernel_table.h"
+
+namespace sg {
+
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// A[M][lda] -> hi[M][ldh], lo[M][ldh] (first K columns).
+__global__ void split_rows_kernel(const float *__restrict__ A, int64_t lda, float *__restrict__ hi,
+                                  float *__restrict__ lo, int64_t ldh, int rows, int cols) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float *src = A + r * lda;
+        float *h = hi + r * ldh;
+        float *l = lo + r * ldh;
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
+            const float x = src[c];
+            const float xh = tf32_rna(x);
+            h[c] = xh;
+            l[c] = tf32_rna(x - xh);
+        }
+    }
+}
+
+// B[K][ldb] -> hiT[N][ldh], loT[N][ldh]: 32 x 32 tiles through shared memory
+// so that both the reads (along N) and the writes (along K) are coalesced.
+__global__ void split_transpose_kernel(const float *__restrict__ B, int64_t ldb,
+                                       float *__restrict__ hiT, float *__restrict__ loT,
+                                       int64_t ldh, int K, int N) {
+    __shared__ float th[32][33];
+    __shared__ float tl[32][33];
+    const int n0 = blockIdx.x * 32;
+    const int k0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int k = k0 + i, n = n0 + threadIdx.x;
+        float xh = 0.f, xl = 0.f;
+        if (k < K && n < N) {
+            const float x = B[(int64_t)k * ldb + n];
+            xh = tf32_rna(x);
+            xl = tf32_rna(x - xh);
+        }
+        th[i][threadIdx.x] = xh;
+        tl[i][threadIdx.x] = xl;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int n = n0 + i, k = k0 + threadIdx.x;
+        if (n < N && k < K) {
+            hiT[(int64_t)n * ldh + k] = th[threadIdx.x][i];
+            loT[(int64_t)n * ldh + k] = tl[threadIdx.x][i];
+        }
+    }
+}
+
+template <int BN_, int STAGES_>
+struct Tf32x3Config {
+    static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
+    static constexpr int A_BYTES = BM * BK * 4;     // one of A_hi / A_lo
+    static constexpr int B_BYTES = BN * BK * 4;     // one of B_hi / B_lo
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;        // two accumulators
+    static constexpr int THREADS = 192;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16 + 1024;
+    static_assert(BN == 64 || BN == 128 || BN == 256, "UMMA N for M = 128");
+    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM");
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
+};
+
+template <class Cfg, bool BETA_ZERO, bool C_VEC>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
+                    const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+                    const Tf32x3Args p)
+{
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr uint32_t IDESC = idesc_tf32(BM, BN);
+
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    unsigned char *smem = smem_raw + pad;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t *full = bars;                      // TMA -> MMA, per stage
+    uint64_t *empty = bars + STAGES;            // MMA -> TMA, per stage
+    uint64_t *tfull = bars + 2 * STAGES;        // MMA -> epilogue, per accumulator
+    uint64_t *tempty = tfull + 2;               // epilogue -> MMA, per accumulator
+    uint64_t *drain = tempty + 2;               // MMA completion before teardown
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        prefetch_tensormap(&tmAhi);
+        prefetch_tensormap(&tmAlo);
+        prefetch_tensormap(&tmBhi);
+        prefetch_tensormap(&tmBlo);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                    record_error(p.err, kSiteProducerEmpty);
+                    ok = false;
+                    break;
+                }
+                unsigned char *st = smem + stage * Cfg::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                tma_load_2d(st, &tmAhi, &full[stage], kb * BK, tm * BM);
+                tma_load_2d(st + Cfg::A_BYTES, &tmAlo, &full[stage], kb * BK, tm * BM);
+                tma_load_2d(st + 2 * Cfg::A_BYTES, &tmBhi, &full[stage], kb * BK, tn * BN);
+                tma_load_2d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, &full[stage], kb * BK, tn * BN);
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            // Let this CTA's own copies land before it can exit.
+            const int pending = issued < STAGES ? issued : STAGES;
+            for (int back = 1; back <= pending; ++back) {
+                int s = stage - back;
+                uint32_t ph = phase;
+                if (s < 0) { s += STAGES; ph ^= 1u; }
+                mbar_wait_bounded(&full[s], ph, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int lt = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++lt) {
+            const int ab = lt & 1;
+            const uint32_t use = (uint32_t)(lt >> 1);
+            if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
+                record_error(p.err, kSiteConsumerFull);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+                    record_error(p.err, kSiteConsumerFull);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s_ahi = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                const uint32_t s_alo = s_ahi + Cfg::A_BYTES;
+                const uint32_t s_bhi = s_ahi + 2 * Cfg::A_BYTES;
+                const uint32_t s_blo = s_bhi + Cfg::B_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    // K = 8 tf32 values = 32 bytes per MMA along the swizzled row.
+                    const uint32_t off = (uint32_t)kk * 32u;
+                    const uint64_t a_hi = smem_desc_k_sw128(s_ahi + off);
+                    const uint64_t a_lo = smem_desc_k_sw128(s_alo + off);
+                    const uint64_t b_hi = smem_desc_k_sw128(s_bhi + off);
+                    const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    // Small terms first, then the dominant product.
+                    mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
+                    mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
+                    mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
+                }
+                mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(&tfull[ab]);             // accumulator ready for the epilogue
+        }
+        // All MMAs this thread issued complete before the CTA tears down.
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0u, p.timeout_ns);
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM -> registers -> C ----------------
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+        const float alpha = p.alpha, beta = p.beta;
+        int lt = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+            const int ab = lt & 1;
+            const uint32_t use = (uint32_t)(lt >> 1);
+            if (!mbar_wait_bounded(&tfull[ab], use & 1u, p.timeout_ns)) {
+                record_error(p.err, kSiteConsumerFull);
+                break;
+            }
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int row = tm * BM + quarter * 32 + lane;
+            float *crow = p.C + (int64_t)row * p.ldc;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld_32cols(taddr + (uint32_t)c0, v);
+                if (row < p.M) {
+                    const int col0 = tn * BN + c0;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int col = col0 + 4 * q;
+                        if (C_VEC && col + 3 < p.N) {
+                            float4 *dst = reinterpret_cast<float4 *>(crow + col);
+                            float4 o;
+                            if constexpr (BETA_ZERO) {
+                                o = make_float4(alpha * v[4 * q], alpha * v[4 * q + 1],
+                                                alpha * v[4 * q + 2], alpha * v[4 * q + 3]);
+                            } else {
+                                const float4 c = *dst;
+                                o = make_float4(fmaf(beta, c.x, alpha * v[4 * q]),
+                                                fmaf(beta, c.y, alpha * v[4 * q + 1]),
+                                                fmaf(beta, c.z, alpha * v[4 * q + 2]),
+                                                fmaf(beta, c.w, alpha * v[4 * q + 3]));
+                            }
+                            *dst = o;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (col + e < p.N) {
+                                    float *dst = crow + col + e;
+                                    if constexpr (BETA_ZERO) *dst = alpha * v[4 * q + e];
+                                    else *dst = fmaf(beta, *dst, alpha * v[4 * q + e]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- launches
+
+namespace {
+inline int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
+
+template <class Cfg>
+struct Tf32x3Entries {
+    const void *fn[4];
+    Tf32x3Entries() {
+        fn[0] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, true>);
+        fn[1] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, false>);
+        fn[2] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, true>);
+        fn[3] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, false>);
+    }
+};
+
+using Tf32x3Cfg = Tf32x3Config<128, 3>;
+}  // namespace
+
+Tf32x3Info tf32x3_info() {
+    static const Tf32x3Entries<Tf32x3Cfg> entries;
+    Tf32x3Info info;
+    for (int i = 0; i < 4; ++i) info.fn[i] = entries.fn[i];
+    info.threads = Tf32x3Cfg::THREADS;
+    info.smem = Tf32x3Cfg::SMEM_BYTES;
+    info.bm = Tf32x3Cfg::BM;
+    info.bn = Tf32x3Cfg::BN;
+    info.bk = Tf32x3Cfg::BK;
+    info.stages = Tf32x3Cfg::STAGES;
+    return info;
+}
+
+void launch_split_rows(const float *A, int64_t lda, float *hi, float *lo, int64_t ldh, int rows,
+                       int cols, cudaStream_t s) {
+    dim3 grid(unsigned(std::min<int64_t>(cdiv(cols, 256), 8)), unsigned(std::min<int64_t>(rows, 65535)));
+    split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, hi, lo, ldh, rows, cols);
+}
+
+void launch_split_transpose(const float *B, int64_t ldb, float *hiT, float *loT, int64_t ldh,
+                            int K, int N, cudaStream_t s) {
+    dim3 grid(unsigned(cdiv(N, 32)), unsigned(cdiv(K, 32)));
+    split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(B, ldb, hiT, loT, ldh, K, N);
+}
+
+}  // namespace sg

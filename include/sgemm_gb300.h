@@ -164,7 +164,8 @@ typedef struct sgemmPlan {
     int ctas;           /* CTAs of the main kernel (persistent grid) */
     int packs_a, packs_b; /* 1 if the operand is repacked into the workspace */
     int vector_epilogue;  /* 1 if C is written with 16-byte stores */
-    int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0) */
+    int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0),
+                           3 3xTF32 tensor-core kernel (after the split pre-pass) */
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
 } sgemmPlan_t;
 
@@ -183,6 +184,24 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * computes the same result up to summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
+
+/*
+ * Arithmetic of the main kernel for calls on this handle:
+ * 0 = FP32 FFMA on the CUDA cores (default): every product and sum in FP32.
+ * 1 = error-compensated 3xTF32 on the 5th-generation tensor cores
+ *     (tcgen05): each operand is split into a TF32 part and a TF32 residual
+ *     (x = hi + lo, both rounded to nearest) and C = alpha * (A_hi.B_hi +
+ *     A_hi.B_lo + A_lo.B_hi) + beta * C with FP32 accumulation.  The omitted
+ *     A_lo.B_lo term and the rounding of lo bound the extra relative error
+ *     per product near 2^-21; integer-valued inputs of magnitude < 2^11 give
+ *     bit-exact results.  Needs a workspace of 2 * (M + N) * round_up(K, 4)
+ *     floats (rounded up to 256 bytes per part) for the split operands;
+ *     the split runs as two extra kernels before the product.
+ * The pages treat TF32 only as a different contest; the splitting follows
+ * Ootomo & Yokota, "Recovering single precision accuracy from Tensor Cores
+ * while surpassing the FP32 theoretical peak performance" (2022).
+ */
+sgemmStatus_t sgemmSetMathMode(sgemmHandle_t handle, int mode);
 
 /*
  * How output tiles are shared among the persistent CTAs of the main kernel:

@@ -1,0 +1,135 @@
+"""Error-compensated 3xTF32 tensor-core path (math mode 1) vs the fp64 oracle,
+through the C ABI: the same FP32 acceptance bound as the FFMA path for
+uniform inputs, bit-exact results for integer-valued inputs."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from fp32_sgemm_gb300 import inputs
+from conftest import fp32_tolerance
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def handle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp32_sgemm_gb300 as m
+    m.build()
+    h = m.Handle()
+    h.set_math_mode(1)
+    yield h
+    h.close()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _run(h, p, C_init=None):
+    A = _dev(p.A)[:, : p.K]
+    B = _dev(p.B)[:, : p.N]
+    if C_init is None:
+        C_init = p.C0 if p.C0 is not None else np.full((p.M, p.N), np.nan, np.float32)
+    Cbuf = _dev(C_init)
+    h.gemm(A, B, Cbuf[:, : p.N], p.alpha, p.beta)
+    torch.cuda.synchronize()
+    assert h.device_error() == 0
+    return Cbuf.cpu().numpy()
+
+
+def _ref(p):
+    return oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0)
+
+
+def _close(got, ref):
+    err = np.abs(got.astype(np.float64) - ref)
+    tol = fp32_tolerance(ref)
+    assert np.all(err <= tol), f"worst error/tolerance {float(np.max(err / tol)):.3g}"
+    return float(np.max(err / tol))
+
+
+def test_plan_uses_the_tensor_core_kernel(handle):
+    A = torch.zeros((256, 64), device="cuda")
+    B = torch.zeros((64, 128), device="cuda")
+    C = torch.zeros((256, 128), device="cuda")
+    plan = handle.plan(A, B, C)
+    assert plan["kind"] == 3 and plan["launches"] == 3
+
+
+@pytest.mark.parametrize("name", ["sgemm_128", "sgemm_1024", "sgemm_4096", "sgemm_4095x4097x1023"])
+def test_workloads_uniform_and_integer(handle, name):
+    w = inputs.WORKLOADS[name]
+    p = inputs.workload_problem(w, "uniform")
+    ratio = _close(_run(handle, p)[:, : p.N], _ref(p))
+    assert ratio < 0.5
+    q = inputs.workload_problem(w, "integer")
+    np.testing.assert_array_equal(_run(handle, q)[:, : q.N].astype(np.float64), _ref(q))
+
+
+def test_8192_sampled(handle):
+    w = inputs.WORKLOADS["sgemm_8192"]
+    rows, cols = inputs.sample_entries(w.M, w.N, w.samples, w.seed)
+    for kind in ("uniform", "integer"):
+        p = inputs.workload_problem(w, kind)
+        C = torch.empty((w.M, w.N), device="cuda")
+        handle.gemm(_dev(p.A), _dev(p.B), C)
+        got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy()
+        ref = oracle.sgemm_ref_entries(w.K, w.alpha, p.A, p.B, rows, cols)
+        if kind == "uniform":
+            _close(got, ref)
+        else:
+            np.testing.assert_array_equal(got.astype(np.float64), ref)
+    assert handle.device_error() == 0
+
+
+def test_small_and_edge_shapes(handle):
+    sizes = [1, 3, 8, 31, 33, 127, 129, 200]
+    for M, N, K in itertools.product(sizes[::2], sizes[1::2], [1, 5, 32, 33, 100]):
+        q = inputs.make_problem(M, N, K, seed=M * 7 + N * 3 + K, kind="integer", alpha=1.0,
+                                beta=0.5, with_c=True, lda=K + (M % 3), ldb=N + 1, ldc=N + 2)
+        got = _run(handle, q)
+        np.testing.assert_array_equal(got[:, :N].astype(np.float64), _ref(q),
+                                      err_msg=f"shape {(M, N, K)}")
+        assert np.isnan(got[:, N:]).all()
+        p = inputs.make_problem(M, N, K, seed=M + N + K, alpha=-1.5, beta=0.25)
+        _close(_run(handle, p)[:, :N], _ref(p))
+
+
+def test_beta_zero_never_reads_c(handle):
+    p = inputs.make_problem(300, 260, 100, seed=5)
+    got = _run(handle, p, C_init=np.full((300, 260), np.nan, np.float32))
+    assert np.isfinite(got).all()
+    _close(got, _ref(p))
+
+
+def test_large_magnitudes_and_mixed_scales(handle):
+    # Inputs spread over many binades, where the TF32 residual carries bits
+    # that a single TF32 pass would lose.
+    rng = np.random.default_rng(3)
+    M, N, K = 384, 320, 1000
+    A = (rng.uniform(-1, 1, (M, K)) * 2.0 ** rng.integers(-20, 20, (M, K))).astype(np.float32)
+    B = (rng.uniform(-1, 1, (K, N)) * 2.0 ** rng.integers(-20, 20, (K, N))).astype(np.float32)
+    C = torch.empty((M, N), device="cuda")
+    handle.gemm(_dev(A), _dev(B), C)
+    got = C.cpu().numpy().astype(np.float64)
+    ref = oracle.sgemm_ref(M, N, K, 1.0, A, B)
+    # Relative to the magnitude sum, as any FP32 summation is.
+    scale = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-30)
+
+
+def test_repeated_calls_bitwise_identical(handle):
+    p = inputs.make_problem(1024, 768, 640, seed=10)
+    A, B = _dev(p.A), _dev(p.B)
+    first = torch.empty((1024, 768), device="cuda")
+    handle.gemm(A, B, first)
+    C = torch.empty_like(first)
+    for _ in range(10):
+        handle.gemm(A, B, C)
+        assert torch.equal(C.view(torch.int32), first.view(torch.int32))
