@@ -18,10 +18,19 @@
 //     name;
 //   * main: persistent CTAs of 6 warps.  Warp 0 lane 0 streams the four
 //     operand tiles of each 32-wide K slice into a shared-memory ring (TMA);
-//     warp 1 lane 0 issues tcgen05.mma (M=128, N=BN, K=8, kind::tf32) into a
-//     double-buffered TMEM accumulator; warps 2..5 read the accumulator back
-//     (tcgen05.ld, each warp its 32-lane quarter of TMEM) and write C =
-//     alpha*acc (+ beta*C) while the next tile is multiplied.
+//     warp 1 lane 0 issues tcgen05.mma (M=128, N=BN, K=8, kind::tf32) into
+//     TMEM; warps 2..5 read TMEM back (tcgen05.ld, each warp its 32-lane
+//     quarter) and write C = alpha*acc (+ beta*C).
+//
+// Chunked accumulation.  The tensor core's FP32 accumulation does not round
+// to nearest: summing all of K into one TMEM accumulator, whose sign and
+// magnitude persist, lets those rounding errors pile up in one direction
+// (measured: error growing linearly with K, 3x over the FP32 bound at
+// K = 8192).  So the MMAs restart a fresh accumulator every CHUNK_KB K
+// slices (two TMEM buffers alternate), and the epilogue warps add each chunk
+// into an FP32 register sum with ordinary round-to-nearest additions while
+// the next chunk is being multiplied.  Chunk sums change sign at random, so
+// what is left of the tensor core's rounding averages out.
 // Every wait is bounded; a CTA that gives up records the error, lets its own
 // TMA copies and MMAs finish, and releases its TMEM before returning.
 #include <algorithm>
@@ -82,9 +91,10 @@ __global__ void split_transpose_kernel(const float *__restrict__ B, int64_t ldb,
     }
 }
 
-template <int BN_, int STAGES_>
+template <int BN_, int STAGES_, int CHUNK_KB_>
 struct Tf32x3Config {
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
+    static constexpr int CHUNK_KB = CHUNK_KB_;     // K slices per TMEM accumulator chunk
     static constexpr int A_BYTES = BM * BK * 4;     // one of A_hi / A_lo
     static constexpr int B_BYTES = BN * BK * 4;     // one of B_hi / B_lo
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
@@ -181,108 +191,121 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         // ---------------- MMA issuer ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int lt = 0;
+        int gc = 0;             // chunk counter across tiles: TMEM buffer gc & 1
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++lt) {
-            const int ab = lt & 1;
-            const uint32_t use = (uint32_t)(lt >> 1);
-            if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
-                record_error(p.err, kSiteConsumerFull);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
-                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int kb0 = 0; ok && kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB, ++gc) {
+                const int ab = gc & 1;
+                const uint32_t use = (uint32_t)(gc >> 1);
+                if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s_ahi = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-                const uint32_t s_alo = s_ahi + Cfg::A_BYTES;
-                const uint32_t s_bhi = s_ahi + 2 * Cfg::A_BYTES;
-                const uint32_t s_blo = s_bhi + Cfg::B_BYTES;
+                const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
+                const int kb1 = min(p.k_blocks, kb0 + Cfg::CHUNK_KB);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+                        record_error(p.err, kSiteConsumerFull);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t s_ahi = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                    const uint32_t s_alo = s_ahi + Cfg::A_BYTES;
+                    const uint32_t s_bhi = s_ahi + 2 * Cfg::A_BYTES;
+                    const uint32_t s_blo = s_bhi + Cfg::B_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 8; ++kk) {
-                    // K = 8 tf32 values = 32 bytes per MMA along the swizzled row.
-                    const uint32_t off = (uint32_t)kk * 32u;
-                    const uint64_t a_hi = smem_desc_k_sw128(s_ahi + off);
-                    const uint64_t a_lo = smem_desc_k_sw128(s_alo + off);
-                    const uint64_t b_hi = smem_desc_k_sw128(s_bhi + off);
-                    const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
-                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    // Small terms first, then the dominant product.
-                    mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
-                    mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
-                    mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        // K = 8 tf32 values = 32 bytes per MMA along the swizzled row.
+                        const uint32_t off = (uint32_t)kk * 32u;
+                        const uint64_t a_hi = smem_desc_k_sw128(s_ahi + off);
+                        const uint64_t a_lo = smem_desc_k_sw128(s_alo + off);
+                        const uint64_t b_hi = smem_desc_k_sw128(s_bhi + off);
+                        const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
+                        const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        // Small terms first, then the dominant product.
+                        mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
+                        mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
+                        mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
+                    }
+                    mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (!ok) break;
+                mma_commit(&tfull[ab]);             // chunk ready for the epilogue
             }
-            if (!ok) break;
-            mma_commit(&tfull[ab]);             // accumulator ready for the epilogue
         }
         // All MMAs this thread issued complete before the CTA tears down.
         mma_commit(drain);
         mbar_wait_bounded(drain, 0u, p.timeout_ns);
     } else if (warp >= 2) {
-        // ---------------- epilogue: TMEM -> registers -> C ----------------
+        // ---------------- epilogue: TMEM chunks -> FP32 sums -> C ----------------
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const float alpha = p.alpha, beta = p.beta;
-        int lt = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
-            const int ab = lt & 1;
-            const uint32_t use = (uint32_t)(lt >> 1);
-            if (!mbar_wait_bounded(&tfull[ab], use & 1u, p.timeout_ns)) {
-                record_error(p.err, kSiteConsumerFull);
-                break;
+        int gc = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            float sum[BN];
+#pragma unroll
+            for (int c = 0; c < BN; ++c) sum[c] = 0.f;
+            for (int kb0 = 0; kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB, ++gc) {
+                const int ab = gc & 1;
+                const uint32_t use = (uint32_t)(gc >> 1);
+                if (!mbar_wait_bounded(&tfull[ab], use & 1u, p.timeout_ns)) {
+                    record_error(p.err, kSiteConsumerFull);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN);
+#pragma unroll
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + (uint32_t)c0, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sum[c0 + i] += v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ab]);
             }
-            tc_fence_after();
+            if (!ok) break;
             int tm, tn;
             tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
             const int row = tm * BM + quarter * 32 + lane;
-            float *crow = p.C + (int64_t)row * p.ldc;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN);
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
-                tmem_ld_32cols(taddr + (uint32_t)c0, v);
-                if (row < p.M) {
-                    const int col0 = tn * BN + c0;
+            if (row < p.M) {
+                float *crow = p.C + (int64_t)row * p.ldc;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int col = col0 + 4 * q;
-                        if (C_VEC && col + 3 < p.N) {
-                            float4 *dst = reinterpret_cast<float4 *>(crow + col);
-                            float4 o;
-                            if constexpr (BETA_ZERO) {
-                                o = make_float4(alpha * v[4 * q], alpha * v[4 * q + 1],
-                                                alpha * v[4 * q + 2], alpha * v[4 * q + 3]);
-                            } else {
-                                const float4 c = *dst;
-                                o = make_float4(fmaf(beta, c.x, alpha * v[4 * q]),
-                                                fmaf(beta, c.y, alpha * v[4 * q + 1]),
-                                                fmaf(beta, c.z, alpha * v[4 * q + 2]),
-                                                fmaf(beta, c.w, alpha * v[4 * q + 3]));
-                            }
-                            *dst = o;
+                for (int q = 0; q < BN / 4; ++q) {
+                    const int col = tn * BN + 4 * q;
+                    if (C_VEC && col + 3 < p.N) {
+                        float4 *dst = reinterpret_cast<float4 *>(crow + col);
+                        float4 o;
+                        if constexpr (BETA_ZERO) {
+                            o = make_float4(alpha * sum[4 * q], alpha * sum[4 * q + 1],
+                                            alpha * sum[4 * q + 2], alpha * sum[4 * q + 3]);
                         } else {
+                            const float4 c = *dst;
+                            o = make_float4(fmaf(beta, c.x, alpha * sum[4 * q]),
+                                            fmaf(beta, c.y, alpha * sum[4 * q + 1]),
+                                            fmaf(beta, c.z, alpha * sum[4 * q + 2]),
+                                            fmaf(beta, c.w, alpha * sum[4 * q + 3]));
+                        }
+                        *dst = o;
+                    } else {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (col + e < p.N) {
-                                    float *dst = crow + col + e;
-                                    if constexpr (BETA_ZERO) *dst = alpha * v[4 * q + e];
-                                    else *dst = fmaf(beta, *dst, alpha * v[4 * q + e]);
-                                }
+                        for (int e = 0; e < 4; ++e) {
+                            if (col + e < p.N) {
+                                float *dst = crow + col + e;
+                                if constexpr (BETA_ZERO) *dst = alpha * sum[4 * q + e];
+                                else *dst = fmaf(beta, *dst, alpha * sum[4 * q + e]);
                             }
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[ab]);
         }
     }
 
@@ -309,7 +332,7 @@ struct Tf32x3Entries {
     }
 };
 
-using Tf32x3Cfg = Tf32x3Config<128, 3>;
+using Tf32x3Cfg = Tf32x3Config<128, 3, 2>;
 }  // namespace
 
 Tf32x3Info tf32x3_info() {
