@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--schedule", type=int, default=0,
                     help="0 automatic, 1 whole tiles per CTA, 2 stream-K")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--tensor-steps", type=int, default=100,
+                    help="steps of the 3xTF32 path reported beside the FFMA line (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
@@ -160,6 +162,25 @@ def sm_max_mhz_query(index: int) -> float | None:
         return None
 
 
+def tensor_roofline(flops: float, kernel_ms: float) -> dict:
+    """Roofline of the 3xTF32 main kernel: three TF32 products per useful
+    multiply-add, against the TF32 dense peak (the measured bf16 tensor peak
+    times the nominal TF32/bf16 ratio 1.1/2.25)."""
+    bf16 = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        basis = "of measured (bf16 burst x nominal tf32/bf16 1.1/2.25)"
+    except (OSError, KeyError, ValueError):
+        bf16 = 1900.0
+        basis = "of fallback (1.9 PFLOP/s bf16 x nominal tf32/bf16 1.1/2.25)"
+    peak = bf16 * 1.1 / 2.25
+    achieved = 3.0 * flops / (kernel_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None, "peak_basis": basis,
+            "achieved_basis": "3 TF32 MMAs per useful FMA (hi*hi, hi*lo, lo*hi); split pre-pass excluded"}
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def oracle_rows_sample(w, p, seconds: float, steps: int = 1):
@@ -246,66 +267,97 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     plan = handle.plan(A0, B0, C0, w.alpha, w.beta)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
-        A, B, C = sets[i % nsets]
-        handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
-
-    for i in range(max(args.warmup, 3)):
-        step(i)
-    torch.cuda.synchronize(dev)
-    assert handle.device_error() == 0
+    def timed_loop(steps: int, warmup: int, sample_clocks: bool):
+        """Warm up, then time `steps` calls on the device (events on the
+        launching stream) and each call's main kernel alone (events the
+        library records right around that launch)."""
+        for i in range(max(warmup, 3)):
+            A, B, C = sets[i % nsets]
+            handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
+        torch.cuda.synchronize(dev)
+        assert handle.device_error() == 0
+        kstart = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        kstop = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for e in kstart + kstop:
+            e.record(stream)          # torch creates the event on first record
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local_rank) if sample_clocks else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        t_begin = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_begin.record(stream)
+        for i in range(steps):
+            A, B, C = sets[i % nsets]
+            handle.set_kernel_events(kstart[i], kstop[i])
+            handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        handle.set_kernel_events(None, None)
+        clocks = sampler.stop() if sampler else None
+        if world > 1:
+            dist.barrier()
+        elapsed = t_begin.elapsed_time(t_end)
+        kms = [a.elapsed_time(b) for a, b in zip(kstart, kstop)]
+        assert handle.device_error() == 0
+        if world > 1:
+            t = torch.tensor([elapsed], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            elapsed = float(t.item())
+        return elapsed, kms, clocks
 
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_begin.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = t_begin.elapsed_time(t_end)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    assert handle.device_error() == 0
-
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, launch_ms, clocks = timed_loop(args.steps, args.warmup, True)
 
     flops = 2.0 * w.M * w.N * w.K
     ms_per_step = elapsed_ms / args.steps
     value = flops * world / (ms_per_step * 1e-3) / 1e12
 
-    # Roofline of the dominant (main) kernel: FFMA-bound.
     mean_launch_ms = statistics.mean(launch_ms)
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
     max_mhz = clocks.get("sm_max_mhz") or sm_max_mhz_query(local_rank) or 2070.0
-    peak = sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
     sus_mhz = clocks.get("sm_mhz")
-    peak_sus = sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
-    roofline = {
-        "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak, "traffic": profiled_traffic(),
-        "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x {max_mhz:.0f} MHz (max SM clock)",
-        "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
-        "sustained_sm_mhz": sus_mhz,
-        "kernel_ms_mean": mean_launch_ms, "kernel_ms_min": min(launch_ms),
-        "kernel_ms_median": statistics.median(launch_ms),
-    }
+    if args.math == 0:
+        # Roofline of the dominant (main) kernel: bound by the FP32 FMA pipes.
+        peak = sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
+        peak_sus = sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
+        roofline = {
+            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(),
+            "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x "
+                          f"{max_mhz:.0f} MHz (max SM clock)",
+            "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
+            "sustained_sm_mhz": sus_mhz,
+        }
+    else:
+        roofline = tensor_roofline(flops, mean_launch_ms)
+    roofline.update({"kernel_ms_mean": mean_launch_ms, "kernel_ms_min": min(launch_ms),
+                     "kernel_ms_median": statistics.median(launch_ms)})
+
+    # The tensor-core 3xTF32 path on the same inputs (reported beside the
+    # FFMA headline, which the metric defines against the FFMA peak).
+    tensor_path = None
+    if args.math == 0 and args.tensor_steps > 0:
+        handle.set_math_mode(1)
+        handle._ensure_workspace(handle.workspace_size(w.M, w.N, w.K, A0.data_ptr(), A0.stride(0),
+                                                       B0.data_ptr(), B0.stride(0)))
+        t_el, t_k, _ = timed_loop(args.tensor_steps, args.warmup, False)
+        handle.set_math_mode(0)
+        t_step = t_el / args.tensor_steps
+        tensor_path = {
+            "math": "3xTF32 (tcgen05, error-compensated; same FP32 acceptance bound)",
+            "value": flops * world / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": t_step, "steps": args.tensor_steps,
+            "launches_per_step": 3,
+            "roofline": tensor_roofline(flops, statistics.mean(t_k)),
+        }
+        tensor_path["roofline"]["kernel_ms_mean"] = statistics.mean(t_k)
 
     # End to end through the host-buffer C entry point: pinned host A, B (C),
     # copies up, product, copy of C down, all inside the timed region.
@@ -363,6 +415,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "tensor_path": tensor_path,
         "gpu_launches": args.steps * plan["launches"],
         "clocks": clocks,
     }

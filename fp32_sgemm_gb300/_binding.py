@@ -70,6 +70,7 @@ SIGNATURES = {
     "sgemmSetAlgo": (_st, [_vp, ctypes.c_int]),
     "sgemmSetSchedule": (_st, [_vp, ctypes.c_int]),
     "sgemmSetMathMode": (_st, [_vp, ctypes.c_int]),
+    "sgemmSetKernelEvents": (_st, [_vp, _vp, _vp]),
     "sgemmSetWaitTimeout": (_st, [_vp, ctypes.c_uint64]),
     "sgemmGetDeviceError": (_st, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "sgemmSelfTestWaitTimeout": (_st, [_vp, ctypes.c_uint64, _vp]),
@@ -188,6 +189,14 @@ class Handle:
 
     def set_algo(self, algo: int):
         _check(self._lib.sgemmSetAlgo(self._h, int(algo)), "sgemmSetAlgo")
+
+    def set_kernel_events(self, start, stop):
+        """Record torch.cuda.Event objects around the main kernel of later
+        calls (None, None turns it off).  The events must already have been
+        recorded once so that torch has created them."""
+        sp = start.cuda_event if start is not None else None
+        ep = stop.cuda_event if stop is not None else None
+        _check(self._lib.sgemmSetKernelEvents(self._h, sp, ep), "sgemmSetKernelEvents")
 
     def set_math_mode(self, mode: int):
         """0 FP32 FFMA (default), 1 error-compensated 3xTF32 on the tensor cores."""

@@ -74,6 +74,7 @@ struct sgemmContext {
     int algo = 0;
     int schedule = 0;   // 0 automatic, 1 whole tiles only, 2 stream-K whenever it applies
     int math = 0;       // 0 FP32 FFMA, 1 error-compensated 3xTF32 on the tensor cores
+    cudaEvent_t ev_start = nullptr, ev_stop = nullptr;   // around the main kernel, if set
 };
 
 namespace {
@@ -325,8 +326,11 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, int64_t M, int64_t N, 
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
     void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
+    if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
     cudaError_t err = cudaLaunchKernel(info.fn[pl.variant], dim3(pl.dp_ctas), dim3(info.threads),
                                        kargs, size_t(info.smem), stream);
+    if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
     return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
@@ -409,7 +413,10 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
             return SGEMM_STATUS_LAUNCH_FAILED;
     }
     void *kargs[] = {&tmA, &tmB, &args};
+    if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
     cudaError_t err = cudaLaunchKernel(e.fn, dim3(ctas), dim3(e.threads), kargs, size_t(e.smem), stream);
+    if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
     return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
@@ -601,6 +608,13 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
     if (h == nullptr || algo < 0 || algo > kNumAlgos) return SGEMM_STATUS_INVALID_VALUE;
     h->algo = algo;
+    return SGEMM_STATUS_SUCCESS;
+}
+
+sgemmStatus_t sgemmSetKernelEvents(sgemmHandle_t h, cudaEvent_t start, cudaEvent_t stop) {
+    if (h == nullptr || ((start == nullptr) != (stop == nullptr))) return SGEMM_STATUS_INVALID_VALUE;
+    h->ev_start = start;
+    h->ev_stop = stop;
     return SGEMM_STATUS_SUCCESS;
 }
 

@@ -43,6 +43,7 @@ extern "C" {
 
 #ifndef __CUDA_RUNTIME_API_H__
 typedef struct CUstream_st *cudaStream_t;
+typedef struct CUevent_st *cudaEvent_t;
 #endif
 
 typedef enum sgemmStatus {
@@ -213,6 +214,21 @@ sgemmStatus_t sgemmSetMathMode(sgemmHandle_t handle, int mode);
  *     a fixed order, so results stay deterministic).
  */
 sgemmStatus_t sgemmSetSchedule(sgemmHandle_t handle, int schedule);
+
+/*
+ * Measurement hook: when both events are non-NULL, every later call on this
+ * handle records `start` on its stream immediately before the main kernel
+ * launch and `stop` immediately after it (the repack, split and flag-reset
+ * work of the call falls outside), so cudaEventElapsedTime gives the main
+ * kernel's own duration.  The events are the caller's (created, and kept
+ * alive while calls may record them); NULL, NULL turns the hook off.  One
+ * of the two NULL is INVALID_VALUE.  The pages time whole programs with
+ * nvbench or averaged repetitions (easonhuang.dev "Results"; the HuajingLin
+ * wiki's benchmark table); this hook times the main kernel alone through the
+ * C ABI.
+ */
+sgemmStatus_t sgemmSetKernelEvents(sgemmHandle_t handle, cudaEvent_t start,
+                                   cudaEvent_t stop);
 
 /*
  * Limit, in nanoseconds, on every wait a kernel of this handle performs

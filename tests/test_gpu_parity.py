@@ -353,3 +353,26 @@ def test_bounded_wait_self_test_reports_timeout(sg):
     h.gemm(_to_dev(p.A), _to_dev(p.B), C)
     np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), _ref(p))
     h.close()
+
+
+def test_kernel_events_bracket_the_main_kernel(sg, handle):
+    p = inputs.make_problem(2048, 2048, 2048, seed=31)
+    A, B = _to_dev(p.A), _to_dev(p.B)
+    C = torch.empty((2048, 2048), device="cuda")
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    e.record()
+    torch.cuda.synchronize()
+    outer0, outer1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    handle.set_algo(0)
+    handle.set_kernel_events(s, e)
+    outer0.record()
+    handle.gemm(A, B, C)
+    outer1.record()
+    torch.cuda.synchronize()
+    handle.set_kernel_events(None, None)
+    k_ms, call_ms = s.elapsed_time(e), outer0.elapsed_time(outer1)
+    assert 0.0 < k_ms <= call_ms
+    assert k_ms > 0.05            # 17 GFLOP cannot take less than ~0.2 ms on FP32 FMA
+    with pytest.raises(sg.SgemmError):
+        handle.set_kernel_events(s, None)
