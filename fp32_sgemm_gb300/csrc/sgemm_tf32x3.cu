@@ -45,7 +45,7 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
-// A[M][lda] -> hi[M][ldh], lo[M][ldh] (first K columns).
+// A[M][lda] -> hi[M][ldh], lo[M][ldh] (first K columns), scalar.
 __global__ void split_rows_kernel(const float *__restrict__ A, int64_t lda, float *__restrict__ hi,
                                   float *__restrict__ lo, int64_t ldh, int rows, int cols) {
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
@@ -61,32 +61,63 @@ __global__ void split_rows_kernel(const float *__restrict__ A, int64_t lda, floa
     }
 }
 
-// B[K][ldb] -> hiT[N][ldh], loT[N][ldh]: 32 x 32 tiles through shared memory
-// so that both the reads (along N) and the writes (along K) are coalesced.
-__global__ void split_transpose_kernel(const float *__restrict__ B, int64_t ldb,
-                                       float *__restrict__ hiT, float *__restrict__ loT,
-                                       int64_t ldh, int K, int N) {
-    __shared__ float th[32][33];
-    __shared__ float tl[32][33];
-    const int n0 = blockIdx.x * 32;
-    const int k0 = blockIdx.y * 32;
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int k = k0 + i, n = n0 + threadIdx.x;
-        float xh = 0.f, xl = 0.f;
-        if (k < K && n < N) {
-            const float x = B[(int64_t)k * ldb + n];
-            xh = tf32_rna(x);
-            xl = tf32_rna(x - xh);
-        }
-        th[i][threadIdx.x] = xh;
-        tl[i][threadIdx.x] = xl;
+// Same, 16 bytes at a time: A 16-byte aligned, lda and cols multiples of 4.
+__global__ void split_rows_vec4_kernel(const float4 *__restrict__ A, int64_t lda4, float4 *__restrict__ hi,
+                                       float4 *__restrict__ lo, int64_t ldh4, int64_t rows, int64_t cols4) {
+    const int64_t total = rows * cols4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols4, c = i - r * cols4;
+        const float4 x = __ldcs(&A[r * lda4 + c]);
+        float4 xh, xl;
+        xh.x = tf32_rna(x.x); xl.x = tf32_rna(x.x - xh.x);
+        xh.y = tf32_rna(x.y); xl.y = tf32_rna(x.y - xh.y);
+        xh.z = tf32_rna(x.z); xl.z = tf32_rna(x.z - xh.z);
+        xh.w = tf32_rna(x.w); xl.w = tf32_rna(x.w - xh.w);
+        hi[r * ldh4 + c] = xh;
+        lo[r * ldh4 + c] = xl;
     }
+}
+
+// B[K][ldb] -> hiT[N][ldh], loT[N][ldh], through 32 (k) x 128 (n) tiles in
+// shared memory: reads along N and writes along K are both 128-byte
+// coalesced, and the padded tile (row pitch 129 words) keeps both phases
+// free of bank conflicts.  Each thread has 16 loads in flight.
+__global__ void __launch_bounds__(256)
+split_transpose_kernel(const float *__restrict__ B, int64_t ldb, float *__restrict__ hiT,
+                       float *__restrict__ loT, int64_t ldh, int K, int N) {
+    __shared__ float th[32][129];
+    __shared__ float tl[32][129];
+    const int n0 = blockIdx.x * 128;
+    const int k0 = blockIdx.y * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    float x[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = k0 + ty + 8 * i;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = n0 + tx + 32 * e;
+            x[i][e] = (k < K && n < N) ? __ldcs(&B[(int64_t)k * ldb + n]) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float xh = tf32_rna(x[i][e]);
+            th[ty + 8 * i][tx + 32 * e] = xh;
+            tl[ty + 8 * i][tx + 32 * e] = tf32_rna(x[i][e] - xh);
+        }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int n = n0 + i, k = k0 + threadIdx.x;
+    const int k = k0 + tx;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const int nl = ty + 8 * j;
+        const int n = n0 + nl;
         if (n < N && k < K) {
-            hiT[(int64_t)n * ldh + k] = th[threadIdx.x][i];
-            loT[(int64_t)n * ldh + k] = tl[threadIdx.x][i];
+            hiT[(int64_t)n * ldh + k] = th[tx][nl];
+            loT[(int64_t)n * ldh + k] = tl[tx][nl];
         }
     }
 }
@@ -350,13 +381,26 @@ Tf32x3Info tf32x3_info() {
 
 void launch_split_rows(const float *A, int64_t lda, float *hi, float *lo, int64_t ldh, int rows,
                        int cols, cudaStream_t s) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && lda % 4 == 0 && cols % 4 == 0 &&
+                     ldh % 4 == 0;
+    if (vec) {
+        const int64_t total = int64_t(rows) * (cols / 4);
+        const int64_t blocks = std::min<int64_t>(cdiv(total, 256), int64_t(sms) * 8);
+        split_rows_vec4_kernel<<<unsigned(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
+            reinterpret_cast<const float4 *>(A), lda / 4, reinterpret_cast<float4 *>(hi),
+            reinterpret_cast<float4 *>(lo), ldh / 4, rows, cols / 4);
+        return;
+    }
     dim3 grid(unsigned(std::min<int64_t>(cdiv(cols, 256), 8)), unsigned(std::min<int64_t>(rows, 65535)));
     split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, hi, lo, ldh, rows, cols);
 }
 
 void launch_split_transpose(const float *B, int64_t ldb, float *hiT, float *loT, int64_t ldh,
                             int K, int N, cudaStream_t s) {
-    dim3 grid(unsigned(cdiv(N, 32)), unsigned(cdiv(K, 32)));
+    dim3 grid(unsigned(cdiv(N, 128)), unsigned(cdiv(K, 32)));
     split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(B, ldb, hiT, loT, ldh, K, N);
 }
 
