@@ -68,6 +68,11 @@ SIGNATURES = {
     "sgemmQueryPlan": (_st, [_vp, _i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                              ctypes.POINTER(Plan)]),
     "sgemmSetAlgo": (_st, [_vp, ctypes.c_int]),
+    "sgemmStridedBatched": (_st, [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _f32, _vp, _i64,
+                                  _i64, _vp, _i64, _i64, _f32, _vp, _i64, _i64, _i64, _vp]),
+    "sgemmStridedBatchedWorkspaceSize": (_st, [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64,
+                                               _vp, _i64, _i64, _vp, _i64, _i64, _i64,
+                                               ctypes.POINTER(ctypes.c_size_t)]),
     "sgemmSetSchedule": (_st, [_vp, ctypes.c_int]),
     "sgemmSetMathMode": (_st, [_vp, ctypes.c_int]),
     "sgemmSetKernelEvents": (_st, [_vp, _vp, _vp]),
@@ -249,6 +254,45 @@ class Handle:
         _check(self._lib.sgemmQueryPlan(self._h, M, N, K, float(alpha), a, lda, b, ldb,
                                         float(beta), c, ldc, ctypes.byref(p)), "sgemmQueryPlan")
         return p.as_dict()
+
+    def gemm_batched(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, trans_a: bool = False,
+                     trans_b: bool = False, stream=None):
+        """C[z] = alpha * op(A[z]) @ op(B[z]) + beta * C[z] for every z.
+
+        A, B, C: float32 CUDA tensors of shape [batch, rows, cols] (or 2-D for
+        batch 1) as stored, row major (stride(-1) == 1); op(X) = X^T when
+        trans_x.  Batch strides come from stride(0) (0 broadcasts one matrix).
+        """
+        def mat3(t, name):
+            if t.dim() == 2:
+                t = t.unsqueeze(0)
+            if t.dim() != 3:
+                raise ValueError(f"{name} must be 2-D or 3-D")
+            ptr, ld = _matrix(t[0], name)
+            return t, ptr, ld, (t.stride(0) if t.shape[0] > 1 else 0)
+        A3, a, lda, sa = mat3(A, "A")
+        B3, b, ldb, sb = mat3(B, "B")
+        C3, c, ldc, sc = mat3(C, "C")
+        batch = C3.shape[0]
+        M, N = C3.shape[1], C3.shape[2]
+        K = A3.shape[1] if trans_a else A3.shape[2]
+        if (A3.shape[2] if trans_a else A3.shape[1]) != M or \
+                (B3.shape[2] if trans_b else B3.shape[1]) != K or \
+                (B3.shape[1] if trans_b else B3.shape[2]) != N:
+            raise ValueError("operand shapes do not match")
+        if A3.shape[0] not in (1, batch) or B3.shape[0] not in (1, batch):
+            raise ValueError("batch sizes do not match")
+        oa, ob = int(bool(trans_a)), int(bool(trans_b))
+        if M and N and K and batch and alpha != 0.0:
+            n = ctypes.c_size_t()
+            _check(self._lib.sgemmStridedBatchedWorkspaceSize(
+                self._h, oa, ob, M, N, K, a, lda, sa, b, ldb, sb, batch, ctypes.byref(n)),
+                "sgemmStridedBatchedWorkspaceSize")
+            self._ensure_workspace(n.value)
+        _check(self._lib.sgemmStridedBatched(self._h, oa, ob, M, N, K, float(alpha), a, lda, sa, b,
+                                             ldb, sb, float(beta), c, ldc, sc, batch,
+                                             _stream_ptr(stream)), "sgemmStridedBatched")
+        return C
 
     def gemm(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
         """C = alpha*A@B + beta*C in place (C: [M, N] row-major view)."""

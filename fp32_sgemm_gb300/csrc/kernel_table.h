@@ -60,6 +60,7 @@ struct Tf32x3Args {
     float alpha, beta;
     float *C;
     int64_t ldc;
+    int64_t stride_c;
     int tiles_m, tiles_n, num_tiles;
     int k_blocks;
     int group_m;
@@ -71,15 +72,16 @@ struct Tf32x3Info {
     int threads, smem, bm, bn, bk, stages;
 };
 Tf32x3Info tf32x3_info();
-void launch_split_rows(const float *A, int64_t lda, float *hi, float *lo, int64_t ldh, int rows,
-                       int cols, cudaStream_t s);
-void launch_split_transpose(const float *B, int64_t ldb, float *hiT, float *loT, int64_t ldh,
-                            int K, int N, cudaStream_t s);
-
-// Auxiliary kernels (sgemm_aux.cu).
-void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, cudaStream_t s);
-void launch_pack_rows(const float *src, int64_t ld_src, float *dst, int64_t ld_dst,
-                      int rows, int cols, cudaStream_t s);
+// Auxiliary kernels (sgemm_aux.cu); all take a batch (matrix z at base + z * stride).
+void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t stride_c, int batch,
+                    cudaStream_t s);
+void launch_pack_rows(const float *src, int64_t ld_src, int64_t s_src, float *dst, int64_t ld_dst,
+                      int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);
+// src[r][c] -> dst[c][r]; with dst2 != NULL the TF32 split: dst = hi, dst2 = lo.
+void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
+                      int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);
+void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *hi, float *lo,
+                       int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);
 void launch_wait_selftest(uint32_t *err, uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace sg

@@ -116,6 +116,25 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
         : "memory");
 }
 
+// Round an FP32 value to TF32 (10 explicit mantissa bits), to nearest with
+// ties away from zero; the result is an FP32 value whose low 13 bits are 0.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// 3-D TMA tile load (c0 innermost, c2 the batch index).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)),
+           "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 }  // namespace sg
 
 // ---------------------------------------------------------------------------

@@ -89,32 +89,85 @@ inline int64_t ceil_div(int64_t x, int64_t a) { return (x + a - 1) / a; }
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 constexpr int64_t kMaxBytes = int64_t(1) << 40;
 
+// One call in its general form: C_z = alpha * op(A_z) . op(B_z) + beta * C_z
+// for z < batch, every matrix row major; op(A) is M x K (opA == N: A stored
+// M x K; opA == T: A stored K x M), op(B) is K x N (opB == N: B stored
+// K x N; opB == T: B stored N x K); matrix z of an operand starts at
+// base + z * stride (elements).
+struct Problem {
+    int opA = 0, opB = 0;
+    int64_t M = 0, N = 0, K = 0;
+    float alpha = 1.f, beta = 0.f;
+    const float *A = nullptr;
+    int64_t lda = 0, sa = 0;
+    const float *B = nullptr;
+    int64_t ldb = 0, sb = 0;
+    float *C = nullptr;
+    int64_t ldc = 0, sc = 0;
+    int64_t batch = 1;
+
+    int64_t a_rows() const { return opA ? K : M; }   // stored A
+    int64_t a_cols() const { return opA ? M : K; }
+    int64_t b_rows() const { return opB ? N : K; }   // stored B
+    int64_t b_cols() const { return opB ? K : N; }
+    bool empty() const { return M == 0 || N == 0 || batch == 0; }
+};
+
+Problem nn_problem(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                   const float *B, int64_t ldb, float beta, const float *C, int64_t ldc) {
+    Problem q;
+    q.M = M; q.N = N; q.K = K;
+    q.alpha = alpha; q.beta = beta;
+    q.A = A; q.lda = lda;
+    q.B = B; q.ldb = ldb;
+    q.C = const_cast<float *>(C); q.ldc = ldc;
+    return q;
+}
+
 // Validation shared by every entry point.  Pure host logic: no CUDA calls.
-sgemmStatus_t validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
-                       const void *B, int64_t ldb, const void *C, int64_t ldc,
-                       bool need_ab) {
-    if (M < 0 || N < 0 || K < 0) return SGEMM_STATUS_INVALID_VALUE;
-    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) ||
-        ldc < std::max<int64_t>(1, N))
+sgemmStatus_t validate(const Problem &q, bool need_c = true) {
+    if (q.opA < 0 || q.opA > 1 || q.opB < 0 || q.opB > 1) return SGEMM_STATUS_INVALID_VALUE;
+    if (q.M < 0 || q.N < 0 || q.K < 0 || q.batch < 0) return SGEMM_STATUS_INVALID_VALUE;
+    if (q.sa < 0 || q.sb < 0 || q.sc < 0) return SGEMM_STATUS_INVALID_VALUE;
+    if (q.lda < std::max<int64_t>(1, q.a_cols()) || q.ldb < std::max<int64_t>(1, q.b_cols()) ||
+        q.ldc < std::max<int64_t>(1, q.N))
         return SGEMM_STATUS_INVALID_VALUE;
-    if (M == 0 || N == 0) return SGEMM_STATUS_SUCCESS;
-    if (C == nullptr) return SGEMM_STATUS_INVALID_VALUE;
-    if (need_ab && K > 0 && (A == nullptr || B == nullptr)) return SGEMM_STATUS_INVALID_VALUE;
-    if (!aligned(C, 4)) return SGEMM_STATUS_MISALIGNED;
-    if (need_ab && K > 0 && (!aligned(A, 4) || !aligned(B, 4))) return SGEMM_STATUS_MISALIGNED;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
-    if (lda > kMaxBytes / 4 || ldb > kMaxBytes / 4 || ldc > kMaxBytes / 4)
+    if (q.empty()) return SGEMM_STATUS_SUCCESS;
+    const bool need_ab = q.alpha != 0.0f && q.K > 0;
+    if (need_c && q.C == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    if (need_ab && (q.A == nullptr || q.B == nullptr)) return SGEMM_STATUS_INVALID_VALUE;
+    if (need_c && !aligned(q.C, 4)) return SGEMM_STATUS_MISALIGNED;
+    if (need_ab && (!aligned(q.A, 4) || !aligned(q.B, 4))) return SGEMM_STATUS_MISALIGNED;
+    if (q.M > kMaxDim || q.N > kMaxDim || q.K > kMaxDim || q.batch > kMaxDim)
+        return SGEMM_STATUS_NOT_SUPPORTED;
+    if (q.lda > kMaxBytes / 4 || q.ldb > kMaxBytes / 4 || q.ldc > kMaxBytes / 4 ||
+        q.sa > kMaxBytes / 4 || q.sb > kMaxBytes / 4 || q.sc > kMaxBytes / 4)
         return SGEMM_STATUS_NOT_SUPPORTED;
     return SGEMM_STATUS_SUCCESS;
 }
 
+sgemmStatus_t validate(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                       const void *B, int64_t ldb, const void *C, int64_t ldc, bool need_ab) {
+    Problem q = nn_problem(M, N, K, need_ab ? 1.f : 0.f, static_cast<const float *>(A), lda,
+                           static_cast<const float *>(B), ldb, 0.f, static_cast<const float *>(C), ldc);
+    return validate(q);
+}
+
 inline bool tma_ok(const void *p, int64_t ld) { return aligned(p, 16) && (ld % 4) == 0; }
+// Operand readable in place by 3-D TMA: base 16-byte aligned, row pitch and
+// (for a real batch) batch stride multiples of 16 bytes.
+inline bool tma_ok_batched(const void *p, int64_t ld, int64_t stride, int64_t batch) {
+    return tma_ok(p, ld) && (batch == 1 || (stride % 4 == 0 && stride > 0));
+}
 
 struct Plan {
     sgemmPlan_t pub{};
     int algo_index = -1;   // row of g_kernels
     int variant = 0;       // column of g_kernels
-    int64_t lda_p = 0, ldb_p = 0;
+    // FFMA path: how each operand reaches TMA (0 in place, 1 repacked rows,
+    // 2 transposed into the workspace) and its pitch / batch stride there.
+    int prep_a = 0, prep_b = 0;
+    int64_t lda_p = 0, ldb_p = 0, sa_p = 0, sb_p = 0;
     size_t ws_a = 0, ws_b = 0;      // repacked A / B
     size_t ws_flags = 0, ws_partials = 0;   // stream-K scratch (0 when not used)
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 8;
@@ -122,6 +175,7 @@ struct Plan {
     int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
     int sk_tile0 = 0;               // first tile of the stream-K part
     int64_t kp = 0;                 // 3xTF32: row pitch of the split operands
+    size_t ws_split_a = 0, ws_split_b = 0;   // 3xTF32: bytes of one part (hi or lo)
     size_t ws_split = 0;            // 3xTF32: A_hi, A_lo, B_hi^T, B_lo^T
 };
 
@@ -130,9 +184,8 @@ struct Plan {
 // fastest at 1024^3 to 8192^3; it is the automatic choice for every shape.
 constexpr int kDefaultAlgo = 10;
 
-int choose_algo(const sgemmContext *h, int64_t M, int64_t N, int64_t K) {
+int choose_algo(const sgemmContext *h) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
-    (void)M; (void)N; (void)K;
     return kDefaultAlgo - 1;
 }
 
@@ -152,23 +205,28 @@ int occupancy_for(const sgemmContext *h, KernelEntry &e) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+bool c_vector_ok(const Problem &q) {
+    return tma_ok(q.C, q.ldc) && (q.batch == 1 || q.sc % 4 == 0);
+}
+
 // 3xTF32 plan: operands are always split into the workspace (TF32 hi and lo
-// parts, B transposed), so any pitch and alignment of A and B is accepted.
-sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, int64_t M, int64_t N, int64_t K,
-                               const float *C, int64_t ldc, float beta, Plan &pl) {
+// parts, K contiguous), so any layout, pitch and alignment of A and B works.
+sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl) {
     const sg::Tf32x3Info info = sg::tf32x3_info();
     pl.pub.kind = 3;
-    pl.pub.vector_epilogue = tma_ok(C, ldc) ? 1 : 0;
-    pl.variant = (beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
-    pl.kp = round_up(K, 4);
-    if (ceil_div(K, 32) > 65535) return SGEMM_STATUS_NOT_SUPPORTED;   // split grid
-    pl.ws_split = 2 * align256(size_t(M) * size_t(pl.kp) * 4) + 2 * align256(size_t(N) * size_t(pl.kp) * 4);
-    pl.tiles_m = int(ceil_div(M, info.bm));
-    pl.tiles_n = int(ceil_div(N, info.bn));
-    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n;
+    pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
+    pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
+    pl.kp = round_up(q.K, 4);
+    if (ceil_div(q.K, 32) > 65535 || ceil_div(q.M, 32) > 65535) return SGEMM_STATUS_NOT_SUPPORTED;
+    pl.ws_split_a = align256(size_t(q.batch) * size_t(q.M) * size_t(pl.kp) * 4);
+    pl.ws_split_b = align256(size_t(q.batch) * size_t(q.N) * size_t(pl.kp) * 4);
+    pl.ws_split = 2 * pl.ws_split_a + 2 * pl.ws_split_b;
+    pl.tiles_m = int(ceil_div(q.M, info.bm));
+    pl.tiles_n = int(ceil_div(q.N, info.bn));
+    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * q.batch;
     if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.num_tiles = int(tiles);
-    pl.k_blocks = int(ceil_div(K, info.bk));
+    pl.k_blocks = int(ceil_div(q.K, info.bk));
     static std::mutex occ_mutex;
     static int occ_cache[kMaxDevices][4] = {};
     int occ = 0;
@@ -197,41 +255,56 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, int64_t M, int64_t N, int6
     return SGEMM_STATUS_SUCCESS;
 }
 
-sgemmStatus_t encode_2d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer,
-                        int64_t ld, int box_inner, int box_outer, CUtensorMapSwizzle swz);
-
-// Plan of one call: repacking, kernel variant, grid and stream-K split.
-// Queries the kernel's occupancy once per device (a CUDA call); everything
-// else is host arithmetic.
-sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
-                        const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
-                        const float *C, int64_t ldc, Plan &pl) {
+// Plan of one call: operand preparation, kernel variant, grid and stream-K
+// split.  Queries the kernel's occupancy once per device (a CUDA call);
+// everything else is host arithmetic.
+sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     pl = Plan{};
-    if (M == 0 || N == 0) return SGEMM_STATUS_SUCCESS;
-    if (K == 0 || alpha == 0.0f) {
+    if (q.empty()) return SGEMM_STATUS_SUCCESS;
+    if (q.K == 0 || q.alpha == 0.0f) {
         pl.pub.kind = 2;
         pl.pub.launches = 1;
         return SGEMM_STATUS_SUCCESS;
     }
     std::call_once(g_kernels_once, init_kernel_table);
-    if (h->math == 1) return make_plan_tf32x3(h, M, N, K, C, ldc, beta, pl);
+    if (h->math == 1) return make_plan_tf32x3(h, q, pl);
     pl.pub.kind = 1;
-    pl.pub.packs_a = tma_ok(A, lda) ? 0 : 1;
-    pl.pub.packs_b = tma_ok(B, ldb) ? 0 : 1;
-    pl.pub.vector_epilogue = tma_ok(C, ldc) ? 1 : 0;
-    pl.lda_p = pl.pub.packs_a ? round_up(K, 4) : lda;
-    pl.ldb_p = pl.pub.packs_b ? round_up(N, 4) : ldb;
-    pl.ws_a = pl.pub.packs_a ? align256(size_t(M) * size_t(pl.lda_p) * 4) : 0;
-    pl.ws_b = pl.pub.packs_b ? align256(size_t(K) * size_t(pl.ldb_p) * 4) : 0;
-    pl.algo_index = choose_algo(h, M, N, K);
-    pl.variant = (beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
+    // A as TMA reads it: [batch][M][K] rows of K.
+    if (q.opA == 0 && tma_ok_batched(q.A, q.lda, q.sa, q.batch)) {
+        pl.prep_a = 0;
+        pl.lda_p = q.lda;
+        pl.sa_p = q.batch == 1 ? round_up(q.M * q.lda, 4) : q.sa;
+    } else {
+        pl.prep_a = q.opA == 0 ? 1 : 2;
+        pl.lda_p = round_up(q.K, 4);
+        pl.sa_p = q.M * pl.lda_p;
+        pl.ws_a = align256(size_t(q.batch) * size_t(pl.sa_p) * 4);
+    }
+    // B as TMA reads it: [batch][K][N] rows of N.
+    if (q.opB == 0 && tma_ok_batched(q.B, q.ldb, q.sb, q.batch)) {
+        pl.prep_b = 0;
+        pl.ldb_p = q.ldb;
+        pl.sb_p = q.batch == 1 ? round_up(q.K * q.ldb, 4) : q.sb;
+    } else {
+        pl.prep_b = q.opB == 0 ? 1 : 2;
+        pl.ldb_p = round_up(q.N, 4);
+        pl.sb_p = q.K * pl.ldb_p;
+        pl.ws_b = align256(size_t(q.batch) * size_t(pl.sb_p) * 4);
+    }
+    if ((pl.prep_a == 2 && ceil_div(q.K, 32) > 65535) || (pl.prep_b == 2 && ceil_div(q.N, 32) > 65535))
+        return SGEMM_STATUS_NOT_SUPPORTED;   // transpose grid
+    pl.pub.packs_a = pl.prep_a != 0;
+    pl.pub.packs_b = pl.prep_b != 0;
+    pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
+    pl.algo_index = choose_algo(h);
+    pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
-    pl.tiles_m = int(ceil_div(M, e.bm));
-    pl.tiles_n = int(ceil_div(N, e.bn));
-    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n;
+    pl.tiles_m = int(ceil_div(q.M, e.bm));
+    pl.tiles_n = int(ceil_div(q.N, e.bn));
+    const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * q.batch;
     if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.num_tiles = int(tiles);
-    pl.k_blocks = int(ceil_div(K, e.bk));
+    pl.k_blocks = int(ceil_div(q.K, e.bk));
     const int occ = occupancy_for(h, e);
     if (occ < 1) return SGEMM_STATUS_LAUNCH_FAILED;
     const int64_t slots = int64_t(h->sm_count) * occ;
@@ -261,15 +334,24 @@ sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, 
     return SGEMM_STATUS_SUCCESS;
 }
 
-sgemmStatus_t encode_2d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer,
-                        int64_t ld, int box_inner, int box_outer, CUtensorMapSwizzle swz) {
+sgemmStatus_t make_plan(const sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                        const float *C, int64_t ldc, Plan &pl) {
+    return make_plan(h, nn_problem(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc), pl);
+}
+
+// 3-D tiled tensor map over FP32 data: dims {inner, outer, batch}, row pitch
+// ld and batch stride in elements (both multiples of 4), box {bi, bo, 1}.
+sgemmStatus_t encode_3d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer,
+                        int64_t batch, int64_t ld, int64_t bstride, int box_inner, int box_outer,
+                        CUtensorMapSwizzle swz) {
     auto enc = encode_fn();
     if (enc == nullptr) return SGEMM_STATUS_LAUNCH_FAILED;
-    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
-    cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
-    cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims,
+    cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(outer), cuuint64_t(batch)};
+    cuuint64_t strides[2] = {cuuint64_t(ld) * 4, cuuint64_t(bstride) * 4};
+    cuuint32_t box[3] = {cuuint32_t(box_inner), cuuint32_t(box_outer), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
@@ -280,44 +362,55 @@ CUtensorMapSwizzle swizzle_for_bk(int bk) {
                     : bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
-sgemmStatus_t launch_pack(const float *src, int64_t ld_src, float *dst, int64_t ld_dst,
-                          int64_t rows, int64_t cols, cudaStream_t stream) {
-    sg::launch_pack_rows(src, ld_src, dst, ld_dst, int(rows), int(cols), stream);
+inline sgemmStatus_t last_launch() {
     return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
-sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, int64_t M, int64_t N, int64_t K,
-                         float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
-                         float beta, float *C, int64_t ldc, cudaStream_t stream) {
+sgemmStatus_t launch_main(sgemmContext *h, const void *fn, int ctas, int threads, int smem,
+                          void **kargs, cudaStream_t stream) {
+    if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    cudaError_t err = cudaLaunchKernel(fn, dim3(ctas), dim3(threads), kargs, size_t(smem), stream);
+    if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
+    return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cudaStream_t stream) {
     if (h->ws == nullptr || h->ws_bytes < pl.ws_split) return SGEMM_STATUS_WORKSPACE_REQUIRED;
     const sg::Tf32x3Info info = sg::tf32x3_info();
     char *ws = static_cast<char *>(h->ws);
-    const size_t a_bytes = align256(size_t(M) * size_t(pl.kp) * 4);
-    const size_t b_bytes = align256(size_t(N) * size_t(pl.kp) * 4);
     float *a_hi = reinterpret_cast<float *>(ws);
-    float *a_lo = reinterpret_cast<float *>(ws + a_bytes);
-    float *b_hi = reinterpret_cast<float *>(ws + 2 * a_bytes);
-    float *b_lo = reinterpret_cast<float *>(ws + 2 * a_bytes + b_bytes);
-    sg::launch_split_rows(A, lda, a_hi, a_lo, pl.kp, int(M), int(K), stream);
-    sg::launch_split_transpose(B, ldb, b_hi, b_lo, pl.kp, int(K), int(N), stream);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    float *a_lo = reinterpret_cast<float *>(ws + pl.ws_split_a);
+    float *b_hi = reinterpret_cast<float *>(ws + 2 * pl.ws_split_a);
+    float *b_lo = reinterpret_cast<float *>(ws + 2 * pl.ws_split_a + pl.ws_split_b);
+    const int M = int(q.M), N = int(q.N), K = int(q.K), batch = int(q.batch);
+    const int64_t sa_d = q.M * pl.kp, sb_d = q.N * pl.kp;
+    // A_hi / A_lo as [batch][M][kp] and B_hi / B_lo as [batch][N][kp]: K
+    // contiguous for both, whatever the stored layout.
+    if (q.opA == 0) sg::launch_split_rows(q.A, q.lda, q.sa, a_hi, a_lo, pl.kp, sa_d, M, K, batch, stream);
+    else sg::launch_transpose(q.A, q.lda, q.sa, a_hi, a_lo, pl.kp, sa_d, K, M, batch, stream);
+    if (q.opB == 0) sg::launch_transpose(q.B, q.ldb, q.sb, b_hi, b_lo, pl.kp, sb_d, K, N, batch, stream);
+    else sg::launch_split_rows(q.B, q.ldb, q.sb, b_hi, b_lo, pl.kp, sb_d, N, K, batch, stream);
+    if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
 
     CUtensorMap tm[4];
     const float *ptrs[4] = {a_hi, a_lo, b_hi, b_lo};
     for (int i = 0; i < 4; ++i) {
         const bool is_a = i < 2;
-        sgemmStatus_t st = encode_2d(&tm[i], ptrs[i], K, is_a ? M : N, pl.kp, info.bk,
-                                     is_a ? info.bm : info.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        sgemmStatus_t st = encode_3d(&tm[i], ptrs[i], q.K, is_a ? q.M : q.N, q.batch, pl.kp,
+                                     is_a ? sa_d : sb_d, info.bk, is_a ? info.bm : info.bn,
+                                     CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != SGEMM_STATUS_SUCCESS) return st;
     }
     sg::Tf32x3Args args{};
-    args.M = int(M);
-    args.N = int(N);
-    args.K = int(K);
-    args.alpha = alpha;
-    args.beta = beta;
-    args.C = C;
-    args.ldc = ldc;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.alpha = q.alpha;
+    args.beta = q.beta;
+    args.C = q.C;
+    args.ldc = q.ldc;
+    args.stride_c = q.sc;
     args.tiles_m = pl.tiles_m;
     args.tiles_n = pl.tiles_n;
     args.num_tiles = pl.num_tiles;
@@ -326,22 +419,15 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, int64_t M, int64_t N, 
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
     void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
-    if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
-        return SGEMM_STATUS_LAUNCH_FAILED;
-    cudaError_t err = cudaLaunchKernel(info.fn[pl.variant], dim3(pl.dp_ctas), dim3(info.threads),
-                                       kargs, size_t(info.smem), stream);
-    if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
-    return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+    return launch_main(h, info.fn[pl.variant], pl.dp_ctas, info.threads, info.smem, kargs, stream);
 }
 
-sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                  int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-                  cudaStream_t stream) {
-    sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
-    if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
+    sgemmStatus_t st = validate(q);
+    if (st != SGEMM_STATUS_SUCCESS || q.empty()) return st;
     if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
     Plan pl;
-    st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
+    st = make_plan(h, q, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
 
     int cur = -1;
@@ -349,49 +435,51 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
     if (cur != h->device) return SGEMM_STATUS_INVALID_VALUE;
 
     if (pl.pub.kind == 2) {
-        sg::launch_scale_c(int(M), int(N), beta, C, ldc, stream);
-        return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+        sg::launch_scale_c(int(q.M), int(q.N), q.beta, q.C, q.ldc, q.sc, int(q.batch), stream);
+        return last_launch();
     }
+    if (pl.pub.kind == 3) return run_tf32x3(h, pl, q, stream);
 
-    if (pl.pub.kind == 3) return run_tf32x3(h, pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
-
-    const float *Ause = A, *Buse = B;
+    const float *Ause = q.A, *Buse = q.B;
     // Stream-K scratch is optional: without room for it, whole tiles are used.
     const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
                         h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
-    if (pl.pub.packs_a || pl.pub.packs_b) {
+    const int M = int(q.M), N = int(q.N), K = int(q.K), batch = int(q.batch);
+    if (pl.prep_a || pl.prep_b) {
         if (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b) return SGEMM_STATUS_WORKSPACE_REQUIRED;
         char *ws = static_cast<char *>(h->ws);
-        if (pl.pub.packs_a) {
+        if (pl.prep_a) {
             float *Ap = reinterpret_cast<float *>(ws);
-            st = launch_pack(A, lda, Ap, pl.lda_p, M, K, stream);
-            if (st != SGEMM_STATUS_SUCCESS) return st;
+            if (pl.prep_a == 1) sg::launch_pack_rows(q.A, q.lda, q.sa, Ap, pl.lda_p, pl.sa_p, M, K, batch, stream);
+            else sg::launch_transpose(q.A, q.lda, q.sa, Ap, nullptr, pl.lda_p, pl.sa_p, K, M, batch, stream);
             Ause = Ap;
         }
-        if (pl.pub.packs_b) {
+        if (pl.prep_b) {
             float *Bp = reinterpret_cast<float *>(ws + pl.ws_a);
-            st = launch_pack(B, ldb, Bp, pl.ldb_p, K, N, stream);
-            if (st != SGEMM_STATUS_SUCCESS) return st;
+            if (pl.prep_b == 1) sg::launch_pack_rows(q.B, q.ldb, q.sb, Bp, pl.ldb_p, pl.sb_p, K, N, batch, stream);
+            else sg::launch_transpose(q.B, q.ldb, q.sb, Bp, nullptr, pl.ldb_p, pl.sb_p, N, K, batch, stream);
             Buse = Bp;
         }
+        if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
     }
 
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
 
     CUtensorMap tmA, tmB;
-    st = encode_2d(&tmA, Ause, K, M, pl.lda_p, e.bk, e.bm, swizzle_for_bk(e.bk));
+    st = encode_3d(&tmA, Ause, q.K, q.M, q.batch, pl.lda_p, pl.sa_p, e.bk, e.bm, swizzle_for_bk(e.bk));
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    st = encode_2d(&tmB, Buse, N, K, pl.ldb_p, e.bn, e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = encode_3d(&tmB, Buse, q.N, q.K, q.batch, pl.ldb_p, pl.sb_p, e.bn, e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != SGEMM_STATUS_SUCCESS) return st;
 
     sg::GemmArgs args{};
-    args.M = int(M);
-    args.N = int(N);
-    args.K = int(K);
-    args.alpha = alpha;
-    args.beta = beta;
-    args.C = C;
-    args.ldc = ldc;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.alpha = q.alpha;
+    args.beta = q.beta;
+    args.C = q.C;
+    args.ldc = q.ldc;
+    args.stride_c = q.sc;
     args.tiles_m = pl.tiles_m;
     args.tiles_n = pl.tiles_n;
     args.num_tiles = pl.num_tiles;
@@ -413,11 +501,17 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
             return SGEMM_STATUS_LAUNCH_FAILED;
     }
     void *kargs[] = {&tmA, &tmB, &args};
-    if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
-        return SGEMM_STATUS_LAUNCH_FAILED;
-    cudaError_t err = cudaLaunchKernel(e.fn, dim3(ctas), dim3(e.threads), kargs, size_t(e.smem), stream);
-    if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
-    return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+    return launch_main(h, e.fn, ctas, e.threads, e.smem, kargs, stream);
+}
+
+sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                  int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                  cudaStream_t stream) {
+    return run(h, nn_problem(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc), stream);
+}
+
+size_t workspace_bytes(const Plan &pl) {
+    return pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials + pl.ws_split;
 }
 
 }  // namespace
@@ -538,6 +632,58 @@ sgemmStatus_t sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A
     st = sgemmGetDefaultHandle(&h);
     if (st != SGEMM_STATUS_SUCCESS) return st;
     return run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+namespace {
+Problem general_problem(int opA, int opB, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, int64_t sa, const float *B, int64_t ldb,
+                        int64_t sb, float beta, float *C, int64_t ldc, int64_t sc, int64_t batch) {
+    Problem q;
+    q.opA = opA; q.opB = opB;
+    q.M = M; q.N = N; q.K = K;
+    q.alpha = alpha; q.beta = beta;
+    q.A = A; q.lda = lda; q.sa = sa;
+    q.B = B; q.ldb = ldb; q.sb = sb;
+    q.C = C; q.ldc = ldc; q.sc = sc;
+    q.batch = batch;
+    return q;
+}
+}  // namespace
+
+sgemmStatus_t sgemmStridedBatched(sgemmHandle_t h, sgemmOperation_t opA, sgemmOperation_t opB,
+                                  int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                  int64_t lda, int64_t strideA, const float *B, int64_t ldb,
+                                  int64_t strideB, float beta, float *C, int64_t ldc, int64_t strideC,
+                                  int64_t batchCount, cudaStream_t stream) {
+    const Problem q = general_problem(int(opA), int(opB), M, N, K, alpha, A, lda, strideA, B, ldb,
+                                      strideB, beta, C, ldc, strideC, batchCount);
+    sgemmStatus_t st = validate(q);
+    if (st != SGEMM_STATUS_SUCCESS || q.empty()) return st;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    return run(h, q, stream);
+}
+
+sgemmStatus_t sgemmStridedBatchedWorkspaceSize(sgemmHandle_t h, sgemmOperation_t opA,
+                                               sgemmOperation_t opB, int64_t M, int64_t N, int64_t K,
+                                               const float *A, int64_t lda, int64_t strideA,
+                                               const float *B, int64_t ldb, int64_t strideB,
+                                               int64_t batchCount, size_t *bytes) {
+    if (bytes == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *bytes = 0;
+    const float dummy_c = 0.f;
+    const Problem q = general_problem(int(opA), int(opB), M, N, K, 1.0f, A, lda, strideA, B, ldb,
+                                      strideB, 0.0f, const_cast<float *>(&dummy_c),
+                                      std::max<int64_t>(1, N), 0, batchCount);
+    sgemmStatus_t st = validate(q);
+    if (st != SGEMM_STATUS_SUCCESS || q.empty() || K == 0) return st;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    Plan pl;
+    Problem qc = q;
+    qc.C = nullptr;
+    st = make_plan(h, qc, pl);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
+    *bytes = workspace_bytes(pl);
+    return SGEMM_STATUS_SUCCESS;
 }
 
 sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K, size_t *bytes) {

@@ -53,7 +53,8 @@ struct GemmArgs {
     float alpha, beta;
     float *C;
     int64_t ldc;
-    int tiles_m, tiles_n, num_tiles;
+    int64_t stride_c;     // elements between the C matrices of consecutive batches
+    int tiles_m, tiles_n, num_tiles;   // num_tiles = batch * tiles_m * tiles_n
     int k_blocks;
     int group_m;          // rasterisation: tile rows per band
     int sk_tile0;         // tiles [0, sk_tile0) whole, round robin; [sk_tile0, num_tiles) stream-K
@@ -119,8 +120,14 @@ struct FfmaConfig {
     static_assert(STAGES >= 2, "ring depth");
 };
 
+// Tile t -> (batch b, tile row tm, tile column tn).  Inside a batch, tiles
+// are walked in bands of group_m tile rows, column by column, so that the
+// tiles running at the same time share rows of A and columns of B in L2.
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
-                                            int &tm, int &tn) {
+                                            int &b, int &tm, int &tn) {
+    const int per_batch = tiles_m * tiles_n;
+    b = t / per_batch;
+    t -= b * per_batch;
     const int per_group = group_m * tiles_n;
     const int g = t / per_group;
     const int first_m = g * group_m;
@@ -190,7 +197,7 @@ struct SliceCursor {
     WorkIter it;
     Segment seg;
     int valid;
-    int kb, tm, tn;
+    int kb, bt, tm, tn;
     int stage;
     uint32_t phase;
     int issued;
@@ -219,8 +226,8 @@ __device__ __forceinline__ void cursor_begin(SliceCursor *sc, const GemmArgs &p)
     c.it.begin(p);
     c.valid = c.it.get(p, c.seg) ? 1 : 0;
     c.kb = c.seg.kb0;
-    c.tm = c.tn = 0;
-    if (c.valid) tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.tm, c.tn);
+    c.bt = c.tm = c.tn = 0;
+    if (c.valid) tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.bt, c.tm, c.tn);
     c.stage = 0;
     c.phase = 0;
     c.issued = 0;
@@ -243,8 +250,8 @@ __device__ __forceinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
     SliceCursor c = cursor_load(sc);
     if (!mbar_wait_bounded(&empty[c.stage], c.phase ^ 1u, p.timeout_ns)) return false;
     mbar_arrive_expect_tx(&full[c.stage], Cfg::STAGE_BYTES);
-    tma_load_2d(sA + c.stage * Cfg::A_STAGE_BYTES, tmA, &full[c.stage], c.kb * Cfg::BK, c.tm * Cfg::BM);
-    tma_load_2d(sB + c.stage * Cfg::B_STAGE_BYTES, tmB, &full[c.stage], c.tn * Cfg::BN, c.kb * Cfg::BK);
+    tma_load_3d(sA + c.stage * Cfg::A_STAGE_BYTES, tmA, &full[c.stage], c.kb * Cfg::BK, c.tm * Cfg::BM, c.bt);
+    tma_load_3d(sB + c.stage * Cfg::B_STAGE_BYTES, tmB, &full[c.stage], c.tn * Cfg::BN, c.kb * Cfg::BK, c.bt);
     ++c.issued;
     if (++c.stage == Cfg::STAGES) { c.stage = 0; c.phase ^= 1u; }
     if (++c.kb == c.seg.kb1) {
@@ -252,7 +259,7 @@ __device__ __forceinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
         c.valid = c.it.get(p, c.seg) ? 1 : 0;
         if (c.valid) {
             c.kb = c.seg.kb0;
-            tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.tm, c.tn);
+            tile_coords(c.seg.t, p.tiles_m, p.tiles_n, p.group_m, c.bt, c.tm, c.tn);
         }
     }
     cursor_store(sc, c);
@@ -403,8 +410,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     int stage = 0;
     uint32_t phase = 0;
     while (it.get(p, seg)) {
-        int tm, tn;
-        tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        int bt, tm, tn;
+        tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
 
 #pragma unroll
         for (int i = 0; i < TM; ++i)
@@ -530,7 +537,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int i = 0; i < TM; ++i) {
             const int row = tm * BM + row0 + WR * i;
             if (row >= p.M) continue;
-            float *crow = p.C + (int64_t)row * p.ldc;
+            float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
                 const int col = tn * BN + col0 + 4 * WC * j;

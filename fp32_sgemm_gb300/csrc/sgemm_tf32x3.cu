@@ -39,89 +39,6 @@
 
 namespace sg {
 
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-// A[M][lda] -> hi[M][ldh], lo[M][ldh] (first K columns), scalar.
-__global__ void split_rows_kernel(const float *__restrict__ A, int64_t lda, float *__restrict__ hi,
-                                  float *__restrict__ lo, int64_t ldh, int rows, int cols) {
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-        const float *src = A + r * lda;
-        float *h = hi + r * ldh;
-        float *l = lo + r * ldh;
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
-            const float x = src[c];
-            const float xh = tf32_rna(x);
-            h[c] = xh;
-            l[c] = tf32_rna(x - xh);
-        }
-    }
-}
-
-// Same, 16 bytes at a time: A 16-byte aligned, lda and cols multiples of 4.
-__global__ void split_rows_vec4_kernel(const float4 *__restrict__ A, int64_t lda4, float4 *__restrict__ hi,
-                                       float4 *__restrict__ lo, int64_t ldh4, int64_t rows, int64_t cols4) {
-    const int64_t total = rows * cols4;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / cols4, c = i - r * cols4;
-        const float4 x = __ldcs(&A[r * lda4 + c]);
-        float4 xh, xl;
-        xh.x = tf32_rna(x.x); xl.x = tf32_rna(x.x - xh.x);
-        xh.y = tf32_rna(x.y); xl.y = tf32_rna(x.y - xh.y);
-        xh.z = tf32_rna(x.z); xl.z = tf32_rna(x.z - xh.z);
-        xh.w = tf32_rna(x.w); xl.w = tf32_rna(x.w - xh.w);
-        hi[r * ldh4 + c] = xh;
-        lo[r * ldh4 + c] = xl;
-    }
-}
-
-// B[K][ldb] -> hiT[N][ldh], loT[N][ldh], through 32 (k) x 128 (n) tiles in
-// shared memory: reads along N and writes along K are both 128-byte
-// coalesced, and the padded tile (row pitch 129 words) keeps both phases
-// free of bank conflicts.  Each thread has 16 loads in flight.
-__global__ void __launch_bounds__(256)
-split_transpose_kernel(const float *__restrict__ B, int64_t ldb, float *__restrict__ hiT,
-                       float *__restrict__ loT, int64_t ldh, int K, int N) {
-    __shared__ float th[32][129];
-    __shared__ float tl[32][129];
-    const int n0 = blockIdx.x * 128;
-    const int k0 = blockIdx.y * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
-    float x[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int k = k0 + ty + 8 * i;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int n = n0 + tx + 32 * e;
-            x[i][e] = (k < K && n < N) ? __ldcs(&B[(int64_t)k * ldb + n]) : 0.f;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float xh = tf32_rna(x[i][e]);
-            th[ty + 8 * i][tx + 32 * e] = xh;
-            tl[ty + 8 * i][tx + 32 * e] = tf32_rna(x[i][e] - xh);
-        }
-    __syncthreads();
-    const int k = k0 + tx;
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const int nl = ty + 8 * j;
-        const int n = n0 + nl;
-        if (n < N && k < K) {
-            hiT[(int64_t)n * ldh + k] = th[tx][nl];
-            loT[(int64_t)n * ldh + k] = tl[tx][nl];
-        }
-    }
-}
-
 template <int BN_, int STAGES_, int CHUNK_KB_>
 struct Tf32x3Config {
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
@@ -190,8 +107,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         int issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            int bt, tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                     record_error(p.err, kSiteProducerEmpty);
@@ -200,10 +117,10 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 }
                 unsigned char *st = smem + stage * Cfg::STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                tma_load_2d(st, &tmAhi, &full[stage], kb * BK, tm * BM);
-                tma_load_2d(st + Cfg::A_BYTES, &tmAlo, &full[stage], kb * BK, tm * BM);
-                tma_load_2d(st + 2 * Cfg::A_BYTES, &tmBhi, &full[stage], kb * BK, tn * BN);
-                tma_load_2d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, &full[stage], kb * BK, tn * BN);
+                tma_load_3d(st, &tmAhi, &full[stage], kb * BK, tm * BM, bt);
+                tma_load_3d(st + Cfg::A_BYTES, &tmAlo, &full[stage], kb * BK, tm * BM, bt);
+                tma_load_3d(st + 2 * Cfg::A_BYTES, &tmBhi, &full[stage], kb * BK, tn * BN, bt);
+                tma_load_3d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, &full[stage], kb * BK, tn * BN, bt);
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -303,11 +220,11 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 if (lane == 0) mbar_arrive(&tempty[ab]);
             }
             if (!ok) break;
-            int tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            int bt, tm, tn;
+            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
             const int row = tm * BM + quarter * 32 + lane;
             if (row < p.M) {
-                float *crow = p.C + (int64_t)row * p.ldc;
+                float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
                 for (int q = 0; q < BN / 4; ++q) {
                     const int col = tn * BN + 4 * q;
@@ -377,31 +294,6 @@ Tf32x3Info tf32x3_info() {
     info.bk = Tf32x3Cfg::BK;
     info.stages = Tf32x3Cfg::STAGES;
     return info;
-}
-
-void launch_split_rows(const float *A, int64_t lda, float *hi, float *lo, int64_t ldh, int rows,
-                       int cols, cudaStream_t s) {
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && lda % 4 == 0 && cols % 4 == 0 &&
-                     ldh % 4 == 0;
-    if (vec) {
-        const int64_t total = int64_t(rows) * (cols / 4);
-        const int64_t blocks = std::min<int64_t>(cdiv(total, 256), int64_t(sms) * 8);
-        split_rows_vec4_kernel<<<unsigned(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
-            reinterpret_cast<const float4 *>(A), lda / 4, reinterpret_cast<float4 *>(hi),
-            reinterpret_cast<float4 *>(lo), ldh / 4, rows, cols / 4);
-        return;
-    }
-    dim3 grid(unsigned(std::min<int64_t>(cdiv(cols, 256), 8)), unsigned(std::min<int64_t>(rows, 65535)));
-    split_rows_kernel<<<grid, 256, 0, s>>>(A, lda, hi, lo, ldh, rows, cols);
-}
-
-void launch_split_transpose(const float *B, int64_t ldb, float *hiT, float *loT, int64_t ldh,
-                            int K, int N, cudaStream_t s) {
-    dim3 grid(unsigned(cdiv(N, 128)), unsigned(cdiv(K, 32)));
-    split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(B, ldb, hiT, loT, ldh, K, N);
 }
 
 }  // namespace sg

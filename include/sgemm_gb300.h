@@ -60,6 +60,13 @@ typedef enum sgemmStatus {
 
 typedef struct sgemmContext *sgemmHandle_t;
 
+/* Operand form for sgemmStridedBatched: the operand as stored (N) or its
+ * transpose (T), both row major. */
+typedef enum sgemmOperation {
+    SGEMM_OP_N = 0,
+    SGEMM_OP_T = 1
+} sgemmOperation_t;
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *sgemmGetStatusString(sgemmStatus_t status);
 
@@ -128,6 +135,48 @@ sgemmStatus_t sgemmEx(sgemmHandle_t handle, int64_t M, int64_t N, int64_t K,
 sgemmStatus_t sgemm(int64_t M, int64_t N, int64_t K, float alpha,
                     const float *A, int64_t lda, const float *B, int64_t ldb,
                     float beta, float *C, int64_t ldc, cudaStream_t stream);
+
+/*
+ * Strided-batched product with optional transposed operands:
+ *
+ *   C_z = alpha * op(A_z) . op(B_z) + beta * C_z,   z = 0 .. batchCount-1
+ *
+ * all matrices ROW MAJOR.  op(A) is M x K: opA == SGEMM_OP_N reads A stored
+ * M x K (lda >= K), SGEMM_OP_T reads A stored K x M (lda >= M) as its
+ * transpose.  op(B) is K x N: opB == SGEMM_OP_N reads B stored K x N
+ * (ldb >= N), SGEMM_OP_T reads B stored N x K (ldb >= K).  C_z is M x N
+ * (ldc >= N).  Matrix z of an operand starts at base + z * stride (elements;
+ * strides >= 0, a zero stride reuses one matrix for every z).  The C
+ * matrices of different z must not overlap.  batchCount == 0 is a no-op.
+ * With (N, N, batchCount 1) this is sgemmEx().
+ *
+ * FFMA path: operands given transposed, or whose base, row pitch or batch
+ * stride TMA cannot address (16-byte multiples), are first copied into the
+ * workspace in M x K / K x N row-major form; all output tiles of all batch
+ * entries share one persistent grid (and one stream-K split).  3xTF32 path
+ * (sgemmSetMathMode 1): the split pre-pass reads either form directly.
+ * Workspace needs: sgemmStridedBatchedWorkspaceSize().  Errors as for
+ * sgemmEx(); INVALID_VALUE also for an unknown op, a negative batchCount or
+ * stride; NOT_SUPPORTED when batchCount * output tiles reaches 2^31.
+ * These forms are not on the pages (which fix row-major NN); the transposed
+ * forms follow the BLAS convention that "Matmul I" cites for cuBLAS.
+ */
+sgemmStatus_t sgemmStridedBatched(sgemmHandle_t handle, sgemmOperation_t opA,
+                                  sgemmOperation_t opB, int64_t M, int64_t N,
+                                  int64_t K, float alpha, const float *A,
+                                  int64_t lda, int64_t strideA, const float *B,
+                                  int64_t ldb, int64_t strideB, float beta,
+                                  float *C, int64_t ldc, int64_t strideC,
+                                  int64_t batchCount, cudaStream_t stream);
+
+/* Workspace sgemmStridedBatched() can use for these operands (same meaning
+ * as sgemmGetWorkspaceSize(): repacking is required, stream-K scratch
+ * optional, the 3xTF32 split parts required in math mode 1). */
+sgemmStatus_t sgemmStridedBatchedWorkspaceSize(
+    sgemmHandle_t handle, sgemmOperation_t opA, sgemmOperation_t opB, int64_t M,
+    int64_t N, int64_t K, const float *A, int64_t lda, int64_t strideA,
+    const float *B, int64_t ldb, int64_t strideB, int64_t batchCount,
+    size_t *bytes);
 
 /*
  * Bytes of device workspace sgemmHostEx() needs: device copies of A, B and C

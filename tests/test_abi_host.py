@@ -111,3 +111,29 @@ def test_null_handle_rejected(lib):
     code = ctypes.c_int()
     assert lib.sgemmGetDeviceError(None, ctypes.byref(code)) == _binding.Status.INVALID_VALUE
     assert lib.sgemmDestroy(None) == 0
+
+
+def _batched(lib, opA=0, opB=0, M=4, N=4, K=4, lda=None, ldb=None, ldc=None, sa=0, sb=0, sc=0,
+             batch=2, A=F, B=F, C=F):
+    # The handle is a fake pointer: only use with arguments that fail
+    # validation or describe an empty product (both return before using it).
+    lda = (K if opA == 0 else M) if lda is None else lda
+    ldb = (N if opB == 0 else K) if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return lib.sgemmStridedBatched(F, opA, opB, M, N, K, 1.0, A, lda, sa, B, ldb, sb, 0.0, C, ldc,
+                                   sc, batch, None)
+
+
+@pytest.mark.parametrize("args", [
+    dict(opA=2), dict(opB=-1), dict(batch=-1), dict(sa=-4), dict(sc=-1),
+    dict(opA=1, M=8, K=4, lda=7),      # A stored K x M needs lda >= M
+    dict(opB=1, N=8, K=6, ldb=5),      # B stored N x K needs ldb >= K
+    dict(opA=0, M=8, K=6, lda=5),
+])
+def test_batched_invalid_arguments(lib, args):
+    assert _batched(lib, **args) == _binding.Status.INVALID_VALUE
+
+
+def test_batched_empty_is_a_no_op(lib):
+    assert _batched(lib, batch=0, A=None, B=None, C=None) == 0
+    assert _batched(lib, M=0, A=None, B=None, C=None) == 0
