@@ -72,6 +72,14 @@ struct Tf32x3Info {
     int threads, smem, bm, bn, bk, stages;
 };
 Tf32x3Info tf32x3_info();
+// Skinny products, M <= 16 or N <= 16 (sgemm_skinny.cu).
+constexpr int kSkinnyMax = 16;
+int skinny_splits(bool small_m, int M, int N, int K, int sms);
+size_t skinny_workspace(int M, int N, int splits);
+void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *A, int64_t lda,
+                   const float *B, int64_t ldb, float beta, float *C, int64_t ldc, float *part,
+                   int splits, cudaStream_t s);
+
 // Auxiliary kernels (sgemm_aux.cu); all take a batch (matrix z at base + z * stride).
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t stride_c, int batch,
                     cudaStream_t s);

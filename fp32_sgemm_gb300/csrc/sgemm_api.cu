@@ -177,6 +177,10 @@ struct Plan {
     int64_t kp = 0;                 // 3xTF32: row pitch of the split operands
     size_t ws_split_a = 0, ws_split_b = 0;   // 3xTF32: bytes of one part (hi or lo)
     size_t ws_split = 0;            // 3xTF32: A_hi, A_lo, B_hi^T, B_lo^T
+    // Skinny path (kind 4): which side is small, K splits, partial sums.
+    bool skinny_m = false;
+    int skinny_split = 0;
+    size_t ws_skinny = 0;
 };
 
 // Configuration 10 (BK = 32, 3 stages, TMA issued by a compute thread, two
@@ -267,6 +271,23 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
         return SGEMM_STATUS_SUCCESS;
     }
     std::call_once(g_kernels_once, init_kernel_table);
+    // Few rows or few columns: streaming kernels bound by HBM (either math
+    // mode; their FMAs are FP32), when the workspace holds their partial sums.
+    if (q.opA == 0 && q.opB == 0 && q.batch == 1 && (q.M <= sg::kSkinnyMax || q.N <= sg::kSkinnyMax)) {
+        const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
+        const int splits = sg::skinny_splits(small_m, int(q.M), int(q.N), int(q.K), h->sm_count);
+        const size_t need = align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
+        if (h->ws != nullptr && h->ws_bytes >= need) {
+            pl.pub.kind = 4;
+            pl.pub.launches = 2;
+            pl.pub.vector_epilogue = 0;
+            pl.skinny_m = small_m;
+            pl.skinny_split = splits;
+            pl.ws_skinny = need;
+            pl.pub.ctas = int(ceil_div(small_m ? q.N : q.M, 1024) * splits);
+            return SGEMM_STATUS_SUCCESS;
+        }
+    }
     if (h->math == 1) return make_plan_tf32x3(h, q, pl);
     pl.pub.kind = 1;
     // A as TMA reads it: [batch][M][K] rows of K.
@@ -439,6 +460,16 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
         return last_launch();
     }
     if (pl.pub.kind == 3) return run_tf32x3(h, pl, q, stream);
+    if (pl.pub.kind == 4) {
+        if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        sg::launch_skinny(pl.skinny_m, int(q.M), int(q.N), int(q.K), q.alpha, q.A, q.lda, q.B, q.ldb,
+                          q.beta, q.C, q.ldc, static_cast<float *>(h->ws), pl.skinny_split, stream);
+        if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
+        if (h->ev_stop != nullptr && cudaEventRecord(h->ev_stop, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        return SGEMM_STATUS_SUCCESS;
+    }
 
     const float *Ause = q.A, *Buse = q.B;
     // Stream-K scratch is optional: without room for it, whole tiles are used.
@@ -512,6 +543,16 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
 
 size_t workspace_bytes(const Plan &pl) {
     return pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials + pl.ws_split;
+}
+
+// Skinny products use the workspace only when it is big enough; the size
+// query reports what they would use so that callers can provide it.
+size_t skinny_query_bytes(const sgemmContext *h, const Problem &q) {
+    if (q.opA != 0 || q.opB != 0 || q.batch != 1 || q.empty() || q.K == 0 || q.alpha == 0.0f) return 0;
+    if (q.M > sg::kSkinnyMax && q.N > sg::kSkinnyMax) return 0;
+    const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
+    const int splits = sg::skinny_splits(small_m, int(q.M), int(q.N), int(q.K), h->sm_count);
+    return align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
 }
 
 }  // namespace
@@ -602,7 +643,8 @@ sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t h, int64_t M, int64_t N, int64
     Plan pl;
     st = make_plan(h, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, std::max<int64_t>(1, N), pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials + pl.ws_split;
+    *bytes = std::max(workspace_bytes(pl),
+                      skinny_query_bytes(h, nn_problem(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, N)));
     return SGEMM_STATUS_SUCCESS;
 }
 
@@ -682,7 +724,7 @@ sgemmStatus_t sgemmStridedBatchedWorkspaceSize(sgemmHandle_t h, sgemmOperation_t
     qc.C = nullptr;
     st = make_plan(h, qc, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = workspace_bytes(pl);
+    *bytes = std::max(workspace_bytes(pl), skinny_query_bytes(h, qc));
     return SGEMM_STATUS_SUCCESS;
 }
 

@@ -167,6 +167,14 @@ WORKLOADS = {
                            samples=65536),
 }
 
+# Skinny shapes beyond the five workloads: bound by HBM, not by the FMA pipes
+# (few rows or few columns of C; intensity about min(M, N) / 2 FLOP/byte).
+EXTRA_WORKLOADS = {
+    "skinny_m1": Workload("skinny_m1", 1, 16384, 16384, 1.0, 0.0, 11, True),
+    "skinny_m8": Workload("skinny_m8", 8, 16384, 16384, 1.0, 0.0, 12, True),
+    "skinny_n8": Workload("skinny_n8", 16384, 8, 16384, 1.0, 0.0, 13, True),
+}
+
 SAMPLE_SEED_XOR = 0x5A4D
 
 
