@@ -5,12 +5,14 @@
 // would waste up to 127/128 of their FMAs here.
 //
 //   small M: each thread owns 4 consecutive columns of C and walks them down
-//     its K range with 16-byte loads of B (coalesced across the warp); the A
-//     values of the current K piece sit in shared memory and are read as
-//     warp-wide broadcasts, each feeding 4 FMAs.
-//   small N: each thread owns 4 rows of C and walks them along K with two
-//     16-byte loads per row (whole 32-byte sectors); the K x N operand B sits
-//     in shared memory, and each broadcast B value feeds 4 FMAs.
+//     its K range with 16-byte loads of B (coalesced across the warp, eight
+//     in flight per thread); the A values of the current K piece sit in
+//     shared memory and are read as warp-wide broadcasts, each feeding 4
+//     FMAs (packed two-wide).
+//   small N: each thread owns 2 rows of C and walks them along K with four
+//     16-byte loads per row (whole 32-byte sectors, eight loads in flight);
+//     the K x N operand B sits in shared memory, and each broadcast B value
+//     feeds 2 FMAs.
 //   Both split K across CTAs until the chip is full: every split writes its
 //   M x N partial sums to the workspace and a third kernel adds the splits in
 //   order (deterministic) and applies alpha and beta.
@@ -56,8 +58,30 @@ skinny_m_partial_kernel(int M, int N, int K, const float *__restrict__ A, int64_
         __syncthreads();
         if (!active) continue;
         const float *bcol = B + (int64_t)k0 * ldb + n;
-#pragma unroll 4
-        for (int k = 0; k < kn; ++k) {
+        // Eight independent 16-byte loads in flight per thread, then the
+        // FMAs (packed two-wide, a broadcast from shared memory).
+        int k = 0;
+        if (full4) {
+            for (; k + 8 <= kn; k += 8) {
+                float4 b[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    b[q] = __ldcs(reinterpret_cast<const float4 *>(bcol + (int64_t)(k + q) * ldb));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const float a = sA[m][k + q];
+                        const float2 a2 = make_float2(a, a);
+                        float2 lo = make_float2(acc[m][0], acc[m][1]);
+                        float2 hi = make_float2(acc[m][2], acc[m][3]);
+                        lo = __ffma2_rn(a2, make_float2(b[q].x, b[q].y), lo);
+                        hi = __ffma2_rn(a2, make_float2(b[q].z, b[q].w), hi);
+                        acc[m][0] = lo.x; acc[m][1] = lo.y; acc[m][2] = hi.x; acc[m][3] = hi.y;
+                    }
+            }
+        }
+        for (; k < kn; ++k) {
             float4 b;
             const float *bp = bcol + (int64_t)k * ldb;
             if (full4) {
@@ -91,20 +115,23 @@ skinny_m_partial_kernel(int M, int N, int K, const float *__restrict__ A, int64_
 
 // ------------------------------------------------------------ small N
 
+constexpr int kRowsPerThread = 2;
+
 template <int NT>
 __global__ void __launch_bounds__(kSkinnyThreads)
 skinny_n_partial_kernel(int M, int N, int K, const float *__restrict__ A, int64_t lda,
                         const float *__restrict__ B, int64_t ldb, float *__restrict__ part,
                         int k_chunk, bool vec_a) {
     constexpr int NP = (NT + 3) / 4 * 4;          // B row padded to whole float4s
+    constexpr int R = kRowsPerThread;
     __shared__ __align__(16) float sB[kSkinnyKT][NP];
     const int split = blockIdx.y;
     const int kbeg = split * k_chunk;
     const int kend = min(K, kbeg + k_chunk);
-    const int r0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    float acc[4][NP];
+    const int r0 = (blockIdx.x * blockDim.x + threadIdx.x) * R;
+    float acc[R][NP];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < R; ++i)
 #pragma unroll
         for (int j = 0; j < NP; ++j) acc[i][j] = 0.f;
     for (int k0 = kbeg; k0 < kend; k0 += kSkinnyKT) {
@@ -117,47 +144,49 @@ skinny_n_partial_kernel(int M, int N, int K, const float *__restrict__ A, int64_
         __syncthreads();
         if (r0 >= M) continue;
         // 16-byte row reads need the K piece to start 16-byte aligned too.
-        const bool vec = vec_a && ((k0 & 3) == 0) && (kn & 7) == 0;
+        const bool vec = vec_a && ((k0 & 3) == 0) && (kn & 15) == 0;
         if (vec) {
-            for (int k = 0; k < kn; k += 8) {
-                float a[4][8];
+            for (int k = 0; k < kn; k += 16) {
+                float4 a[R][4];                   // 16 consecutive k of each row
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < R; ++i) {
                     if (r0 + i < M) {
                         const float4 *ap = reinterpret_cast<const float4 *>(A + (int64_t)(r0 + i) * lda + k0 + k);
-                        const float4 lo = __ldcs(ap), hi = __ldcs(ap + 1);
-                        a[i][0] = lo.x; a[i][1] = lo.y; a[i][2] = lo.z; a[i][3] = lo.w;
-                        a[i][4] = hi.x; a[i][5] = hi.y; a[i][6] = hi.z; a[i][7] = hi.w;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) a[i][v] = __ldcs(ap + v);
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) a[i][q] = 0.f;
+                        for (int v = 0; v < 4; ++v) a[i][v] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < 16; ++q) {
 #pragma unroll
                     for (int g = 0; g < NP / 4; ++g) {
                         const float4 b = *reinterpret_cast<const float4 *>(&sB[k + q][4 * g]);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            acc[i][4 * g] = fmaf(a[i][q], b.x, acc[i][4 * g]);
-                            acc[i][4 * g + 1] = fmaf(a[i][q], b.y, acc[i][4 * g + 1]);
-                            acc[i][4 * g + 2] = fmaf(a[i][q], b.z, acc[i][4 * g + 2]);
-                            acc[i][4 * g + 3] = fmaf(a[i][q], b.w, acc[i][4 * g + 3]);
+                        for (int i = 0; i < R; ++i) {
+                            const float4 &av = a[i][q >> 2];
+                            const float x = (q & 3) == 0 ? av.x : (q & 3) == 1 ? av.y : (q & 3) == 2 ? av.z : av.w;
+                            acc[i][4 * g] = fmaf(x, b.x, acc[i][4 * g]);
+                            acc[i][4 * g + 1] = fmaf(x, b.y, acc[i][4 * g + 1]);
+                            acc[i][4 * g + 2] = fmaf(x, b.z, acc[i][4 * g + 2]);
+                            acc[i][4 * g + 3] = fmaf(x, b.w, acc[i][4 * g + 3]);
                         }
                     }
+                }
             }
         } else {
             for (int k = 0; k < kn; ++k) {
-                float a[4];
+                float a[R];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < R; ++i)
                     a[i] = (r0 + i < M) ? A[(int64_t)(r0 + i) * lda + k0 + k] : 0.f;
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
                     const float b = sB[k][j];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(a[i], b, acc[i][j]);
+                    for (int i = 0; i < R; ++i) acc[i][j] = fmaf(a[i], b, acc[i][j]);
                 }
             }
         }
@@ -165,7 +194,7 @@ skinny_n_partial_kernel(int M, int N, int K, const float *__restrict__ A, int64_
     if (r0 >= M) return;
     float *out = part + (int64_t)split * M * N;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
         if (r0 + i >= M) break;
 #pragma unroll
         for (int j = 0; j < NP; ++j)
@@ -195,7 +224,7 @@ inline int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
 
 // Splits of K: about 8 CTAs per SM in total, each at least 128 deep in K.
 int skinny_splits(bool small_m, int M, int N, int K, int sms) {
-    const int64_t blocks = small_m ? cdiv(N, 4 * kSkinnyThreads) : cdiv(M, 4 * kSkinnyThreads);
+    const int64_t blocks = small_m ? cdiv(N, 4 * kSkinnyThreads) : cdiv(M, kRowsPerThread * kSkinnyThreads);
     int64_t splits = cdiv(int64_t(sms) * 8, blocks);
     splits = std::min<int64_t>(splits, cdiv(K, kSkinnyKT));
     return int(std::max<int64_t>(1, std::min<int64_t>(splits, 65535)));
@@ -217,16 +246,16 @@ template <int T>
 void launch_n(int M, int N, int K, const float *A, int64_t lda, const float *B, int64_t ldb,
               float *part, int splits, int k_chunk, cudaStream_t s) {
     const bool vec_a = (reinterpret_cast<uintptr_t>(A) % 16 == 0) && lda % 4 == 0;
-    dim3 grid(unsigned(cdiv(M, 4 * kSkinnyThreads)), unsigned(splits));
+    dim3 grid(unsigned(cdiv(M, kRowsPerThread * kSkinnyThreads)), unsigned(splits));
     skinny_n_partial_kernel<T><<<grid, kSkinnyThreads, 0, s>>>(M, N, K, A, lda, B, ldb, part, k_chunk, vec_a);
 }
 
 void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *A, int64_t lda,
                    const float *B, int64_t ldb, float beta, float *C, int64_t ldc, float *part,
                    int splits, cudaStream_t s) {
-    // k_chunk a multiple of 8 so that every split after the first starts
-    // 32-byte aligned along K.
-    const int k_chunk = int(cdiv(cdiv(K, splits), 8) * 8);
+    // k_chunk a multiple of 16 so that every split starts 64-byte aligned
+    // along K (the small-N kernel reads 16 k per row at a time).
+    const int k_chunk = int(cdiv(cdiv(K, splits), 16) * 16);
     const int small = small_m ? M : N;
     if (small_m) {
         if (small <= 1) launch_m<1>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
