@@ -71,7 +71,8 @@ struct Tf32x3Info {
     const void *fn[4];   // variant index as for the FFMA kernels
     int threads, smem, bm, bn, bk, stages;
 };
-Tf32x3Info tf32x3_info();
+constexpr int kNumTf32x3Configs = 3;
+Tf32x3Info tf32x3_info(int config);   // 1-based tile configuration
 // Skinny products, M <= 16 or N <= 16 (sgemm_skinny.cu).
 constexpr int kSkinnyMax = 16;
 int skinny_splits(bool small_m, int M, int N, int K, int sms);

@@ -177,6 +177,7 @@ struct Plan {
     int64_t kp = 0;                 // 3xTF32: row pitch of the split operands
     size_t ws_split_a = 0, ws_split_b = 0;   // 3xTF32: bytes of one part (hi or lo)
     size_t ws_split = 0;            // 3xTF32: A_hi, A_lo, B_hi^T, B_lo^T
+    int tf32_cfg = 0;               // 3xTF32: tile configuration (1-based)
     // Skinny path (kind 4): which side is small, K splits, partial sums.
     bool skinny_m = false;
     int skinny_split = 0;
@@ -215,8 +216,29 @@ bool c_vector_ok(const Problem &q) {
 
 // 3xTF32 plan: operands are always split into the workspace (TF32 hi and lo
 // parts, K contiguous), so any layout, pitch and alignment of A and B works.
+// Automatic tensor-core tile choice: the one with the least estimated time,
+// waves (whole tiles per SM, rounded up) times the time of one tile, which
+// grows with its width over the tensor-pipe efficiency measured at 8192^3
+// (128 x 128: 0.86, shared-memory bound; 128 x 256: 0.91).  128 x 192 was
+// slower than both everywhere and is only used when asked for.
+int choose_tf32x3_config(const sgemmContext *h, const Problem &q) {
+    if (h->algo >= 1 && h->algo <= sg::kNumTf32x3Configs) return h->algo;
+    const double width[2] = {128.0, 256.0};
+    const double eff[2] = {0.86, 0.91};
+    const int cfg[2] = {1, 3};
+    int best = 1;
+    double best_t = 0.0;
+    for (int i = 0; i < 2; ++i) {
+        const int64_t tiles = ceil_div(q.M, 128) * ceil_div(q.N, int64_t(width[i])) * q.batch;
+        const double t = double(ceil_div(tiles, h->sm_count)) * width[i] / eff[i];
+        if (i == 0 || t < best_t) { best_t = t; best = cfg[i]; }
+    }
+    return best;
+}
+
 sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl) {
-    const sg::Tf32x3Info info = sg::tf32x3_info();
+    pl.tf32_cfg = choose_tf32x3_config(h, q);
+    const sg::Tf32x3Info info = sg::tf32x3_info(pl.tf32_cfg);
     pl.pub.kind = 3;
     pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
     pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
@@ -232,11 +254,11 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
     pl.num_tiles = int(tiles);
     pl.k_blocks = int(ceil_div(q.K, info.bk));
     static std::mutex occ_mutex;
-    static int occ_cache[kMaxDevices][4] = {};
+    static int occ_cache[kMaxDevices][sg::kNumTf32x3Configs][4] = {};
     int occ = 0;
     {
         std::lock_guard<std::mutex> lk(occ_mutex);
-        int &o = occ_cache[h->device][pl.variant];
+        int &o = occ_cache[h->device][pl.tf32_cfg - 1][pl.variant];
         if (o == 0) {
             const void *fn = info.fn[pl.variant];
             int n = 0;
@@ -398,7 +420,7 @@ sgemmStatus_t launch_main(sgemmContext *h, const void *fn, int ctas, int threads
 
 sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cudaStream_t stream) {
     if (h->ws == nullptr || h->ws_bytes < pl.ws_split) return SGEMM_STATUS_WORKSPACE_REQUIRED;
-    const sg::Tf32x3Info info = sg::tf32x3_info();
+    const sg::Tf32x3Info info = sg::tf32x3_info(pl.tf32_cfg);
     char *ws = static_cast<char *>(h->ws);
     float *a_hi = reinterpret_cast<float *>(ws);
     float *a_lo = reinterpret_cast<float *>(ws + pl.ws_split_a);

@@ -39,18 +39,23 @@
 
 namespace sg {
 
-template <int BN_, int STAGES_, int CHUNK_KB_>
+template <int BN_, int STAGES_, int CHUNK_KB_, int EPI_WARPS_>
 struct Tf32x3Config {
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
     static constexpr int CHUNK_KB = CHUNK_KB_;     // K slices per TMEM accumulator chunk
+    // Epilogue warps: 4 lane quarters of TMEM x EPI_WARPS/4 column slabs.
+    static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int SLAB = BN / (EPI_WARPS / 4);   // columns per epilogue thread
     static constexpr int A_BYTES = BM * BK * 4;     // one of A_hi / A_lo
     static constexpr int B_BYTES = BN * BK * 4;     // one of B_hi / B_lo
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;        // two accumulators
-    static constexpr int THREADS = 192;
+    // Two accumulators of BN columns; the allocation is a power of two.
+    static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+    static constexpr int THREADS = (2 + EPI_WARPS) * 32;
     static constexpr int NUM_BARRIERS = 2 * STAGES + 5;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16 + 1024;
-    static_assert(BN == 64 || BN == 128 || BN == 256, "UMMA N for M = 128");
+    static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+    static_assert(EPI_WARPS % 4 == 0 && SLAB % 32 == 0 && SLAB * (EPI_WARPS / 4) == BN, "epilogue slabs");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM");
     static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
 };
@@ -86,7 +91,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -191,13 +196,15 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM chunks -> FP32 sums -> C ----------------
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+        constexpr int SLAB = Cfg::SLAB;
+        const int slab0 = ((warp - 2) >> 2) * SLAB;   // first column of this warp's slab
         const float alpha = p.alpha, beta = p.beta;
         int gc = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            float sum[BN];
+            float sum[SLAB];
 #pragma unroll
-            for (int c = 0; c < BN; ++c) sum[c] = 0.f;
+            for (int c = 0; c < SLAB; ++c) sum[c] = 0.f;
             for (int kb0 = 0; kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB, ++gc) {
                 const int ab = gc & 1;
                 const uint32_t use = (uint32_t)(gc >> 1);
@@ -207,13 +214,14 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * BN);
+                const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(ab * BN + slab0);
 #pragma unroll
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    float v[32];
-                    tmem_ld_32cols(taddr + (uint32_t)c0, v);
+                for (int c0 = 0; c0 < SLAB; c0 += 16) {
+                    float v[16];
+                    tmem_ld_16cols(taddr + (uint32_t)c0, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sum[c0 + i] += v[i];
+                    for (int i = 0; i < 16; ++i) sum[c0 + i] += v[i];
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -226,8 +234,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             if (row < p.M) {
                 float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
 #pragma unroll
-                for (int q = 0; q < BN / 4; ++q) {
-                    const int col = tn * BN + 4 * q;
+                for (int q = 0; q < SLAB / 4; ++q) {
+                    const int col = tn * BN + slab0 + 4 * q;
                     if (C_VEC && col + 3 < p.N) {
                         float4 *dst = reinterpret_cast<float4 *>(crow + col);
                         float4 o;
@@ -270,30 +278,33 @@ namespace {
 inline int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
 
 template <class Cfg>
-struct Tf32x3Entries {
-    const void *fn[4];
-    Tf32x3Entries() {
-        fn[0] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, true>);
-        fn[1] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, false>);
-        fn[2] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, true>);
-        fn[3] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, false>);
-    }
-};
-
-using Tf32x3Cfg = Tf32x3Config<128, 3, 2>;
+Tf32x3Info make_info() {
+    Tf32x3Info info;
+    info.fn[0] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, true>);
+    info.fn[1] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, true, false>);
+    info.fn[2] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, true>);
+    info.fn[3] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, false>);
+    info.threads = Cfg::THREADS;
+    info.smem = Cfg::SMEM_BYTES;
+    info.bm = Cfg::BM;
+    info.bn = Cfg::BN;
+    info.bk = Cfg::BK;
+    info.stages = Cfg::STAGES;
+    return info;
+}
 }  // namespace
 
-Tf32x3Info tf32x3_info() {
-    static const Tf32x3Entries<Tf32x3Cfg> entries;
-    Tf32x3Info info;
-    for (int i = 0; i < 4; ++i) info.fn[i] = entries.fn[i];
-    info.threads = Tf32x3Cfg::THREADS;
-    info.smem = Tf32x3Cfg::SMEM_BYTES;
-    info.bm = Tf32x3Cfg::BM;
-    info.bn = Tf32x3Cfg::BN;
-    info.bk = Tf32x3Cfg::BK;
-    info.stages = Tf32x3Cfg::STAGES;
-    return info;
+// Tensor-core tile configurations: 1: 128 x 128 (3 stages, 4 epilogue
+// warps), 2: 128 x 192 (2 stages, 8), 3: 128 x 256 (2 stages, 8).  Wider
+// tiles read fewer shared-memory bytes per MMA FLOP.
+Tf32x3Info tf32x3_info(int config) {
+    static const Tf32x3Info infos[kNumTf32x3Configs] = {
+        make_info<Tf32x3Config<128, 3, 2, 4>>(),
+        make_info<Tf32x3Config<192, 2, 2, 8>>(),
+        make_info<Tf32x3Config<256, 2, 2, 8>>(),
+    };
+    if (config < 1 || config > kNumTf32x3Configs) config = 1;
+    return infos[config - 1];
 }
 
 }  // namespace sg

@@ -230,8 +230,10 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * 0 = automatic choice by shape (default); 1..10 = a fixed configuration of
  * the 128 x 128 output tile (K slice 16 or 32, 3 or 4 pipeline stages, a
  * dedicated TMA warp or TMA issued by a compute thread, one or two CTAs per
- * SM; see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  Every configuration
- * computes the same result up to summation order.
+ * SM; see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1 (3xTF32)
+ * the values 1..3 pick the tensor-core tile instead: 128 x 128, 128 x 192
+ * or 128 x 256.  Every configuration computes the same result up to
+ * summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
 

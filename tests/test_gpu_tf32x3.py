@@ -133,3 +133,18 @@ def test_repeated_calls_bitwise_identical(handle):
     for _ in range(10):
         handle.gemm(A, B, C)
         assert torch.equal(C.view(torch.int32), first.view(torch.int32))
+
+
+@pytest.mark.parametrize("config", [1, 2, 3])
+@pytest.mark.parametrize("shape", [(1000, 1500, 700), (256, 4097, 333), (4096, 4096, 4096)])
+def test_every_tensor_tile_configuration(handle, config, shape):
+    M, N, K = shape
+    handle.set_algo(config)
+    try:
+        p = inputs.make_problem(M, N, K, seed=M + N + K + config, alpha=0.5, beta=0.25)
+        _close(_run(handle, p)[:, :N], _ref(p))
+        q = inputs.make_problem(M, N, K, seed=M + N + K + config + 1000, kind="integer", alpha=0.5,
+                                beta=0.25)
+        np.testing.assert_array_equal(_run(handle, q)[:, :N].astype(np.float64), _ref(q))
+    finally:
+        handle.set_algo(0)
