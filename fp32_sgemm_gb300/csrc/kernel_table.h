@@ -42,7 +42,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 10;
+constexpr int kNumAlgos = 11;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -53,6 +53,7 @@ void fill_algo7(KernelEntry *v);
 void fill_algo8(KernelEntry *v);
 void fill_algo9(KernelEntry *v);
 void fill_algo10(KernelEntry *v);
+void fill_algo11(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {

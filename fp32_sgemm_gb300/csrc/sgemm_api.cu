@@ -45,6 +45,7 @@ void init_kernel_table() {
     sg::fill_algo8(g_kernels[7]);
     sg::fill_algo9(g_kernels[8]);
     sg::fill_algo10(g_kernels[9]);
+    sg::fill_algo11(g_kernels[10]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

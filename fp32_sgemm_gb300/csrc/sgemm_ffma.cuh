@@ -85,7 +85,7 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 //   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2).
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_,
           int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4, int PRODUCER_WARP_ = 1,
-          int PIPE_ = 0>
+          int PIPE_ = 0, int SCALAR_FMA_ = 0>
 struct FfmaConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -97,6 +97,7 @@ struct FfmaConfig {
     static constexpr int KA = KA_;
     static constexpr bool PRODUCER_WARP = PRODUCER_WARP_ != 0;
     static constexpr bool PIPE = PIPE_ != 0;
+    static constexpr bool SCALAR_FMA = SCALAR_FMA_ != 0;   // fmaf instead of packed fma.rn.f32x2
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     static constexpr int THREADS = (CONSUMER_WARPS + (PRODUCER_WARP ? 1 : 0)) * 32;
     static constexpr int ROW_BYTES_A = BK * 4;                 // one row of the A slice
@@ -387,8 +388,15 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const float2 a2 = make_float2(av, av);
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
-                acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
-                acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
+                if constexpr (Cfg::SCALAR_FMA) {
+                    acc[i][2 * j].x = fmaf(av, b[j].x, acc[i][2 * j].x);
+                    acc[i][2 * j].y = fmaf(av, b[j].y, acc[i][2 * j].y);
+                    acc[i][2 * j + 1].x = fmaf(av, b[j].z, acc[i][2 * j + 1].x);
+                    acc[i][2 * j + 1].y = fmaf(av, b[j].w, acc[i][2 * j + 1].y);
+                } else {
+                    acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
+                    acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
+                }
             }
         }
     };

@@ -227,7 +227,7 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
 
 /*
  * Pin the main kernel's tile configuration for calls on this handle:
- * 0 = automatic choice by shape (default); 1..10 = a fixed configuration of
+ * 0 = automatic choice by shape (default); 1..11 = a fixed configuration of
  * the 128 x 128 output tile (K slice 16 or 32, 3 or 4 pipeline stages, a
  * dedicated TMA warp or TMA issued by a compute thread, one or two CTAs per
  * SM; see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1 (3xTF32)

@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 11)))
+@pytest.mark.parametrize("algo", list(range(1, 12)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
