@@ -360,6 +360,10 @@ def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, *, workspace, han
     M, K = A.shape
     N = B.shape[1]
     h = handle or default_handle(workspace.device)
+    # The device copies are 256-byte aligned with pitches padded to 4 floats;
+    # the handle's own workspace must cover the product on them.
+    pad4 = lambda n: (max(n, 1) + 3) // 4 * 4
+    h._ensure_workspace(h.workspace_size(M, N, K, 256, pad4(K), 256, pad4(N)))
     lib = load_library()
     _check(lib.sgemmHostEx(h.ptr, M, N, K, float(alpha), A.data_ptr(), max(A.stride(0), K, 1),
                            B.data_ptr(), max(B.stride(0), N, 1), float(beta), C.data_ptr(),

@@ -76,6 +76,12 @@ struct sgemmContext {
     int schedule = 0;   // 0 automatic, 1 whole tiles only, 2 stream-K whenever it applies
     int math = 0;       // 0 FP32 FFMA, 1 error-compensated 3xTF32 on the tensor cores
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;   // around the main kernel, if set
+    // sgemmHostEx pipeline: copy-in and copy-out streams and their events,
+    // created with the handle.
+    static constexpr int kHostChunks = 4;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_begin = nullptr, ev_end = nullptr;
+    cudaEvent_t ev_in[kHostChunks] = {}, ev_done[kHostChunks] = {};
 };
 
 namespace {
@@ -578,6 +584,19 @@ size_t skinny_query_bytes(const sgemmContext *h, const Problem &q) {
     return align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
 }
 
+void release_handle_resources(sgemmContext *h) {
+    if (h->d_err) cudaFree(h->d_err);
+    if (h->s_in) cudaStreamDestroy(h->s_in);
+    if (h->s_out) cudaStreamDestroy(h->s_out);
+    if (h->ev_begin) cudaEventDestroy(h->ev_begin);
+    if (h->ev_end) cudaEventDestroy(h->ev_end);
+    for (int i = 0; i < sgemmContext::kHostChunks; ++i) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
+    }
+    h->d_err = nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -619,9 +638,17 @@ sgemmStatus_t sgemmCreate(sgemmHandle_t *handle) {
     if (h == nullptr) return SGEMM_STATUS_INTERNAL_ERROR;
     h->device = dev;
     h->sm_count = sms;
-    if (cudaMalloc(&h->d_err, sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
-        cudaFree(h->d_err);
+    bool ok = cudaMalloc(&h->d_err, sizeof(uint32_t)) == cudaSuccess &&
+              cudaMemset(h->d_err, 0, sizeof(uint32_t)) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_begin, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < sgemmContext::kHostChunks; ++i)
+        ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        release_handle_resources(h);
         delete h;
         return SGEMM_STATUS_LAUNCH_FAILED;
     }
@@ -635,7 +662,7 @@ sgemmStatus_t sgemmDestroy(sgemmHandle_t h) {
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
     cudaDeviceSynchronize();
-    cudaFree(h->d_err);
+    release_handle_resources(h);
     if (prev >= 0) cudaSetDevice(prev);
     delete h;
     return SGEMM_STATUS_SUCCESS;
@@ -778,18 +805,36 @@ sgemmStatus_t sgemmHostEx(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, floa
     float *dC = reinterpret_cast<float *>(base + align256(size_t(M) * lda_p * 4) +
                                           align256(size_t(K) * ldb_p * 4));
     const bool use_ab = K > 0 && alpha != 0.0f;
-    if (use_ab) {
-        if (cudaMemcpy2DAsync(dA, lda_p * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-            cudaMemcpy2DAsync(dB, ldb_p * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    // Rows of A and C go up, get multiplied and come back in chunks: while
+    // chunk i is multiplied on `stream`, chunk i+1 is copied in on the
+    // handle's copy-in stream and chunk i-1 copied out on its copy-out
+    // stream.  B is copied in first (every chunk needs all of it).
+    const int chunks = int(std::max<int64_t>(1, std::min<int64_t>(sgemmContext::kHostChunks, M / 1024)));
+    auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+    if (fail(cudaEventRecord(h->ev_begin, stream)) || fail(cudaStreamWaitEvent(h->s_in, h->ev_begin, 0)) ||
+        fail(cudaStreamWaitEvent(h->s_out, h->ev_begin, 0)))
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    if (use_ab && fail(cudaMemcpy2DAsync(dB, ldb_p * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, h->s_in)))
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    for (int c = 0; c < chunks; ++c) {
+        const int64_t r0 = M * c / chunks, r1 = M * (c + 1) / chunks, rows = r1 - r0;
+        if (use_ab && fail(cudaMemcpy2DAsync(dA + r0 * lda_p, lda_p * 4, A + r0 * lda, lda * 4, K * 4, rows,
+                                             cudaMemcpyHostToDevice, h->s_in)))
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        if (beta != 0.0f && fail(cudaMemcpy2DAsync(dC + r0 * ldc_p, ldc_p * 4, C + r0 * ldc, ldc * 4, N * 4,
+                                                   rows, cudaMemcpyHostToDevice, h->s_in)))
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        if (fail(cudaEventRecord(h->ev_in[c], h->s_in)) || fail(cudaStreamWaitEvent(stream, h->ev_in[c], 0)))
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        st = run(h, rows, N, K, alpha, dA + r0 * lda_p, lda_p, dB, ldb_p, beta, dC + r0 * ldc_p, ldc_p, stream);
+        if (st != SGEMM_STATUS_SUCCESS) return st;
+        if (fail(cudaEventRecord(h->ev_done[c], stream)) || fail(cudaStreamWaitEvent(h->s_out, h->ev_done[c], 0)) ||
+            fail(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * ldc_p, ldc_p * 4, N * 4, rows,
+                                   cudaMemcpyDeviceToHost, h->s_out)))
             return SGEMM_STATUS_LAUNCH_FAILED;
     }
-    if (beta != 0.0f) {
-        if (cudaMemcpy2DAsync(dC, ldc_p * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            return SGEMM_STATUS_LAUNCH_FAILED;
-    }
-    st = run(h, M, N, K, alpha, dA, lda_p, dB, ldb_p, beta, dC, ldc_p, stream);
-    if (st != SGEMM_STATUS_SUCCESS) return st;
-    if (cudaMemcpy2DAsync(C, ldc * 4, dC, ldc_p * 4, N * 4, M, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    // Join: work enqueued on `stream` after this call sees the result.
+    if (fail(cudaEventRecord(h->ev_end, h->s_out)) || fail(cudaStreamWaitEvent(stream, h->ev_end, 0)))
         return SGEMM_STATUS_LAUNCH_FAILED;
     return SGEMM_STATUS_SUCCESS;
 }

@@ -75,9 +75,10 @@ sgemmStatus_t sgemmGetVersion(int *version);
 
 /*
  * Create a handle bound to the CURRENT device.  Checks that the device is
- * compute capability 10.3 (ARCH_MISMATCH otherwise), reads its SM count and
- * allocates the handle's 4-byte device error word: the only device
- * allocation the library makes, done here and never on the compute path.
+ * compute capability 10.3 (ARCH_MISMATCH otherwise), reads its SM count,
+ * creates the two copy streams and the events of sgemmHostEx, and allocates
+ * the handle's 4-byte device error word: the only device allocation the
+ * library makes, done here and never on the compute path.
  */
 sgemmStatus_t sgemmCreate(sgemmHandle_t *handle);
 
@@ -190,10 +191,18 @@ sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K,
  * copy bandwidth; pageable memory works but is staged by the driver).  The
  * operands are copied into `dev_workspace` (device memory of at least
  * sgemmHostWorkspaceSize() bytes, owned by the caller), the product runs
- * there, and the M x N result is copied back into C.  All of it is enqueued
- * on `stream`; the call returns before the copies finish, so the host
- * buffers must stay untouched until the stream has been synchronised.
- * C is read (copied up) only when beta != 0.
+ * there, and the M x N result is copied back into C.  The copies overlap the
+ * arithmetic: B goes up first, then A and C move in up to four row chunks,
+ * chunk i+1 copied in and chunk i-1 copied out (on two streams the handle
+ * owns) while chunk i is multiplied on `stream`.  The call returns before
+ * the work finishes; everything it enqueued is ordered before later work on
+ * `stream`, so synchronising `stream` makes C valid, and the host buffers
+ * must stay untouched until then.  C is read (copied up) only when
+ * beta != 0.  The multiplication itself uses the handle's own workspace as
+ * sgemmEx() does (3xTF32 operand splits, stream-K scratch): its size is
+ * sgemmGetWorkspaceSize() for 256-byte aligned A and B with
+ * lda = K and ldb = N rounded up to multiples of 4; WORKSPACE_REQUIRED when
+ * a required part is missing.
  */
 sgemmStatus_t sgemmHostEx(sgemmHandle_t handle, int64_t M, int64_t N, int64_t K,
                           float alpha, const float *A_host, int64_t lda,

@@ -340,6 +340,48 @@ def test_host_buffer_entry_point(sg, handle):
     _assert_close(C.numpy(), _ref(p))
 
 
+@pytest.mark.parametrize("math", [0, 1], ids=["ffma", "tf32x3"])
+@pytest.mark.parametrize("M,N,K,alpha,beta", [
+    (4099, 515, 257, 0.5, 0.25),     # four row chunks of unequal height
+    (2047, 1029, 130, 1.0, 0.0),     # one chunk; C starts as NaN and is never read
+    (3072, 96, 1000, -2.0, 1.0),     # three chunks
+])
+def test_host_entry_point_chunked_copies(sg, M, N, K, alpha, beta, math):
+    h = sg.Handle()
+    h.set_math_mode(math)
+    try:
+        for kind in ("integer", "uniform"):
+            p = inputs.make_problem(M, N, K, seed=M + N + K, kind=kind, alpha=alpha, beta=beta,
+                                    with_c=True, lda=K + 3, ldb=N + 1, ldc=N + 5)
+            A = torch.from_numpy(p.A).pin_memory()
+            B = torch.from_numpy(p.B).pin_memory()
+            C0 = p.C0.copy()
+            if beta == 0.0:
+                C0[:, :N] = np.nan
+            C = torch.from_numpy(C0).pin_memory()
+            ws = torch.empty(sg.host_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+            stream = torch.cuda.Stream()
+            A2 = A[:, :K]
+            sg.sgemm_host(A2, B[:, :N], C[:, :N], alpha, beta, workspace=ws, handle=h, stream=stream)
+            # Work enqueued on the same stream afterwards is ordered after the
+            # copy of C back to the host.
+            flag = torch.zeros(1, device="cuda")
+            with torch.cuda.stream(stream):
+                flag.fill_(1.0)
+            stream.synchronize()
+            assert flag.item() == 1.0
+            assert h.device_error() == 0
+            got = C.numpy()
+            ref = oracle.sgemm_ref(M, N, K, alpha, p.A, p.B, beta, p.C0)
+            if kind == "integer":
+                np.testing.assert_array_equal(got[:, :N].astype(np.float64), ref)
+            else:
+                _assert_close(got[:, :N], ref)
+            assert np.isnan(got[:, N:]).all(), "padding columns of C written"
+    finally:
+        h.close()
+
+
 def test_bounded_wait_self_test_reports_timeout(sg):
     h = sg.Handle()
     assert h.device_error() == 0
