@@ -192,25 +192,48 @@ def tensor_roofline(flops: float, kernel_ms: float) -> dict:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_rows_sample(w, p, seconds: float, steps: int = 1):
+def oracle_rows_sample(w, p, seconds: float, steps: int = 1, threads: int = 0):
     """Time the oracle on whole output rows of the workload.  Returns
     (flops_per_step, seconds_per_step, rows, threads) for a sample sized so
-    that `steps` samples take about `seconds` in total."""
+    that `steps` samples take about `seconds` in total.  threads 0: all the
+    host cores OpenMP sees."""
     import oracle
-    threads = oracle.max_threads()
+    threads = threads or oracle.max_threads()
     probe_rows = max(1, min(w.M, 32))
     t0 = time.perf_counter()
     oracle.sgemm_ref(probe_rows, w.N, w.K, w.alpha, p.A[:probe_rows], p.B, w.beta,
-                     p.C0[:probe_rows] if p.C0 is not None else None)
+                     p.C0[:probe_rows] if p.C0 is not None else None, threads=threads)
     rate = probe_rows / max(time.perf_counter() - t0, 1e-6)      # rows per second
     rows = int(max(1, min(w.M, rate * seconds / max(steps, 1))))
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
         oracle.sgemm_ref(rows, w.N, w.K, w.alpha, p.A[:rows], p.B, w.beta,
-                         p.C0[:rows] if p.C0 is not None else None)
+                         p.C0[:rows] if p.C0 is not None else None, threads=threads)
         times.append(time.perf_counter() - t0)
     return 2.0 * rows * w.N * w.K, times, rows, threads
+
+
+def oracle_extra_timings(w, p, seconds: float) -> dict:
+    """Oracle timings beside the all-core row sample: single-threaded as well
+    for workloads up to 1024^3, and the sampled-entry check the 8192^3
+    workload uses (its full-matrix time stated as an extrapolation)."""
+    import oracle
+    out = {}
+    if w.M * w.N * w.K <= 1024 ** 3:
+        f, t, rows, _ = oracle_rows_sample(w, p, seconds, 1, threads=1)
+        out["single_thread"] = {"value": f / t[0] / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                "sample": f"{rows} of {w.M} output rows in {t[0]:.2f} s"}
+    if w.samples:
+        rows, cols = inputs.sample_entries(w.M, w.N, w.samples, w.seed)
+        t0 = time.perf_counter()
+        oracle.sgemm_ref_entries(w.K, w.alpha, p.A, p.B, rows, cols, w.beta, p.C0)
+        t = time.perf_counter() - t0
+        out["sampled_entries"] = {
+            "entries": int(w.samples), "seconds": t,
+            "value": 2.0 * w.samples * w.K / t / 1e12, "unit": "TFLOP/s",
+            "full_matrix_seconds_extrapolated": t * w.M * w.N / w.samples}
+    return out
 
 
 def run_reference(args, w, rank: int, world: int):
@@ -418,6 +441,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
                "kind": "oracle",
                "sample": f"{rows} of {w.M} output rows (all {w.N} columns, K={w.K}) "
                          f"in {c_times[0]:.1f} s, fp64 C oracle"}
+        cpu.update(oracle_extra_timings(w, p, min(args.cpu_seconds, 10.0)))
 
     if rank != 0:
         return
