@@ -82,6 +82,36 @@ void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *
                    const float *B, int64_t ldb, float beta, float *C, int64_t ldc, float *part,
                    int splits, cudaStream_t s);
 
+// TMA-fed skinny kernels (sgemm_skinny_tma.cu), for operands TMA reads in
+// place.  A unit is one (output block, k-block) pair; CTA c of `ctas` takes
+// units [c * units / ctas, (c + 1) * units / ctas) and writes one partial
+// tile per output block its range meets (at most `segs`).
+struct SkinnyTmaArgs {
+    int M, N, K;
+    int kb;              // k-blocks per output block
+    int64_t units;       // output blocks x kb
+    int ctas, segs, tile_elems;
+    float *part;         // [ctas][segs][tile_elems]
+    uint32_t *err;
+    uint64_t timeout_ns;
+};
+struct SkinnyTmaGeom {
+    int rows = 0;        // the small dimension rounded up to 1, 2, 4, 8 or 16
+    int kb = 0;
+    int64_t units = 0;
+    int ctas = 0, segs = 0, tile_elems = 0;
+    size_t ws_bytes = 0;
+    int a_box[2] = {0, 0}, b_box[2] = {0, 0};   // TMA boxes {inner, outer}
+    bool a_swizzle64 = false;                    // A box with the 64-byte swizzle
+};
+SkinnyTmaGeom skinny_tma_geometry(bool small_m, int M, int N, int K, int sms);
+// tmA: 2-D map of A (dims {K, M}); tmB: 2-D map of B (dims {N, K}); boxes as
+// the geometry gives.  Launches the streaming kernel and the reduction.
+void launch_skinny_tma(bool small_m, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                       const SkinnyTmaGeom &g, int M, int N, int K, float alpha, float beta,
+                       float *C, int64_t ldc, float *part, uint32_t *err, uint64_t timeout_ns,
+                       cudaStream_t s);
+
 // Auxiliary kernels (sgemm_aux.cu); all take a batch (matrix z at base + z * stride).
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t stride_c, int batch,
                     cudaStream_t s);

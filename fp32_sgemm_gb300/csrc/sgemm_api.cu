@@ -167,6 +167,13 @@ inline bool tma_ok_batched(const void *p, int64_t ld, int64_t stride, int64_t ba
     return tma_ok(p, ld) && (batch == 1 || (stride % 4 == 0 && stride > 0));
 }
 
+// The TMA-fed skinny kernels read A and B in place: both 16-byte aligned
+// with row pitches of whole 16-byte units; below a 256-wide large dimension
+// or K < 16 the plain-load kernels serve.
+inline bool skinny_tma_eligible(const Problem &q, bool small_m) {
+    return tma_ok(q.A, q.lda) && tma_ok(q.B, q.ldb) && q.K >= 16 && (small_m ? q.N : q.M) >= 256;
+}
+
 struct Plan {
     sgemmPlan_t pub{};
     int algo_index = -1;   // row of g_kernels
@@ -189,6 +196,8 @@ struct Plan {
     bool skinny_m = false;
     int skinny_split = 0;
     size_t ws_skinny = 0;
+    bool skinny_tma = false;        // TMA-fed skinny kernels (operands read in place)
+    sg::SkinnyTmaGeom skinny_geom;
 };
 
 // Configuration 10 (BK = 32, 3 stages, TMA issued by a compute thread, two
@@ -304,6 +313,24 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     // mode; their FMAs are FP32), when the workspace holds their partial sums.
     if (q.opA == 0 && q.opB == 0 && q.batch == 1 && (q.M <= sg::kSkinnyMax || q.N <= sg::kSkinnyMax)) {
         const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
+        if (skinny_tma_eligible(q, small_m)) {
+            const sg::SkinnyTmaGeom g = sg::skinny_tma_geometry(small_m, int(q.M), int(q.N), int(q.K),
+                                                               h->sm_count);
+            const size_t need = align256(g.ws_bytes);
+            if (h->ws != nullptr && h->ws_bytes >= need) {
+                pl.pub.kind = 4;
+                pl.pub.launches = 2;
+                pl.pub.vector_epilogue = 0;
+                pl.pub.stages = 6;
+                pl.pub.tile_k = small_m ? 8 : 16;
+                pl.skinny_m = small_m;
+                pl.skinny_tma = true;
+                pl.skinny_geom = g;
+                pl.ws_skinny = need;
+                pl.pub.ctas = g.ctas;
+                return SGEMM_STATUS_SUCCESS;
+            }
+        }
         const int splits = sg::skinny_splits(small_m, int(q.M), int(q.N), int(q.K), h->sm_count);
         const size_t need = align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
         if (h->ws != nullptr && h->ws_bytes >= need) {
@@ -407,6 +434,20 @@ sgemmStatus_t encode_3d(CUtensorMap *map, const float *ptr, int64_t inner, int64
     return r == CUDA_SUCCESS ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
+sgemmStatus_t encode_2d(CUtensorMap *map, const float *ptr, int64_t inner, int64_t outer, int64_t ld,
+                        int box_inner, int box_outer, CUtensorMapSwizzle swz) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return SGEMM_STATUS_LAUNCH_FAILED;
+    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    cuuint64_t strides[1] = {cuuint64_t(ld) * 4};
+    cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
 CUtensorMapSwizzle swizzle_for_bk(int bk) {
     return bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
                     : bk == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -492,8 +533,28 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     if (pl.pub.kind == 4) {
         if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
             return SGEMM_STATUS_LAUNCH_FAILED;
-        sg::launch_skinny(pl.skinny_m, int(q.M), int(q.N), int(q.K), q.alpha, q.A, q.lda, q.B, q.ldb,
-                          q.beta, q.C, q.ldc, static_cast<float *>(h->ws), pl.skinny_split, stream);
+        bool done = false;
+        if (pl.skinny_tma) {
+            const sg::SkinnyTmaGeom &g = pl.skinny_geom;
+            CUtensorMap tmA, tmB;
+            if (encode_2d(&tmA, q.A, q.K, q.M, q.lda, g.a_box[0], g.a_box[1],
+                          g.a_swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE) ==
+                    SGEMM_STATUS_SUCCESS &&
+                encode_2d(&tmB, q.B, q.N, q.K, q.ldb, g.b_box[0], g.b_box[1], CU_TENSOR_MAP_SWIZZLE_NONE) ==
+                    SGEMM_STATUS_SUCCESS) {
+                sg::launch_skinny_tma(pl.skinny_m, tmA, tmB, g, int(q.M), int(q.N), int(q.K), q.alpha, q.beta,
+                                      q.C, q.ldc, static_cast<float *>(h->ws), h->d_err, h->timeout_ns, stream);
+                done = true;
+            }
+        }
+        if (!done) {
+            // Plain-load kernels (also the fallback should a tensor map be refused).
+            const int splits = sg::skinny_splits(pl.skinny_m, int(q.M), int(q.N), int(q.K), h->sm_count);
+            if (h->ws == nullptr || h->ws_bytes < sg::skinny_workspace(int(q.M), int(q.N), splits))
+                return SGEMM_STATUS_WORKSPACE_REQUIRED;
+            sg::launch_skinny(pl.skinny_m, int(q.M), int(q.N), int(q.K), q.alpha, q.A, q.lda, q.B, q.ldb,
+                              q.beta, q.C, q.ldc, static_cast<float *>(h->ws), splits, stream);
+        }
         if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
         if (h->ev_stop != nullptr && cudaEventRecord(h->ev_stop, stream) != cudaSuccess)
             return SGEMM_STATUS_LAUNCH_FAILED;
@@ -581,7 +642,11 @@ size_t skinny_query_bytes(const sgemmContext *h, const Problem &q) {
     if (q.M > sg::kSkinnyMax && q.N > sg::kSkinnyMax) return 0;
     const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
     const int splits = sg::skinny_splits(small_m, int(q.M), int(q.N), int(q.K), h->sm_count);
-    return align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
+    size_t bytes = align256(sg::skinny_workspace(int(q.M), int(q.N), splits));
+    if (skinny_tma_eligible(q, small_m))
+        bytes = std::max(bytes, align256(sg::skinny_tma_geometry(small_m, int(q.M), int(q.N), int(q.K),
+                                                                 h->sm_count).ws_bytes));
+    return bytes;
 }
 
 void release_handle_resources(sgemmContext *h) {

@@ -219,12 +219,14 @@ typedef struct sgemmPlan {
     int launches;       /* kernels one call enqueues (0 for M == 0 or N == 0) */
     int tile_m, tile_n; /* output tile of the main kernel (0 if none) */
     int tile_k;         /* K slice staged per pipeline step */
-    int stages;         /* shared-memory pipeline depth */
+    int stages;         /* shared-memory pipeline depth (kind 4: 6 when the TMA-fed
+                           streaming kernels run, 0 for the plain-load ones) */
     int ctas;           /* CTAs of the main kernel (persistent grid) */
     int packs_a, packs_b; /* 1 if the operand is repacked into the workspace */
     int vector_epilogue;  /* 1 if C is written with 16-byte stores */
     int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0),
-                           3 3xTF32 tensor-core kernel (after the split pre-pass) */
+                           3 3xTF32 tensor-core kernel (after the split pre-pass),
+                           4 skinny streaming kernel + split reduction (M or N <= 16) */
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
 } sgemmPlan_t;
 
