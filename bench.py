@@ -41,8 +41,9 @@ from fp32_sgemm_gb300 import inputs  # noqa: E402
 FFMA_PER_CLK_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
 PAGES_BEST_TFLOPS = 9.66           # best kernel of the pages at 4096^3 (RTX 3060, "09 Staged")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_ffma_4096_traffic.txt")
-KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_ffma.cuh", "fp32_sgemm_gb300/csrc/ptx.cuh",
-                  "fp32_sgemm_gb300/csrc/sgemm_api.cu", "fp32_sgemm_gb300/csrc/kernel_table.h"]
+# The FFMA kernel's code (with every tile configuration); how it is launched
+# is checked separately against the plan recorded beside the traffic figure.
+KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_ffma.cuh", "fp32_sgemm_gb300/csrc/ptx.cuh"]
 
 
 def parse_args():
@@ -78,9 +79,14 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic():
+def plan_signature(plan: dict) -> str:
+    return (f"tile {plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']} stages {plan['stages']} "
+            f"ctas {plan['ctas']} stream_k {plan['stream_k']}")
+
+
+def profiled_traffic(plan: dict):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current kernel sources and the same launch plan; else None."""
     try:
         fields = {}
         for line in open(PROFILE_SUMMARY):
@@ -88,6 +94,8 @@ def profiled_traffic():
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
         if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        if fields.get("plan") != plan_signature(plan):
             return None
         return float(fields["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -374,7 +382,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         peak_sus = sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
         roofline = {
             "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(),
+            "frac": achieved / peak, "traffic": profiled_traffic(plan) if w.name == "sgemm_4096" else None,
             "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x "
                           f"{max_mhz:.0f} MHz (max SM clock)",
             "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
