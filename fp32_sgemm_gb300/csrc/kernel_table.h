@@ -65,12 +65,19 @@ struct Tf32x3Args {
     int tiles_m, tiles_n, num_tiles;
     int k_blocks;
     int group_m;
+    // Stream-K (as for the FFMA kernel): tiles >= sk_tile0 are cut into
+    // (tile, K slice) units shared evenly by the CTAs; partial tiles go to
+    // `partials` (one BM x BN slot per CTA) and are announced in `flags`
+    // (one counter per CTA, zero at launch).  sk_tile0 == num_tiles: none.
+    int sk_tile0;
+    float *partials;
+    uint32_t *flags;
     uint32_t *err;
     uint64_t timeout_ns;
 };
 struct Tf32x3Info {
     const void *fn[4];   // variant index as for the FFMA kernels
-    int threads, smem, bm, bn, bk, stages;
+    int threads, smem, bm, bn, bk, stages, chunk_kb;
 };
 constexpr int kNumTf32x3Configs = 3;
 Tf32x3Info tf32x3_info(int config);   // 1-based tile configuration

@@ -239,6 +239,12 @@ bool c_vector_ok(const Problem &q) {
 // slower than both everywhere and is only used when asked for.
 int choose_tf32x3_config(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= sg::kNumTf32x3Configs) return h->algo;
+    // With stream-K evening out the last wave, the widest tile wins as soon
+    // as it fills the chip once: it reads the fewest shared-memory bytes per
+    // MMA, the resource this kernel is bound by.
+    if (h->schedule != 1 && ceil_div(q.M, 128) * ceil_div(q.N, 256) * q.batch >= h->sm_count &&
+        ceil_div(q.K, 32) >= 4)
+        return 3;
     const double width[2] = {128.0, 256.0};
     const double eff[2] = {0.86, 0.91};
     const int cfg[2] = {1, 3};
@@ -258,7 +264,7 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
     pl.pub.kind = 3;
     pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
     pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
-    pl.kp = round_up(q.K, 4);
+    pl.kp = round_up(q.K, 32);     // split rows start on 128-byte lines
     if (ceil_div(q.K, 32) > 65535 || ceil_div(q.M, 32) > 65535) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.ws_split_a = align256(size_t(q.batch) * size_t(q.M) * size_t(pl.kp) * 4);
     pl.ws_split_b = align256(size_t(q.batch) * size_t(q.N) * size_t(pl.kp) * 4);
@@ -286,7 +292,28 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
         }
         occ = o;
     }
-    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, int64_t(h->sm_count) * occ));
+    const int64_t slots = int64_t(h->sm_count) * occ;
+    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, slots));
+    // Stream-K for a partial last wave, as for the FFMA kernel.
+    const double per_sm = double(pl.num_tiles) / double(slots);
+    const double dp_eff = per_sm / std::ceil(per_sm);
+    const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
+    const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
+    if (want_sk && pl.k_blocks >= 2 && units >= slots && units < kMaxDim) {
+        // Only the tiles past the last full wave are cut, when they give
+        // every CTA at least 8 K slices: CTAs working at different K offsets
+        // of many tiles at once would need all of those tiles' operands in
+        // L2 (four hi/lo streams), so the cut region is kept small.  With a
+        // thinner remainder, the last full wave joins it.
+        const int64_t waves = pl.num_tiles / slots;
+        const int64_t rem_units = (pl.num_tiles - waves * slots) * pl.k_blocks;
+        int64_t first = waves * slots;
+        if (rem_units < 8 * slots) first = waves >= 1 ? (waves - 1) * slots : 0;
+        pl.sk_tile0 = int(first);
+        pl.sk_ctas = int(slots);
+        pl.ws_flags = align256(size_t(slots) * 4);
+        pl.ws_partials = size_t(slots) * size_t(info.bm) * size_t(info.bn) * 4;
+    }
     pl.pub.tile_m = info.bm;
     pl.pub.tile_n = info.bn;
     pl.pub.tile_k = info.bk;
@@ -509,8 +536,20 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
     args.group_m = pl.group_m;
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
+    args.sk_tile0 = pl.num_tiles;
+    int ctas = pl.dp_ctas;
+    if (pl.sk_ctas > 0 && h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials) {
+        char *sk = ws + pl.ws_split;
+        args.sk_tile0 = pl.sk_tile0;
+        args.flags = reinterpret_cast<uint32_t *>(sk);
+        args.partials = reinterpret_cast<float *>(sk + pl.ws_flags);
+        ctas = pl.sk_ctas;
+        // Counters start at zero for every launch.
+        if (cudaMemsetAsync(args.flags, 0, size_t(ctas) * 4, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+    }
     void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
-    return launch_main(h, info.fn[pl.variant], pl.dp_ctas, info.threads, info.smem, kargs, stream);
+    return launch_main(h, info.fn[pl.variant], ctas, info.threads, info.smem, kargs, stream);
 }
 
 sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
@@ -915,7 +954,12 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
     Plan pl;
     st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    if (pl.pub.kind == 3) pl.pub.ctas = pl.dp_ctas;
+    if (pl.pub.kind == 3) {
+        const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
+                            h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials;
+        pl.pub.ctas = use_sk ? pl.sk_ctas : pl.dp_ctas;
+        pl.pub.stream_k = use_sk ? 1 : 0;
+    }
     if (pl.pub.kind == 1) {
         const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
                             h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;

@@ -36,31 +36,37 @@ __global__ void sgemm_pack_rows_kernel(const float *src, int64_t ld_src, int64_t
         }
 }
 
-// Transpose rows x cols matrices src[r][c] -> dst[c][r] through 32 x 128
-// tiles in shared memory (128-byte coalesced reads and writes; the tile's
-// row pitch of 129 words keeps both phases free of bank conflicts).
+// Transpose rows x cols matrices src[r][c] -> dst[c][r] through 64 x 64
+// tiles in shared memory: 16-byte reads along source rows (VEC_SRC, when the
+// source allows; else 4-byte reads) and 16-byte writes of 256-byte
+// destination row segments (VEC_DST).  Row pitch 65 keeps shared-memory
+// accesses at most two-way conflicted.
 //   SPLIT = false: plain copy (operands given transposed, for the FFMA path);
 //   SPLIT = true : dst gets tf32(x), dst2 gets tf32(x - tf32(x)) (3xTF32 path).
-template <bool SPLIT>
+template <bool SPLIT, bool VEC_SRC, bool VEC_DST>
 __global__ void __launch_bounds__(256)
 sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
                        float *__restrict__ dst, float *__restrict__ dst2, int64_t ld_dst,
                        int64_t s_dst, int rows, int cols, int batch) {
-    __shared__ float t0[32][129];
-    __shared__ float t1[SPLIT ? 32 : 1][SPLIT ? 129 : 1];
-    const int c0 = blockIdx.x * 128;     // source columns
-    const int r0 = blockIdx.y * 32;      // source rows
-    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+    __shared__ float t0[64][65];
+    __shared__ float t1[SPLIT ? 64 : 1][SPLIT ? 65 : 1];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;     // 16 x 16
+    const int c0 = blockIdx.x * 64;      // source columns
+    const int r0 = blockIdx.y * 64;      // source rows
     for (int64_t z = blockIdx.z; z < batch; z += gridDim.z) {
         const float *sb = src + z * s_src;
         float x[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = r0 + ty + 8 * i;
+            const int r = r0 + ty + 16 * i;
+            const int c = c0 + 4 * tx;
+            const float *sp = sb + (int64_t)r * ld_src + c;
+            if (VEC_SRC && r < rows && c + 3 < cols) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(sp));
+                x[i][0] = v.x; x[i][1] = v.y; x[i][2] = v.z; x[i][3] = v.w;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = c0 + tx + 32 * e;
-                x[i][e] = (r < rows && c < cols) ? __ldcs(&sb[(int64_t)r * ld_src + c]) : 0.f;
+                for (int e = 0; e < 4; ++e) x[i][e] = (r < rows && c + e < cols) ? __ldcs(sp + e) : 0.f;
             }
         }
 #pragma unroll
@@ -69,23 +75,42 @@ sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_
             for (int e = 0; e < 4; ++e) {
                 if constexpr (SPLIT) {
                     const float xh = tf32_rna(x[i][e]);
-                    t0[ty + 8 * i][tx + 32 * e] = xh;
-                    t1[ty + 8 * i][tx + 32 * e] = tf32_rna(x[i][e] - xh);
+                    t0[ty + 16 * i][4 * tx + e] = xh;
+                    t1[ty + 16 * i][4 * tx + e] = tf32_rna(x[i][e] - xh);
                 } else {
-                    t0[ty + 8 * i][tx + 32 * e] = x[i][e];
+                    t0[ty + 16 * i][4 * tx + e] = x[i][e];
                 }
             }
         __syncthreads();
-        const int r = r0 + tx;
         float *db = dst + z * s_dst;
         float *db2 = SPLIT ? dst2 + z * s_dst : nullptr;
-#pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
-            const int cl = ty + 8 * j;
-            const int c = c0 + cl;
-            if (c < cols && r < rows) {
-                db[(int64_t)c * ld_dst + r] = t0[tx][cl];
-                if constexpr (SPLIT) db2[(int64_t)c * ld_dst + r] = t1[tx][cl];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int cl = ty + 16 * j;
+            const int c = c0 + cl;                   // destination row
+            const int r = r0 + 4 * tx;               // destination columns r .. r+3
+            if (c < cols) {
+                float *dp = db + (int64_t)c * ld_dst + r;
+                const float v[4] = {t0[4 * tx][cl], t0[4 * tx + 1][cl], t0[4 * tx + 2][cl], t0[4 * tx + 3][cl]};
+                if (VEC_DST && r + 3 < rows) {
+                    *reinterpret_cast<float4 *>(dp) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (r + e < rows) dp[e] = v[e];
+                }
+                if constexpr (SPLIT) {
+                    float *dp2 = db2 + (int64_t)c * ld_dst + r;
+                    const float w[4] = {t1[4 * tx][cl], t1[4 * tx + 1][cl], t1[4 * tx + 2][cl],
+                                        t1[4 * tx + 3][cl]};
+                    if (VEC_DST && r + 3 < rows) {
+                        *reinterpret_cast<float4 *>(dp2) = make_float4(w[0], w[1], w[2], w[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (r + e < rows) dp2[e] = w[e];
+                    }
+                }
             }
         }
         __syncthreads();
@@ -110,28 +135,36 @@ __global__ void sgemm_split_rows_kernel(const float *__restrict__ src, int64_t l
         }
 }
 
-// Same, 16 bytes at a time over the whole batch (src 16-byte aligned; the
-// pitches, batch strides and cols multiples of 4 floats).
-__global__ void sgemm_split_rows_vec4_kernel(const float4 *__restrict__ src, int64_t ld4, int64_t s4,
-                                             float4 *__restrict__ hi, float4 *__restrict__ lo,
-                                             int64_t ldd4, int64_t sd4, int64_t rows, int64_t cols4,
-                                             int64_t batch) {
-    const int64_t per = rows * cols4;
-    const int64_t total = per * batch;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t z = i / per;
-        const int64_t rem = i - z * per;
-        const int64_t r = rem / cols4, c = rem - r * cols4;
-        const float4 x = __ldcs(&src[z * s4 + r * ld4 + c]);
-        float4 xh, xl;
-        xh.x = tf32_rna(x.x); xl.x = tf32_rna(x.x - xh.x);
-        xh.y = tf32_rna(x.y); xl.y = tf32_rna(x.y - xh.y);
-        xh.z = tf32_rna(x.z); xl.z = tf32_rna(x.z - xh.z);
-        xh.w = tf32_rna(x.w); xl.w = tf32_rna(x.w - xh.w);
-        hi[z * sd4 + r * ldd4 + c] = xh;
-        lo[z * sd4 + r * ldd4 + c] = xl;
-    }
+// Same, 16 bytes at a time (src and dst 16-byte aligned; pitches, batch
+// strides and cols multiples of 4 floats).  A block covers 1024 float4 of a
+// row; each thread issues its four loads before any store.
+__global__ void __launch_bounds__(256)
+sgemm_split_rows_vec4_kernel(const float4 *__restrict__ src, int64_t ld4, int64_t s4,
+                             float4 *__restrict__ hi, float4 *__restrict__ lo, int64_t ldd4,
+                             int64_t sd4, int rows, int cols4, int batch) {
+    for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
+        for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+            const float4 *sr = src + z * s4 + r * ld4;
+            float4 *h = hi + z * sd4 + r * ldd4;
+            float4 *l = lo + z * sd4 + r * ldd4;
+            const int c = blockIdx.x * 1024 + threadIdx.x;
+            float4 x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (c + 256 * i < cols4) x[i] = __ldcs(&sr[c + 256 * i]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (c + 256 * i < cols4) {
+                    float4 xh, xl;
+                    xh.x = tf32_rna(x[i].x); xl.x = tf32_rna(x[i].x - xh.x);
+                    xh.y = tf32_rna(x[i].y); xl.y = tf32_rna(x[i].y - xh.y);
+                    xh.z = tf32_rna(x[i].z); xl.z = tf32_rna(x[i].z - xh.z);
+                    xh.w = tf32_rna(x[i].w); xl.w = tf32_rna(x[i].w - xh.w);
+                    h[c + 256 * i] = xh;
+                    l[c + 256 * i] = xl;
+                }
+            }
+        }
 }
 
 // Self test of the bounded wait: waits on a barrier that nothing completes.
@@ -175,23 +208,34 @@ void launch_pack_rows(const float *src, int64_t ld_src, int64_t s_src, float *ds
 
 void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
                       int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s) {
-    dim3 grid(unsigned(cdiv(cols, 128)), unsigned(cdiv(rows, 32)), zdim(batch));
-    if (dst2 != nullptr)
-        sgemm_transpose_kernel<true><<<grid, dim3(32, 8), 0, s>>>(src, ld_src, s_src, dst, dst2, ld_dst,
-                                                                 s_dst, rows, cols, batch);
-    else
-        sgemm_transpose_kernel<false><<<grid, dim3(32, 8), 0, s>>>(src, ld_src, s_src, dst, nullptr, ld_dst,
-                                                                  s_dst, rows, cols, batch);
+    dim3 grid(unsigned(cdiv(cols, 64)), unsigned(cdiv(rows, 64)), zdim(batch));
+    const bool vs = reinterpret_cast<uintptr_t>(src) % 16 == 0 && ld_src % 4 == 0 &&
+                    (batch == 1 || s_src % 4 == 0);
+    const bool vd = reinterpret_cast<uintptr_t>(dst) % 16 == 0 && ld_dst % 4 == 0 &&
+                    (batch == 1 || s_dst % 4 == 0) &&
+                    (dst2 == nullptr || reinterpret_cast<uintptr_t>(dst2) % 16 == 0);
+    auto go = [&](auto kernel) {
+        kernel<<<grid, 256, 0, s>>>(src, ld_src, s_src, dst, dst2, ld_dst, s_dst, rows, cols, batch);
+    };
+    if (dst2 != nullptr) {
+        if (vs && vd) go(sgemm_transpose_kernel<true, true, true>);
+        else if (vd) go(sgemm_transpose_kernel<true, false, true>);
+        else go(sgemm_transpose_kernel<true, false, false>);
+    } else {
+        if (vs && vd) go(sgemm_transpose_kernel<false, true, true>);
+        else if (vd) go(sgemm_transpose_kernel<false, false, true>);
+        else go(sgemm_transpose_kernel<false, false, false>);
+    }
 }
 
 void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *hi, float *lo,
                        int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s) {
     const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && ld_src % 4 == 0 && cols % 4 == 0 &&
                      ld_dst % 4 == 0 && (batch == 1 || (s_src % 4 == 0 && s_dst % 4 == 0));
-    if (vec) {
-        const int64_t total = int64_t(rows) * (cols / 4) * batch;
-        const int64_t blocks = std::min<int64_t>(cdiv(total, 256), int64_t(num_sms()) * 8);
-        sgemm_split_rows_vec4_kernel<<<unsigned(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
+    if (vec && reinterpret_cast<uintptr_t>(hi) % 16 == 0 && reinterpret_cast<uintptr_t>(lo) % 16 == 0) {
+        dim3 grid(unsigned(std::max<int64_t>(1, cdiv(cols / 4, 1024))), unsigned(std::min<int64_t>(rows, 65535)),
+                  zdim(batch));
+        sgemm_split_rows_vec4_kernel<<<grid, 256, 0, s>>>(
             reinterpret_cast<const float4 *>(src), ld_src / 4, s_src / 4, reinterpret_cast<float4 *>(hi),
             reinterpret_cast<float4 *>(lo), ld_dst / 4, s_dst / 4, rows, cols / 4, batch);
         return;

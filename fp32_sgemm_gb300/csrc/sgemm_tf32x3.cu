@@ -53,12 +53,82 @@ struct Tf32x3Config {
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;
     static constexpr int NUM_BARRIERS = 2 * STAGES + 5;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16 + 1024;
+    // Per epilogue warp, a padded 32 x 33 float tile to turn its rows into
+    // coalesced row segments of C (the staged epilogue).
+    static constexpr int XPOSE_BYTES = EPI_WARPS * 32 * 33 * 4;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16 + XPOSE_BYTES + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
     static_assert(EPI_WARPS % 4 == 0 && SLAB % 32 == 0 && SLAB * (EPI_WARPS / 4) == BN, "epilogue slabs");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM");
     static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
 };
+
+// Work of one CTA as segments, K slices [kb0, kb1) of tile t: whole tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... below sk_tile0, then an equal
+// contiguous share of the (tile, slice) units of the tiles from sk_tile0 on
+// ("stream-K").  A tile cut between CTAs is finished by the CTA holding its
+// first slice, whose last segment that is; the others (each CTA has at most
+// one such segment, its first) store partial sums.  All three roles of the
+// CTA walk the same sequence.
+struct TcSegment {
+    int t, kb0, kb1;
+};
+
+struct TcWork {
+    int t, u, u_end;
+    __device__ __forceinline__ void begin(const Tf32x3Args &p) {
+        t = blockIdx.x;
+        const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
+        const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
+        u = (int)(base + (int64_t)blockIdx.x * W / gridDim.x);
+        u_end = (int)(base + (int64_t)(blockIdx.x + 1) * W / gridDim.x);
+    }
+    __device__ __forceinline__ bool get(const Tf32x3Args &p, TcSegment &s) const {
+        if (t < p.sk_tile0) {
+            s.t = t;
+            s.kb0 = 0;
+            s.kb1 = p.k_blocks;
+            return true;
+        }
+        if (u >= u_end) return false;
+        s.t = u / p.k_blocks;
+        s.kb0 = u - s.t * p.k_blocks;
+        s.kb1 = min(p.k_blocks, s.kb0 + (u_end - u));
+        return true;
+    }
+    __device__ __forceinline__ void advance(const Tf32x3Args &p, const TcSegment &s) {
+        if (t < p.sk_tile0) t += gridDim.x;
+        else u += s.kb1 - s.kb0;
+    }
+};
+
+// The CTA whose stream-K unit range contains unit u.
+__device__ __forceinline__ int tc_cta_of_unit(int u, const Tf32x3Args &p) {
+    const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
+    const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
+    return (int)((((int64_t)u - base + 1) * gridDim.x - 1) / W);
+}
+
+__device__ __forceinline__ void prefetch_l2(const float *p) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
+__device__ __forceinline__ void red_release_add_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until a counter reaches `target` (acquire).
+__device__ __forceinline__ bool count_wait_bounded(const uint32_t *p, uint32_t target, uint64_t timeout_ns) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return false;
+}
 
 template <class Cfg, bool BETA_ZERO, bool C_VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
@@ -79,6 +149,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     uint64_t *tempty = tfull + 2;               // epilogue -> MMA, per accumulator
     uint64_t *drain = tempty + 2;               // MMA completion before teardown
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    float *xpose = reinterpret_cast<float *>(tmem_slot + 4);     // 16 bytes after the barriers
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -111,10 +182,13 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        TcWork w;
+        w.begin(p);
+        TcSegment seg;
+        while (ok && w.get(p, seg)) {
             int bt, tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
+            tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
+            for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                     record_error(p.err, kSiteProducerEmpty);
                     ok = false;
@@ -129,6 +203,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            w.advance(p, seg);
         }
         if (!ok) {
             // Let this CTA's own copies land before it can exit.
@@ -144,51 +219,63 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         // ---------------- MMA issuer ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int gc = 0;             // chunk counter across tiles: TMEM buffer gc & 1
+        int gc = 0;             // chunk counter across segments: TMEM buffer gc & 1
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-            for (int kb0 = 0; ok && kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB, ++gc) {
-                const int ab = gc & 1;
-                const uint32_t use = (uint32_t)(gc >> 1);
-                if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
+        // One accumulator chunk: K slices [kb0, kb1) into TMEM buffer gc & 1.
+        auto chunk = [&](int kb0, int kb1) {
+            const int ab = gc & 1;
+            const uint32_t use = (uint32_t)(gc >> 1);
+            ++gc;
+            if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
+                record_error(p.err, kSiteConsumerFull);
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
-                    break;
+                    return;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
-                const int kb1 = min(p.k_blocks, kb0 + Cfg::CHUNK_KB);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
-                        record_error(p.err, kSiteConsumerFull);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t s_ahi = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-                    const uint32_t s_alo = s_ahi + Cfg::A_BYTES;
-                    const uint32_t s_bhi = s_ahi + 2 * Cfg::A_BYTES;
-                    const uint32_t s_blo = s_bhi + Cfg::B_BYTES;
+                const uint32_t s_ahi = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+                const uint32_t s_alo = s_ahi + Cfg::A_BYTES;
+                const uint32_t s_bhi = s_ahi + 2 * Cfg::A_BYTES;
+                const uint32_t s_blo = s_bhi + Cfg::B_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 8; ++kk) {
-                        // K = 8 tf32 values = 32 bytes per MMA along the swizzled row.
-                        const uint32_t off = (uint32_t)kk * 32u;
-                        const uint64_t a_hi = smem_desc_k_sw128(s_ahi + off);
-                        const uint64_t a_lo = smem_desc_k_sw128(s_alo + off);
-                        const uint64_t b_hi = smem_desc_k_sw128(s_bhi + off);
-                        const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
-                        const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-                        // Small terms first, then the dominant product.
-                        mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
-                        mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
-                        mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
-                    }
-                    mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    // K = 8 tf32 values = 32 bytes per MMA along the swizzled row.
+                    const uint32_t off = (uint32_t)kk * 32u;
+                    const uint64_t a_hi = smem_desc_k_sw128(s_ahi + off);
+                    const uint64_t a_lo = smem_desc_k_sw128(s_alo + off);
+                    const uint64_t b_hi = smem_desc_k_sw128(s_bhi + off);
+                    const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
+                    const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+                    // Small terms first, then the dominant product.
+                    mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
+                    mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
+                    mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
                 }
-                if (!ok) break;
-                mma_commit(&tfull[ab]);             // chunk ready for the epilogue
+                mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            mma_commit(&tfull[ab]);             // chunk ready for the epilogue
+        };
+        // Whole tiles, then the stream-K segments (the same order as the
+        // producer and the epilogue walk).
+        for (int t = blockIdx.x; ok && t < p.sk_tile0; t += gridDim.x)
+            for (int kb0 = 0; ok && kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB)
+                chunk(kb0, min(p.k_blocks, kb0 + Cfg::CHUNK_KB));
+        TcWork w;
+        w.begin(p);
+        w.t = p.sk_tile0;                       // whole tiles done above
+        TcSegment seg;
+        while (ok && w.get(p, seg)) {
+            for (int kb0 = seg.kb0; ok && kb0 < seg.kb1; kb0 += Cfg::CHUNK_KB)
+                chunk(kb0, min(seg.kb1, kb0 + Cfg::CHUNK_KB));
+            w.advance(p, seg);
         }
         // All MMAs this thread issued complete before the CTA tears down.
         mma_commit(drain);
@@ -197,15 +284,35 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         // ---------------- epilogue: TMEM chunks -> FP32 sums -> C ----------------
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         constexpr int SLAB = Cfg::SLAB;
-        const int slab0 = ((warp - 2) >> 2) * SLAB;   // first column of this warp's slab
+        const int ew = warp - 2;                // epilogue warp index
+        const int slab0 = (ew >> 2) * SLAB;     // first column of this warp's slab
         const float alpha = p.alpha, beta = p.beta;
         int gc = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        TcWork w;
+        w.begin(p);
+        TcSegment seg;
+        while (ok && w.get(p, seg)) {
             float sum[SLAB];
 #pragma unroll
             for (int c = 0; c < SLAB; ++c) sum[c] = 0.f;
-            for (int kb0 = 0; kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB, ++gc) {
+            if constexpr (!BETA_ZERO) {
+                // This segment ends by reading C: start pulling this lane's
+                // row of the tile into L2 while the products are computed.
+                if (seg.kb0 == 0) {
+                    int bt, tm, tn;
+                    tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
+                    const int row = tm * BM + quarter * 32 + lane;
+                    const int c0 = tn * BN + slab0;
+                    if (row < p.M && c0 < p.N) {
+                        const float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
+                        const int c1 = min(p.N, c0 + SLAB) - 1;
+                        for (int c = c0; c < c1; c += 32) prefetch_l2(crow + c);
+                        prefetch_l2(crow + c1);
+                    }
+                }
+            }
+            for (int kb0 = seg.kb0; kb0 < seg.kb1; kb0 += Cfg::CHUNK_KB, ++gc) {
                 const int ab = gc & 1;
                 const uint32_t use = (uint32_t)(gc >> 1);
                 if (!mbar_wait_bounded(&tfull[ab], use & 1u, p.timeout_ns)) {
@@ -228,40 +335,139 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 if (lane == 0) mbar_arrive(&tempty[ab]);
             }
             if (!ok) break;
+
+            // ---------------- stream-K fixup ----------------
+            if (seg.kb0 != 0 || seg.kb1 != p.k_blocks) {
+                // Thread-major slot layout: the same (warp, lane) holds the
+                // same rows and columns in every CTA, so stores and loads of
+                // a slot are contiguous across the warp.
+                if (seg.kb0 != 0) {
+                    // Not the tile's first slice: hand the partial sums to the
+                    // CTA that finishes the tile, then go on.
+                    float4 *mine = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * (BM * BN));
+#pragma unroll
+                    for (int q = 0; q < SLAB / 4; ++q)
+                        __stcg(&mine[(ew * (SLAB / 4) + q) * 32 + lane],
+                               make_float4(sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3]));
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) red_release_add_gpu(&p.flags[blockIdx.x], 1u);
+                    w.advance(p, seg);
+                    continue;
+                }
+                // The tile's first slice: add the partial tiles of the CTAs
+                // that hold its other slices, in CTA order (deterministic).
+                const int tile_u0 = seg.t * p.k_blocks;
+                const int c_first = tc_cta_of_unit(tile_u0 + seg.kb1, p);
+                const int c_last = tc_cta_of_unit(tile_u0 + p.k_blocks - 1, p);
+                if (lane == 0) {
+                    for (int c = c_first; c <= c_last; ++c)
+                        if (!count_wait_bounded(&p.flags[c], (uint32_t)Cfg::EPI_WARPS, p.timeout_ns))
+                            record_error(p.err, kSiteStreamKFlag);
+                }
+                __syncwarp();
+                for (int c = c_first; c <= c_last; ++c) {
+                    const float4 *other = reinterpret_cast<const float4 *>(p.partials + (size_t)c * (BM * BN));
+#pragma unroll
+                    for (int q = 0; q < SLAB / 4; ++q) {
+                        const float4 v = __ldcg(&other[(ew * (SLAB / 4) + q) * 32 + lane]);
+                        sum[4 * q] += v.x;
+                        sum[4 * q + 1] += v.y;
+                        sum[4 * q + 2] += v.z;
+                        sum[4 * q + 3] += v.w;
+                    }
+                }
+            }
+
             int bt, tm, tn;
-            tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
-            const int row = tm * BM + quarter * 32 + lane;
-            if (row < p.M) {
-                float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
+            tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
+            float *cbase = p.C + (int64_t)bt * p.stride_c;
+            if constexpr (C_VEC) {
+                // Direct: each lane reads and writes its own row, 16 bytes at
+                // a time; the loads of a group of 16 columns are issued
+                // before its stores so that their latencies overlap.
+                const int row = tm * BM + quarter * 32 + lane;
+                if (row < p.M) {
+                    float *crow = cbase + (int64_t)row * p.ldc;
+                    constexpr int G = 4;             // float4 columns per group
 #pragma unroll
-                for (int q = 0; q < SLAB / 4; ++q) {
-                    const int col = tn * BN + slab0 + 4 * q;
-                    if (C_VEC && col + 3 < p.N) {
-                        float4 *dst = reinterpret_cast<float4 *>(crow + col);
-                        float4 o;
-                        if constexpr (BETA_ZERO) {
-                            o = make_float4(alpha * sum[4 * q], alpha * sum[4 * q + 1],
-                                            alpha * sum[4 * q + 2], alpha * sum[4 * q + 3]);
-                        } else {
-                            const float4 c = *dst;
-                            o = make_float4(fmaf(beta, c.x, alpha * sum[4 * q]),
-                                            fmaf(beta, c.y, alpha * sum[4 * q + 1]),
-                                            fmaf(beta, c.z, alpha * sum[4 * q + 2]),
-                                            fmaf(beta, c.w, alpha * sum[4 * q + 3]));
+                    for (int q0 = 0; q0 < SLAB / 4; q0 += G) {
+                        float4 cin[G];
+                        if constexpr (!BETA_ZERO) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) {
+                                const int col = tn * BN + slab0 + 4 * (q0 + j);
+                                if (col + 3 < p.N) {
+                                    cin[j] = *reinterpret_cast<const float4 *>(crow + col);
+                                } else {
+                                    cin[j].x = col < p.N ? crow[col] : 0.f;
+                                    cin[j].y = col + 1 < p.N ? crow[col + 1] : 0.f;
+                                    cin[j].z = col + 2 < p.N ? crow[col + 2] : 0.f;
+                                    cin[j].w = 0.f;
+                                }
+                            }
                         }
-                        *dst = o;
-                    } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (col + e < p.N) {
-                                float *dst = crow + col + e;
-                                if constexpr (BETA_ZERO) *dst = alpha * sum[4 * q + e];
-                                else *dst = fmaf(beta, *dst, alpha * sum[4 * q + e]);
+                        for (int j = 0; j < G; ++j) {
+                            const int q = q0 + j;
+                            const int col = tn * BN + slab0 + 4 * q;
+                            float o[4] = {alpha * sum[4 * q], alpha * sum[4 * q + 1], alpha * sum[4 * q + 2],
+                                          alpha * sum[4 * q + 3]};
+                            if constexpr (!BETA_ZERO) {
+                                o[0] = fmaf(beta, cin[j].x, o[0]);
+                                o[1] = fmaf(beta, cin[j].y, o[1]);
+                                o[2] = fmaf(beta, cin[j].z, o[2]);
+                                o[3] = fmaf(beta, cin[j].w, o[3]);
+                            }
+                            if (col + 3 < p.N) {
+                                *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    if (col + e < p.N) crow[col + e] = o[e];
+                            }
+                        }
+                    }
+                }
+            } else {
+                // Staged (C rows not 16-byte aligned): with 4-byte accesses
+                // one lane per row would touch 32 rows per instruction.  Each 32 x 32 block of the warp's rows goes
+                // through shared memory instead, so that lane l handles
+                // column l of one row at a time: 128-byte row segments.
+                float *tb = xpose + ew * (32 * 33);
+                const int row0 = tm * BM + quarter * 32;
+#pragma unroll
+                for (int b = 0; b < SLAB / 32; ++b) {
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) tb[lane * 33 + c] = sum[32 * b + c];
+                    __syncwarp();
+                    const int col = tn * BN + slab0 + 32 * b + lane;
+                    const bool col_ok = col < p.N;
+#pragma unroll
+                    for (int r0 = 0; r0 < 32; r0 += 16) {
+                        float cin[16];
+                        if constexpr (!BETA_ZERO) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int row = row0 + r0 + j;
+                                cin[j] = (col_ok && row < p.M) ? cbase[(int64_t)row * p.ldc + col] : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int row = row0 + r0 + j;
+                            if (col_ok && row < p.M) {
+                                const float v = alpha * tb[(r0 + j) * 33 + lane];
+                                float *dst = cbase + (int64_t)row * p.ldc + col;
+                                if constexpr (BETA_ZERO) *dst = v;
+                                else *dst = fmaf(beta, cin[j], v);
                             }
                         }
                     }
                 }
             }
+            w.advance(p, seg);
         }
     }
 
@@ -290,6 +496,7 @@ Tf32x3Info make_info() {
     info.bn = Cfg::BN;
     info.bk = Cfg::BK;
     info.stages = Cfg::STAGES;
+    info.chunk_kb = Cfg::CHUNK_KB;
     return info;
 }
 }  // namespace

@@ -148,3 +148,52 @@ def test_every_tensor_tile_configuration(handle, config, shape):
         np.testing.assert_array_equal(_run(handle, q)[:, :N].astype(np.float64), _ref(q))
     finally:
         handle.set_algo(0)
+
+
+def test_plan_at_4096_is_wide_tiles_with_stream_k(handle):
+    A = torch.empty((4096, 4096), device="cuda")
+    B = torch.empty((4096, 4096), device="cuda")
+    C = torch.empty((4096, 4096), device="cuda")
+    handle._ensure_workspace(handle.workspace_size(4096, 4096, 4096, A.data_ptr(), 4096, B.data_ptr(), 4096))
+    plan = handle.plan(A, B, C)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["tile_n"] == 256
+    assert plan["stream_k"] == (1 if (4096 // 128) * (4096 // 256) % sms else 0)
+
+
+@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("config", [1, 3])
+@pytest.mark.parametrize("shape", [(1000, 1500, 700), (257, 255, 4000), (2048, 2048, 2048), (130, 4100, 96)])
+def test_tensor_schedules(handle, schedule, config, shape):
+    # schedule 2 cuts tiles between CTAs (stream-K) and adds the partial
+    # tiles in a fixup; schedule 1 keeps whole tiles.
+    M, N, K = shape
+    handle.set_algo(config)
+    handle.set_schedule(schedule)
+    try:
+        p = inputs.make_problem(M, N, K, seed=M + N + K + 7 * config + schedule, alpha=0.75, beta=-0.5)
+        _close(_run(handle, p)[:, :N], _ref(p))
+        q = inputs.make_problem(M, N, K, seed=M + N + K + 7 * config + schedule + 1000, kind="integer",
+                                alpha=0.75, beta=-0.5)
+        np.testing.assert_array_equal(_run(handle, q)[:, :N].astype(np.float64), _ref(q))
+    finally:
+        handle.set_algo(0)
+        handle.set_schedule(0)
+
+
+def test_stream_k_repeatable_bitwise(handle):
+    p = inputs.make_problem(1536, 1280, 2048, seed=77)
+    A, B = _dev(p.A), _dev(p.B)
+    handle.set_schedule(2)
+    try:
+        first = torch.empty((1536, 1280), device="cuda")
+        handle.gemm(A, B, first)
+        assert handle.plan(A, B, first)["stream_k"] == 1
+        C = torch.empty_like(first)
+        for _ in range(10):
+            handle.gemm(A, B, C)
+            assert torch.equal(C.view(torch.int32), first.view(torch.int32))
+    finally:
+        handle.set_schedule(0)
+    assert handle.device_error() == 0
+    _close(first.cpu().numpy(), _ref(p))
