@@ -78,7 +78,7 @@ struct sgemmContext {
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;   // around the main kernel, if set
     // sgemmHostEx pipeline: copy-in and copy-out streams and their events,
     // created with the handle.
-    static constexpr int kHostChunks = 4;
+    static constexpr int kHostChunks = 8;     // pieces of one sgemmHostEx call (at most 5)
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_begin = nullptr, ev_end = nullptr;
     cudaEvent_t ev_in[kHostChunks] = {}, ev_done[kHostChunks] = {};
@@ -909,32 +909,61 @@ sgemmStatus_t sgemmHostEx(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, floa
     float *dC = reinterpret_cast<float *>(base + align256(size_t(M) * lda_p * 4) +
                                           align256(size_t(K) * ldb_p * 4));
     const bool use_ab = K > 0 && alpha != 0.0f;
-    // Rows of A and C go up, get multiplied and come back in chunks: while
-    // chunk i is multiplied on `stream`, chunk i+1 is copied in on the
-    // handle's copy-in stream and chunk i-1 copied out on its copy-out
-    // stream.  B is copied in first (every chunk needs all of it).
-    const int chunks = int(std::max<int64_t>(1, std::min<int64_t>(sgemmContext::kHostChunks, M / 1024)));
+    // The product runs as a sequence of pieces of C, each multiplied on
+    // `stream` as soon as its operands are up, while the next operands are
+    // copied in on the handle's copy-in stream and finished pieces copied
+    // out on its copy-out stream.  Row blocks of at least 1024 rows (up to
+    // four); the first row block is cut into two column halves when N is
+    // large, so that the first multiplication needs only half of B: the
+    // copy-in order is B's left half, A's first rows, B's right half, then
+    // A's further row blocks (with C's matching parts when beta != 0).
+    struct Piece { int64_t r0, r1, c0, c1; };
+    Piece pieces[sgemmContext::kHostChunks];
+    int np = 0;
+    const int blocks = int(std::max<int64_t>(1, std::min<int64_t>(4, M / 1024)));
+    const int64_t cs = (M >= 2048 && N >= 2048) ? (N / 2) / 128 * 128 : N;   // tile- and 16-byte aligned
+    for (int bi = 0; bi < blocks; ++bi) {
+        const int64_t r0 = M * bi / blocks, r1 = M * (bi + 1) / blocks;
+        if (bi == 0 && cs < N) {
+            pieces[np++] = {r0, r1, 0, cs};
+            pieces[np++] = {r0, r1, cs, N};
+        } else {
+            pieces[np++] = {r0, r1, 0, N};
+        }
+    }
     auto fail = [](cudaError_t e) { return e != cudaSuccess; };
+    auto up = [&](float *dst, int64_t ldd, const float *src, int64_t lds, int64_t rows, int64_t cols) {
+        return rows > 0 && cols > 0 &&
+               fail(cudaMemcpy2DAsync(dst, ldd * 4, src, lds * 4, cols * 4, rows, cudaMemcpyHostToDevice, h->s_in));
+    };
     if (fail(cudaEventRecord(h->ev_begin, stream)) || fail(cudaStreamWaitEvent(h->s_in, h->ev_begin, 0)) ||
         fail(cudaStreamWaitEvent(h->s_out, h->ev_begin, 0)))
         return SGEMM_STATUS_LAUNCH_FAILED;
-    if (use_ab && fail(cudaMemcpy2DAsync(dB, ldb_p * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, h->s_in)))
-        return SGEMM_STATUS_LAUNCH_FAILED;
-    for (int c = 0; c < chunks; ++c) {
-        const int64_t r0 = M * c / chunks, r1 = M * (c + 1) / chunks, rows = r1 - r0;
-        if (use_ab && fail(cudaMemcpy2DAsync(dA + r0 * lda_p, lda_p * 4, A + r0 * lda, lda * 4, K * 4, rows,
-                                             cudaMemcpyHostToDevice, h->s_in)))
+    int64_t a_rows_up = 0, b_cols_up = 0;    // how much of A (rows) and B (columns) is up
+    for (int i = 0; i < np; ++i) {
+        const Piece &pc = pieces[i];
+        if (use_ab) {
+            if (pc.c1 > b_cols_up) {
+                if (up(dB + b_cols_up, ldb_p, B + b_cols_up, ldb, K, pc.c1 - b_cols_up)) return SGEMM_STATUS_LAUNCH_FAILED;
+                b_cols_up = pc.c1;
+            }
+            if (pc.r1 > a_rows_up) {
+                if (up(dA + a_rows_up * lda_p, lda_p, A + a_rows_up * lda, lda, pc.r1 - a_rows_up, K))
+                    return SGEMM_STATUS_LAUNCH_FAILED;
+                a_rows_up = pc.r1;
+            }
+        }
+        if (beta != 0.0f && up(dC + pc.r0 * ldc_p + pc.c0, ldc_p, C + pc.r0 * ldc + pc.c0, ldc, pc.r1 - pc.r0,
+                               pc.c1 - pc.c0))
             return SGEMM_STATUS_LAUNCH_FAILED;
-        if (beta != 0.0f && fail(cudaMemcpy2DAsync(dC + r0 * ldc_p, ldc_p * 4, C + r0 * ldc, ldc * 4, N * 4,
-                                                   rows, cudaMemcpyHostToDevice, h->s_in)))
+        if (fail(cudaEventRecord(h->ev_in[i], h->s_in)) || fail(cudaStreamWaitEvent(stream, h->ev_in[i], 0)))
             return SGEMM_STATUS_LAUNCH_FAILED;
-        if (fail(cudaEventRecord(h->ev_in[c], h->s_in)) || fail(cudaStreamWaitEvent(stream, h->ev_in[c], 0)))
-            return SGEMM_STATUS_LAUNCH_FAILED;
-        st = run(h, rows, N, K, alpha, dA + r0 * lda_p, lda_p, dB, ldb_p, beta, dC + r0 * ldc_p, ldc_p, stream);
+        st = run(h, pc.r1 - pc.r0, pc.c1 - pc.c0, K, alpha, dA + pc.r0 * lda_p, lda_p, dB + pc.c0, ldb_p, beta,
+                 dC + pc.r0 * ldc_p + pc.c0, ldc_p, stream);
         if (st != SGEMM_STATUS_SUCCESS) return st;
-        if (fail(cudaEventRecord(h->ev_done[c], stream)) || fail(cudaStreamWaitEvent(h->s_out, h->ev_done[c], 0)) ||
-            fail(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * ldc_p, ldc_p * 4, N * 4, rows,
-                                   cudaMemcpyDeviceToHost, h->s_out)))
+        if (fail(cudaEventRecord(h->ev_done[i], stream)) || fail(cudaStreamWaitEvent(h->s_out, h->ev_done[i], 0)) ||
+            fail(cudaMemcpy2DAsync(C + pc.r0 * ldc + pc.c0, ldc * 4, dC + pc.r0 * ldc_p + pc.c0, ldc_p * 4,
+                                   (pc.c1 - pc.c0) * 4, pc.r1 - pc.r0, cudaMemcpyDeviceToHost, h->s_out)))
             return SGEMM_STATUS_LAUNCH_FAILED;
     }
     // Join: work enqueued on `stream` after this call sees the result.

@@ -192,9 +192,11 @@ sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K,
  * operands are copied into `dev_workspace` (device memory of at least
  * sgemmHostWorkspaceSize() bytes, owned by the caller), the product runs
  * there, and the M x N result is copied back into C.  The copies overlap the
- * arithmetic: B goes up first, then A and C move in up to four row chunks,
- * chunk i+1 copied in and chunk i-1 copied out (on two streams the handle
- * owns) while chunk i is multiplied on `stream`.  The call returns before
+ * arithmetic: C is computed in pieces (up to four row blocks, the first one
+ * cut into two column halves when M and N are at least 2048), each
+ * multiplied on `stream` as soon as its parts of A and B are up, while the
+ * next parts are copied in and finished pieces copied out (on two streams
+ * the handle owns).  The call returns before
  * the work finishes; everything it enqueued is ordered before later work on
  * `stream`, so synchronising `stream` makes C valid, and the host buffers
  * must stay untouched until then.  C is read (copied up) only when
