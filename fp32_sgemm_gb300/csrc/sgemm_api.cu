@@ -237,6 +237,16 @@ bool c_vector_ok(const Problem &q) {
 // grows with its width over the tensor-pipe efficiency measured at 8192^3
 // (128 x 128: 0.86, shared-memory bound; 128 x 256: 0.91).  128 x 192 was
 // slower than both everywhere and is only used when asked for.
+// CTAs of a stream-K launch (0: none).  At least half a wave of tiles:
+// every resident CTA.  Fewer: each tile's K range is cut into s pieces, s as
+// large as the slots allow but at most 16 (the CTA that finishes a tile
+// adds the other pieces' partial tiles one after another).
+int64_t stream_k_ctas(int64_t tiles, int64_t k_blocks, int64_t slots) {
+    if (2 * tiles > slots) return tiles * k_blocks >= slots ? slots : 0;
+    const int64_t s = std::min<int64_t>({slots / std::max<int64_t>(tiles, 1), 16, k_blocks});
+    return s >= 2 ? tiles * s : 0;
+}
+
 int choose_tf32x3_config(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= sg::kNumTf32x3Configs) return h->algo;
     // With stream-K evening out the last wave, the widest tile wins as soon
@@ -294,12 +304,20 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
     }
     const int64_t slots = int64_t(h->sm_count) * occ;
     pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, slots));
-    // Stream-K for a partial last wave, as for the FFMA kernel.
+    // Stream-K for a partial last wave, as for the FFMA kernel, where it
+    // pays: cutting tiles costs this kernel about a fifth of a tile's time
+    // (measured: partial-tile stores and loads, the counter handshake), so
+    // whole tiles stay when the last wave is more than 3/4 full; few tiles
+    // (at most half a wave) are split along K when K is deep (>= 1024;
+    // below that the split measured slower than one CTA per tile).
     const double per_sm = double(pl.num_tiles) / double(slots);
-    const double dp_eff = per_sm / std::ceil(per_sm);
+    const double frac = per_sm - std::floor(per_sm);
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
-    const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
-    if (want_sk && pl.k_blocks >= 2 && units >= slots && units < kMaxDim) {
+    const bool sk_pays = (per_sm >= 1.0 && frac > 0.0 && frac < 0.75) ||
+                         (2 * pl.num_tiles <= slots && pl.k_blocks >= 32);
+    const bool want_sk = h->schedule == 2 || (h->schedule == 0 && sk_pays);
+    const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots);
+    if (want_sk && pl.k_blocks >= 2 && units < kMaxDim && sk_ctas > 0) {
         // Only the tiles past the last full wave are cut, when they give
         // every CTA at least 8 K slices: CTAs working at different K offsets
         // of many tiles at once would need all of those tiles' operands in
@@ -310,9 +328,9 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
         int64_t first = waves * slots;
         if (rem_units < 8 * slots) first = waves >= 1 ? (waves - 1) * slots : 0;
         pl.sk_tile0 = int(first);
-        pl.sk_ctas = int(slots);
-        pl.ws_flags = align256(size_t(slots) * 4);
-        pl.ws_partials = size_t(slots) * size_t(info.bm) * size_t(info.bn) * 4;
+        pl.sk_ctas = int(sk_ctas);
+        pl.ws_flags = align256(size_t(sk_ctas) * 4);
+        pl.ws_partials = size_t(sk_ctas) * size_t(info.bm) * size_t(info.bn) * 4;
     }
     pl.pub.tile_m = info.bm;
     pl.pub.tile_n = info.bn;
@@ -420,15 +438,16 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     const double dp_eff = per_sm / std::ceil(per_sm);
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
     const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
-    if (want_sk && pl.k_blocks >= 2 && units >= slots && units < kMaxDim) {
+    const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots);
+    if (want_sk && pl.k_blocks >= 2 && units < kMaxDim && sk_ctas > 0) {
         // All but the last full wave of tiles run whole (their concurrent
         // tiles form a compact band, friendly to L2); the last wave plus the
         // remainder is split evenly in (tile, K slice) units.
         const int64_t waves = pl.num_tiles / slots;
         pl.sk_tile0 = waves >= 2 ? int((waves - 1) * slots) : 0;
-        pl.sk_ctas = int(slots);
-        pl.ws_flags = align256(size_t(slots) * 4);
-        pl.ws_partials = size_t(slots) * size_t(e.bm) * size_t(e.bn) * 4;
+        pl.sk_ctas = int(sk_ctas);
+        pl.ws_flags = align256(size_t(sk_ctas) * 4);
+        pl.ws_partials = size_t(sk_ctas) * size_t(e.bm) * size_t(e.bn) * 4;
     }
     pl.pub.tile_m = e.bm;
     pl.pub.tile_n = e.bn;

@@ -324,7 +324,20 @@ def test_workspace_required_without_workspace(sg):
     n = ctypes.c_size_t()
     assert lib.sgemmGetWorkspaceSize(h.ptr, 100, 64, 33, A.data_ptr(), 33, B.data_ptr(), 64,
                                      ctypes.byref(n)) == 0
-    assert n.value == (100 * 36 * 4 + 255) // 256 * 256
+    # Required: room to repack A (pitch 33 -> 36 floats).  The size query
+    # may add optional stream-K scratch on top.
+    required = (100 * 36 * 4 + 255) // 256 * 256
+    assert n.value >= required
+    # With exactly the required part the call runs (whole tiles).
+    ws = torch.empty(required, dtype=torch.uint8, device="cuda")
+    assert lib.sgemmSetWorkspace(h.ptr, ws.data_ptr(), required) == 0
+    A.copy_(torch.arange(100 * 33, device="cuda", dtype=torch.float32) % 5 - 2)
+    B.copy_(torch.arange(33 * 64, device="cuda", dtype=torch.float32) % 7 - 3)
+    assert lib.sgemmEx(h.ptr, 100, 64, 33, 1.0, A.data_ptr(), 33, B.data_ptr(), 64, 0.0,
+                       C.data_ptr(), 64, None) == 0
+    torch.cuda.synchronize()
+    ref = A.view(100, 33).double().cpu().numpy() @ B.view(33, 64).double().cpu().numpy()
+    np.testing.assert_array_equal(C.view(100, 64).cpu().numpy().astype(np.float64), ref)
     h.close()
 
 
