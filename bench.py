@@ -41,9 +41,12 @@ from fp32_sgemm_gb300 import inputs  # noqa: E402
 FFMA_PER_CLK_PER_SM = 128          # FP32 lanes per SM (4 sub-partitions x 32)
 PAGES_BEST_TFLOPS = 9.66           # best kernel of the pages at 4096^3 (RTX 3060, "09 Staged")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_ffma_4096_traffic.txt")
-# The FFMA kernel's code (with every tile configuration); how it is launched
-# is checked separately against the plan recorded beside the traffic figure.
+TENSOR_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_tf32x3_4096_traffic.txt")
+# A kernel's code (the FFMA kernel with every tile configuration; the
+# tensor-core kernel); how it is launched is checked separately against the
+# plan recorded beside the traffic figure.
 KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_ffma.cuh", "fp32_sgemm_gb300/csrc/ptx.cuh"]
+TENSOR_KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_tf32x3.cu", "fp32_sgemm_gb300/csrc/ptx.cuh"]
 
 
 def parse_args():
@@ -68,11 +71,13 @@ def parse_args():
     return ap.parse_args()
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES + sorted(
+    if sources is None:
+        sources = KERNEL_SOURCES + sorted(
             os.path.relpath(p, ROOT) for p in
-            __import__("glob").glob(os.path.join(ROOT, "fp32_sgemm_gb300", "csrc", "sgemm_algo*.cu"))):
+            __import__("glob").glob(os.path.join(ROOT, "fp32_sgemm_gb300", "csrc", "sgemm_algo*.cu")))
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(rel.encode())
             h.update(f.read())
@@ -84,16 +89,16 @@ def plan_signature(plan: dict) -> str:
             f"ctas {plan['ctas']} stream_k {plan['stream_k']}")
 
 
-def profiled_traffic(plan: dict):
+def profiled_traffic(plan: dict, summary: str = PROFILE_SUMMARY, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources and the same launch plan; else None."""
     try:
         fields = {}
-        for line in open(PROFILE_SUMMARY):
+        for line in open(summary):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-        if fields.get("kernel_source_sha256") != kernel_source_hash():
+        if fields.get("kernel_source_sha256") != kernel_source_hash(sources):
             return None
         if fields.get("plan") != plan_signature(plan):
             return None
@@ -400,6 +405,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         handle.set_math_mode(1)
         handle._ensure_workspace(handle.workspace_size(w.M, w.N, w.K, A0.data_ptr(), A0.stride(0),
                                                        B0.data_ptr(), B0.stride(0)))
+        tplan = handle.plan(A0, B0, C0, w.alpha, w.beta)
         t_el, t_k, _ = timed_loop(args.tensor_steps, args.warmup, False)
         handle.set_math_mode(0)
         t_step = t_el / args.tensor_steps
@@ -409,8 +415,14 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
             "ms_per_step": t_step, "steps": args.tensor_steps,
             "launches_per_step": 3,
             "roofline": tensor_roofline(flops, statistics.mean(t_k)),
+            "config": {"tile": f"{tplan['tile_m']}x{tplan['tile_n']}x{tplan['tile_k']}",
+                       "schedule": "stream-K" if tplan["stream_k"] else "whole tiles",
+                       "ctas": tplan["ctas"]},
         }
         tensor_path["roofline"]["kernel_ms_mean"] = statistics.mean(t_k)
+        if w.name == "sgemm_4096":
+            tensor_path["roofline"]["traffic"] = profiled_traffic(tplan, TENSOR_PROFILE_SUMMARY,
+                                                                  TENSOR_KERNEL_SOURCES)
 
     # End to end through the host-buffer C entry point: pinned host A, B (C),
     # copies up, product, copy of C down, all inside the timed region.
