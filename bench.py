@@ -86,7 +86,7 @@ def kernel_source_hash(sources=None) -> str:
 
 def plan_signature(plan: dict) -> str:
     return (f"tile {plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']} stages {plan['stages']} "
-            f"ctas {plan['ctas']} stream_k {plan['stream_k']}")
+            f"ctas {plan['ctas']} stream_k {plan['stream_k']} raster_group {plan['raster_group']}")
 
 
 def profiled_traffic(plan: dict, summary: str = PROFILE_SUMMARY, sources=None):

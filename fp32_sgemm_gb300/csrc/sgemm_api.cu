@@ -184,7 +184,7 @@ struct Plan {
     int64_t lda_p = 0, ldb_p = 0, sa_p = 0, sb_p = 0;
     size_t ws_a = 0, ws_b = 0;      // repacked A / B
     size_t ws_flags = 0, ws_partials = 0;   // stream-K scratch (0 when not used)
-    int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 8;
+    int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 16;
     int k_blocks = 0;
     int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
     int sk_tile0 = 0;               // first tile of the stream-K part
@@ -1002,6 +1002,7 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
     Plan pl;
     st = make_plan(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
     if (st != SGEMM_STATUS_SUCCESS) return st;
+    if (pl.pub.kind == 1 || pl.pub.kind == 3) pl.pub.raster_group = pl.group_m;
     if (pl.pub.kind == 3) {
         const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
                             h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials;

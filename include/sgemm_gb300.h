@@ -230,6 +230,8 @@ typedef struct sgemmPlan {
                            3 3xTF32 tensor-core kernel (after the split pre-pass),
                            4 skinny streaming kernel + split reduction (M or N <= 16) */
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
+    int raster_group;   /* tile rows per band of the tile order (tiles running together
+                           share rows of A and columns of B in L2); 0 if no tiles */
 } sgemmPlan_t;
 
 sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
