@@ -285,6 +285,23 @@ def workload_config(w, l2_note: str) -> dict:
 
 # ------------------------------------------------------------------ GPU path
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest per-rank value over the process group (a job takes as long
+    as its slowest rank); the value itself without a group of several."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def run_ours(args, w, rank: int, world: int, local_rank: int):
     import torch
     import fp32_sgemm_gb300 as sg
@@ -349,10 +366,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         elapsed = t_begin.elapsed_time(t_end)
         kms = [a.elapsed_time(b) for a, b in zip(kstart, kstop)]
         assert handle.device_error() == 0
-        if world > 1:
-            t = torch.tensor([elapsed], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, dev)
         return elapsed, kms, clocks
 
     dist = None
@@ -362,7 +376,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
 
     flops = 2.0 * w.M * w.N * w.K
     ms_per_step = elapsed_ms / args.steps
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms_per_step)
 
     mean_launch_ms = statistics.mean(launch_ms)
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
@@ -411,7 +425,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         t_step = t_el / args.tensor_steps
         tensor_path = {
             "math": "3xTF32 (tcgen05, error-compensated; same FP32 acceptance bound)",
-            "value": flops * world / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "value": job_tflops(flops, world, t_step), "unit": "TFLOP/s",
             "ms_per_step": t_step, "steps": args.tensor_steps,
             "launches_per_step": 3,
             "roofline": tensor_roofline(flops, statistics.mean(t_k)),
@@ -444,12 +458,9 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dev)
         h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0.0 else 0))
-        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(flops, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N,
                "ms_per_step": e_ms, "steps": args.e2e_steps,
                "path": "sgemmHostEx: pinned host A,B -> device, SGEMM, C -> pinned host"}
