@@ -175,6 +175,17 @@ EXTRA_WORKLOADS = {
     "skinny_n8": Workload("skinny_n8", 16384, 8, 16384, 1.0, 0.0, 13, True),
 }
 
+def pattern(rows, cols, seed: int = 0):
+    """Closed-form integer-valued operand entries, ((7 r + 13 c + 5 seed) mod 9)
+    - 4 in {-4..4}, for operands of several GB that the stream would take too
+    long to draw.  `rows` and `cols` are integer arrays (numpy or torch, any
+    broadcastable shapes); returns float32 of the broadcast shape, computed
+    the same way by either library, so the device copy of an operand and the
+    oracle's copy of the entries it needs agree exactly."""
+    v = (rows * 7 + cols * 13 + seed * 5) % 9 - 4
+    return v.astype("float32") if hasattr(v, "astype") else v.float()
+
+
 SAMPLE_SEED_XOR = 0x5A4D
 
 

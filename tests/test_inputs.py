@@ -80,3 +80,15 @@ def test_sample_entries_in_range_and_seeded():
     r2, c2 = inputs.sample_entries(8192, 8192, 65536, 4)
     assert np.array_equal(r, r2) and np.array_equal(c, c2)
     assert len(set(zip(r[:1000].tolist(), c[:1000].tolist()))) > 990
+
+
+def test_pattern_is_integer_valued_and_library_independent():
+    torch = pytest.importorskip("torch")
+    r = np.arange(40)[:, None]
+    c = np.arange(33)[None, :]
+    a = inputs.pattern(r, c, 3)
+    b = inputs.pattern(torch.from_numpy(r), torch.from_numpy(c), 3).numpy()
+    assert a.dtype == np.float32 and b.dtype == np.float32
+    np.testing.assert_array_equal(a, b)
+    assert set(np.unique(a)) <= set(range(-4, 5))
+    assert a[2, 5] == ((2 * 7 + 5 * 13 + 3 * 5) % 9) - 4
