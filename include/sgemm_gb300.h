@@ -30,6 +30,10 @@
  *     k is fixed for a given shape, so repeated calls give identical bits.
  *   - Errors are returned, never printed or raised; see sgemmStatus_t.
  *   - Thread safety: a handle may be used from one host thread at a time.
+ *   - CUDA graphs: sgemmEx(), sgemm() and sgemmStridedBatched() enqueue only
+ *     kernels and memsets on `stream`, so they can be captured, provided the
+ *     workspace they need is attached and the same shape was run once before
+ *     the capture (the first call of a kernel variant sets its attributes).
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -93,14 +97,19 @@ sgemmStatus_t sgemmDestroy(sgemmHandle_t handle);
 sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle);
 
 /*
- * Bytes of device workspace sgemmEx() can use for these operands:
+ * Bytes of device workspace sgemmEx() can use for these operands, under the
+ * handle's current math mode and schedule:
  *   - room to repack A and/or B when an operand cannot be read in place (base
  *     not 16-byte aligned or row pitch not a multiple of 16 bytes) into rows
  *     padded to a multiple of 4 floats: REQUIRED for such operands;
- *   - stream-K scratch (one ready flag and one BM x BN FP32 partial tile per
- *     resident CTA) when the output tiles do not divide evenly over the SMs:
+ *   - math mode 1 (3xTF32): the TF32 hi / lo parts of A and B: REQUIRED;
+ *   - stream-K scratch (one ready counter and one BM x BN FP32 partial tile
+ *     per CTA of the launch) when the output tiles do not divide evenly over
+ *     the SMs or are too few to fill them (their K ranges are then split):
  *     OPTIONAL; with less workspace the call runs whole tiles per CTA instead
- *     (same result up to summation order, less even load).
+ *     (same result up to summation order, less even load);
+ *   - skinny products (M or N <= 16): the partial sums of their K splits:
+ *     OPTIONAL; without them the main kernel runs.
  * Same validation as sgemmEx().  Calls that share a workspace must be
  * ordered on one stream.
  */

@@ -432,3 +432,31 @@ def test_kernel_events_bracket_the_main_kernel(sg, handle):
     assert k_ms > 0.05            # 17 GFLOP cannot take less than ~0.2 ms on FP32 FMA
     with pytest.raises(sg.SgemmError):
         handle.set_kernel_events(s, None)
+
+
+@pytest.mark.parametrize("math", [0, 1], ids=["ffma", "tf32x3"])
+def test_cuda_graph_capture_and_replay(sg, math):
+    # A call enqueues only capturable work (kernel launches and a memset on
+    # the given stream), so a product can be captured once and replayed.
+    h = sg.Handle()
+    h.set_math_mode(math)
+    try:
+        p = inputs.make_problem(384, 320, 1000, seed=71, kind="integer", alpha=0.5, beta=-1.0)
+        A, B = _to_dev(p.A), _to_dev(p.B)
+        C = _to_dev(p.C0)
+        h.gemm(A, B, C.clone(), p.alpha, p.beta)          # sizes the workspace outside the capture
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                h.gemm(A, B, C, p.alpha, p.beta, stream=s)
+        ref = p.C0.astype(np.float64)
+        for _ in range(3):
+            g.replay()
+            torch.cuda.synchronize()
+            ref = oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, ref.astype(np.float32))
+            np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), ref)
+        assert h.device_error() == 0
+    finally:
+        h.close()
