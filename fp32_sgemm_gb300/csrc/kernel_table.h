@@ -42,7 +42,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 11;
+constexpr int kNumAlgos = 13;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -54,6 +54,8 @@ void fill_algo8(KernelEntry *v);
 void fill_algo9(KernelEntry *v);
 void fill_algo10(KernelEntry *v);
 void fill_algo11(KernelEntry *v);
+void fill_algo12(KernelEntry *v);
+void fill_algo13(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {
@@ -81,8 +83,8 @@ struct Tf32x3Info {
 };
 constexpr int kNumTf32x3Configs = 3;
 Tf32x3Info tf32x3_info(int config);   // 1-based tile configuration
-// Skinny products, M <= 16 or N <= 16 (sgemm_skinny.cu).
-constexpr int kSkinnyMax = 16;
+// Skinny products, M <= 32 or N <= 32 (sgemm_skinny.cu).
+constexpr int kSkinnyMax = 32;
 int skinny_splits(bool small_m, int M, int N, int K, int sms);
 size_t skinny_workspace(int M, int N, int splits);
 void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *A, int64_t lda,
@@ -103,7 +105,7 @@ struct SkinnyTmaArgs {
     uint64_t timeout_ns;
 };
 struct SkinnyTmaGeom {
-    int rows = 0;        // the small dimension rounded up to 1, 2, 4, 8 or 16
+    int rows = 0;        // the small dimension rounded up to 1, 2, 4, 8, 16 or 32
     int kb = 0;
     int64_t units = 0;
     int ctas = 0, segs = 0, tile_elems = 0;

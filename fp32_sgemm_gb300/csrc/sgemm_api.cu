@@ -46,6 +46,8 @@ void init_kernel_table() {
     sg::fill_algo9(g_kernels[8]);
     sg::fill_algo10(g_kernels[9]);
     sg::fill_algo11(g_kernels[10]);
+    sg::fill_algo12(g_kernels[11]);
+    sg::fill_algo13(g_kernels[12]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -205,8 +207,13 @@ struct Plan {
 // fastest at 1024^3 to 8192^3; it is the automatic choice for every shape.
 constexpr int kDefaultAlgo = 10;
 
-int choose_algo(const sgemmContext *h) {
+// Products with at most 64 rows (columns) take the 64 x 256 (256 x 64)
+// tile, which computes no padding rows (columns) beyond 64; the rest the
+// 128 x 128 default.
+int choose_algo(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
+    if (q.M <= 64 && q.M <= q.N) return 12 - 1;
+    if (q.N <= 64) return 13 - 1;
     return kDefaultAlgo - 1;
 }
 
@@ -241,8 +248,11 @@ bool c_vector_ok(const Problem &q) {
 // every resident CTA.  Fewer: each tile's K range is cut into s pieces, s as
 // large as the slots allow but at most 16 (the CTA that finishes a tile
 // adds the other pieces' partial tiles one after another).
-int64_t stream_k_ctas(int64_t tiles, int64_t k_blocks, int64_t slots) {
+//   even_deep: with at least 8 K slices per slot and at most 16 pieces per
+//   tile, spread the units evenly over every slot instead (no slot idle).
+int64_t stream_k_ctas(int64_t tiles, int64_t k_blocks, int64_t slots, bool even_deep = false) {
     if (2 * tiles > slots) return tiles * k_blocks >= slots ? slots : 0;
+    if (even_deep && 16 * tiles >= slots && tiles * k_blocks >= 8 * slots) return slots;
     const int64_t s = std::min<int64_t>({slots / std::max<int64_t>(tiles, 1), 16, k_blocks});
     return s >= 2 ? tiles * s : 0;
 }
@@ -418,7 +428,7 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     pl.pub.packs_a = pl.prep_a != 0;
     pl.pub.packs_b = pl.prep_b != 0;
     pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
-    pl.algo_index = choose_algo(h);
+    pl.algo_index = choose_algo(h, q);
     pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
     pl.tiles_m = int(ceil_div(q.M, e.bm));
@@ -438,7 +448,7 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     const double dp_eff = per_sm / std::ceil(per_sm);
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
     const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
-    const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots);
+    const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots, true);
     if (want_sk && pl.k_blocks >= 2 && units < kMaxDim && sk_ctas > 0) {
         // All but the last full wave of tiles run whole (their concurrent
         // tiles form a compact band, friendly to L2); the last wave plus the

@@ -1,5 +1,5 @@
 // Skinny products, bound by HBM rather than by the FMA pipes: few rows of
-// C (M <= 16) or few columns (N <= 16).  The arithmetic intensity is about
+// C (M <= 32) or few columns (N <= 32).  The arithmetic intensity is about
 // M/2 (or N/2) FLOP per byte of the large operand, so at M = 1 no kernel can
 // beat streaming B once at HBM speed; the 128 x 128 tiles of the main kernel
 // would waste up to 127/128 of their FMAs here.
@@ -262,13 +262,15 @@ void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *
         else if (small <= 2) launch_m<2>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
         else if (small <= 4) launch_m<4>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
         else if (small <= 8) launch_m<8>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
-        else launch_m<16>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
+        else if (small <= 16) launch_m<16>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
+        else launch_m<32>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
     } else {
         if (small <= 1) launch_n<1>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
         else if (small <= 2) launch_n<2>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
         else if (small <= 4) launch_n<4>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
         else if (small <= 8) launch_n<8>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
-        else launch_n<16>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
+        else if (small <= 16) launch_n<16>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
+        else launch_n<32>(M, N, K, A, lda, B, ldb, part, splits, k_chunk, s);
     }
     const int64_t total = int64_t(M) * N;
     const unsigned blocks = unsigned(std::max<int64_t>(1, std::min<int64_t>(cdiv(total, 256), 65535)));

@@ -1,10 +1,10 @@
-// Skinny products fed by TMA: few rows of C (M <= 16) or few columns
-// (N <= 16), with the large operand streamed from HBM through a six-stage
+// Skinny products fed by TMA: few rows of C (M <= 32) or few columns
+// (N <= 32), with the large operand streamed from HBM through a six-stage
 // shared-memory ring.  These shapes do M/2 (or N/2) FLOP per byte of the
 // large operand, so the bound is HBM bandwidth; what a kernel must do is
 // keep enough bytes in flight per SM (bandwidth x latency, ~60 KB at
 // 44 GB/s per SM), which plain loads from registers do not reach at M = 8.
-// Here one producer thread per CTA keeps five to six 33 KB stages in flight.
+// Here one producer thread per CTA keeps five to six 34 KB stages in flight.
 //
 // Work decomposition.  The output is cut into blocks (small M: 1024 columns
 // of all M rows; small N: 512 rows of all N columns) and K into k-blocks
@@ -42,7 +42,7 @@ namespace {
 constexpr int kStages = 6;
 constexpr int kConsumers = 256;
 constexpr int kThreads = kConsumers + 32;        // + one producer warp
-constexpr int kStageBytes = 33792;               // 32 KB of the big operand + 1 KB
+constexpr int kStageBytes = 34816;               // 32 KB of the big operand + 2 KB
 
 // small M
 constexpr int kMBK = 8;                          // k per stage
@@ -159,19 +159,22 @@ skinny_m_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const unsigned char *st = smem + s * kStageBytes;
         const float *sB = reinterpret_cast<const float *>(st) + b_off;
         const float *sA = reinterpret_cast<const float *>(st + kMBBytes);
-        float4 b[kMBK];
+        // Two halves of 4 k each: 4 B rows in registers at a time.
 #pragma unroll
-        for (int k = 0; k < kMBK; ++k) b[k] = *reinterpret_cast<const float4 *>(sB + k * kMBoxN);
+        for (int kh = 0; kh < kMBK; kh += 4) {
+            float4 b[4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(sA + m * kMBK);
-            const float4 a1 = *reinterpret_cast<const float4 *>(sA + m * kMBK + 4);
-            const float av[kMBK] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            for (int k = 0; k < 4; ++k) b[k] = *reinterpret_cast<const float4 *>(sB + (kh + k) * kMBoxN);
 #pragma unroll
-            for (int k = 0; k < kMBK; ++k) {
-                const float2 a2 = make_float2(av[k], av[k]);
-                lo[m] = __ffma2_rn(a2, make_float2(b[k].x, b[k].y), lo[m]);
-                hi[m] = __ffma2_rn(a2, make_float2(b[k].z, b[k].w), hi[m]);
+            for (int m = 0; m < MT; ++m) {
+                const float4 a = *reinterpret_cast<const float4 *>(sA + m * kMBK + kh);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 a2 = make_float2(av[k], av[k]);
+                    lo[m] = __ffma2_rn(a2, make_float2(b[k].x, b[k].y), lo[m]);
+                    hi[m] = __ffma2_rn(a2, make_float2(b[k].z, b[k].w), hi[m]);
+                }
             }
         }
         __syncwarp();
@@ -339,7 +342,7 @@ void launch_n_tma(const CUtensorMap &a, const CUtensorMap &b, const SkinnyTmaArg
     skinny_n_tma_kernel<T><<<p.ctas, kThreads, kSmemBytes, s>>>(a, b, p);
 }
 
-inline int round_small(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : 16; }
+inline int round_small(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32; }
 
 }  // namespace
 
@@ -393,7 +396,8 @@ void launch_skinny_tma(bool small_m, const CUtensorMap &tmA, const CUtensorMap &
             case 2: launch_m_tma<2>(tmA, tmB, p, s); break;
             case 4: launch_m_tma<4>(tmA, tmB, p, s); break;
             case 8: launch_m_tma<8>(tmA, tmB, p, s); break;
-            default: launch_m_tma<16>(tmA, tmB, p, s); break;
+            case 16: launch_m_tma<16>(tmA, tmB, p, s); break;
+            default: launch_m_tma<32>(tmA, tmB, p, s); break;
         }
     } else {
         switch (g.rows) {
@@ -401,7 +405,8 @@ void launch_skinny_tma(bool small_m, const CUtensorMap &tmA, const CUtensorMap &
             case 2: launch_n_tma<2>(tmA, tmB, p, s); break;
             case 4: launch_n_tma<4>(tmA, tmB, p, s); break;
             case 8: launch_n_tma<8>(tmA, tmB, p, s); break;
-            default: launch_n_tma<16>(tmA, tmB, p, s); break;
+            case 16: launch_n_tma<16>(tmA, tmB, p, s); break;
+            default: launch_n_tma<32>(tmA, tmB, p, s); break;
         }
     }
     const int64_t total = int64_t(M) * N;

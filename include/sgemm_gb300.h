@@ -108,7 +108,7 @@ sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle);
  *     the SMs or are too few to fill them (their K ranges are then split):
  *     OPTIONAL; with less workspace the call runs whole tiles per CTA instead
  *     (same result up to summation order, less even load);
- *   - skinny products (M or N <= 16): the partial sums of their K splits:
+ *   - skinny products (M or N <= 32): the partial sums of their K splits:
  *     OPTIONAL; without them the main kernel runs.
  * Same validation as sgemmEx().  Calls that share a workspace must be
  * ordered on one stream.
@@ -237,7 +237,7 @@ typedef struct sgemmPlan {
     int vector_epilogue;  /* 1 if C is written with 16-byte stores */
     int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0),
                            3 3xTF32 tensor-core kernel (after the split pre-pass),
-                           4 skinny streaming kernel + split reduction (M or N <= 16) */
+                           4 skinny streaming kernel + split reduction (M or N <= 32) */
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
     int raster_group;   /* tile rows per band of the tile order (tiles running together
                            share rows of A and columns of B in L2); 0 if no tiles */
@@ -251,10 +251,12 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
 
 /*
  * Pin the main kernel's tile configuration for calls on this handle:
- * 0 = automatic choice by shape (default); 1..11 = a fixed configuration of
- * the 128 x 128 output tile (K slice 16 or 32, 3 or 4 pipeline stages, a
- * dedicated TMA warp or TMA issued by a compute thread, one or two CTAs per
- * SM; see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1 (3xTF32)
+ * 0 = automatic choice by shape (default: 12 for at most 64 rows, 13 for at
+ * most 64 columns, else 10); 1..11 = a fixed configuration of the 128 x 128
+ * output tile (K slice 16 or 32, 3 or 4 pipeline stages, a dedicated TMA
+ * warp or TMA issued by a compute thread, one or two CTAs per SM, packed or
+ * scalar FMAs); 12 = 64 x 256, 13 = 256 x 64 (see
+ * fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1 (3xTF32)
  * the values 1..3 pick the tensor-core tile instead: 128 x 128, 128 x 192
  * or 128 x 256.  Every configuration computes the same result up to
  * summation order.

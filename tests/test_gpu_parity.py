@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 12)))
+@pytest.mark.parametrize("algo", list(range(1, 14)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
@@ -460,3 +460,19 @@ def test_cuda_graph_capture_and_replay(sg, math):
         assert h.device_error() == 0
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 4000, 1500), (64, 2048, 777), (48, 300, 5000),
+                                   (4000, 40, 1500), (2500, 64, 999), (700, 33, 3000)])
+def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
+    # 33..64 rows (columns): the 64 x 256 (256 x 64) tile configuration.
+    p = inputs.make_problem(M, N, K, seed=M + N + K, alpha=0.5, beta=0.25)
+    got = _gpu(sg, handle, p)[:, :N]
+    _assert_close(got, _ref(p))
+    q = inputs.make_problem(M, N, K, seed=M + N + K + 1000, kind="integer", alpha=0.5, beta=0.25)
+    np.testing.assert_array_equal(_gpu(sg, handle, q)[:, :N].astype(np.float64), _ref(q))
+    A = _to_dev(p.A)[:, :K]
+    B = _to_dev(p.B)[:, :N]
+    C = torch.empty((M, N), device="cuda")
+    plan = handle.plan(A, B, C)
+    assert plan["kind"] == 1 and (plan["tile_m"], plan["tile_n"]) == ((64, 256) if M <= N else (256, 64))

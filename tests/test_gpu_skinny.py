@@ -1,4 +1,4 @@
-"""Skinny products (M <= 16 or N <= 16): the HBM-bound streaming kernels vs
+"""Skinny products (M <= 32 or N <= 32): the HBM-bound streaming kernels vs
 the fp64 oracle.  Integer inputs bit exact (the split partial sums are
 exact), uniform inputs within the FP32 bound.  Operands TMA can read in
 place take the TMA-fed kernels (plan stages == 6); odd pitches and small
@@ -44,7 +44,7 @@ def _ref(p):
     return oracle.sgemm_ref(p.M, p.N, p.K, p.alpha, p.A, p.B, p.beta, p.C0)
 
 
-SMALL = [1, 2, 3, 5, 8, 13, 16]
+SMALL = [1, 2, 3, 5, 8, 13, 16, 17, 24, 32]
 BIG = [(1000, 129), (4097, 3000), (64, 5)]
 
 
@@ -101,6 +101,10 @@ def _aligned_problem(M, N, K, seed, kind, alpha=1.0, beta=0.0):
     (65539, 3, 48),         # 129 row blocks of 3 k-blocks
     (1000, 16, 2047),
     (600, 5, 16),
+    (32, 5000, 777),        # 32-row variant
+    (20, 2048, 4096),
+    (3000, 32, 999),        # 32-column variant
+    (5000, 27, 64),
 ])
 def test_tma_fed_kernels(handle, M, N, K):
     for kind in ("integer", "uniform"):
