@@ -421,6 +421,26 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         int bt, tm, tn;
         tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
 
+        if constexpr (!BETA_ZERO) {
+            // This segment finishes its tile (its first slice) and reads C:
+            // pull the tile's C rows into L2 while the products run.  Thread
+            // r of the consumers takes row r (all rows once, BM <= threads
+            // x 2), one prefetch per 128-byte line.
+            if (seg.kb0 == 0) {
+                for (int r = threadIdx.x; r < BM; r += CONSUMER_THREADS) {
+                    const int row = tm * BM + r;
+                    const int c0 = tn * BN;
+                    if (row < p.M && c0 < p.N) {
+                        const float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
+                        const int c1 = min(p.N, c0 + BN) - 1;
+                        for (int c = c0; c < c1; c += 32)
+                            asm volatile("prefetch.global.L2 [%0];" :: "l"(crow + c));
+                        asm volatile("prefetch.global.L2 [%0];" :: "l"(crow + c1));
+                    }
+                }
+            }
+        }
+
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -546,30 +566,38 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const int row = tm * BM + row0 + WR * i;
             if (row >= p.M) continue;
             float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
+            // Reading C: all of this row's loads are issued before its
+            // stores, so that their latencies overlap (a store followed by
+            // the next load of the same thread would serialise them).
+            float cin[NJ][4];
+            if constexpr (!BETA_ZERO) {
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int col = tn * BN + col0 + 4 * WC * j;
+                    if (C_VEC && col + 3 < p.N) {
+                        const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+                        cin[j][0] = c.x; cin[j][1] = c.y; cin[j][2] = c.z; cin[j][3] = c.w;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) cin[j][q] = col + q < p.N ? crow[col + q] : 0.f;
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
                 const int col = tn * BN + col0 + 4 * WC * j;
                 float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if constexpr (BETA_ZERO) v[q] = alpha * v[q];
+                    else v[q] = fmaf(beta, cin[j][q], alpha * v[q]);
+                }
                 if (C_VEC && col + 3 < p.N) {
-                    float4 *dst = reinterpret_cast<float4 *>(crow + col);
-                    float4 o;
-                    if constexpr (BETA_ZERO) {
-                        o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
-                    } else {
-                        const float4 c = *dst;
-                        o = make_float4(fmaf(beta, c.x, alpha * v[0]), fmaf(beta, c.y, alpha * v[1]),
-                                        fmaf(beta, c.z, alpha * v[2]), fmaf(beta, c.w, alpha * v[3]));
-                    }
-                    *dst = o;
+                    *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (col + q < p.N) {
-                            float *dst = crow + col + q;
-                            if constexpr (BETA_ZERO) *dst = alpha * v[q];
-                            else *dst = fmaf(beta, *dst, alpha * v[q]);
-                        }
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        if (col + q < p.N) crow[col + q] = v[q];
                 }
             }
         }
