@@ -566,11 +566,26 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const int row = tm * BM + row0 + WR * i;
             if (row >= p.M) continue;
             float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
-            // Reading C: all of this row's loads are issued before its
-            // stores, so that their latencies overlap (a store followed by
-            // the next load of the same thread would serialise them).
-            float cin[NJ][4];
-            if constexpr (!BETA_ZERO) {
+            if constexpr (BETA_ZERO) {
+                // C is only written: alpha * acc, 16 bytes at a time when allowed.
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int col = tn * BN + col0 + 4 * WC * j;
+                    float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+                    if (C_VEC && col + 3 < p.N) {
+                        *reinterpret_cast<float4 *>(crow + col) =
+                            make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (col + q < p.N) crow[col + q] = alpha * v[q];
+                    }
+                }
+            } else {
+                // Reading C: all of this row's loads are issued before its
+                // stores, so that their latencies overlap (a store followed
+                // by the next load of the same thread would serialise them).
+                float cin[NJ][4];
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     const int col = tn * BN + col0 + 4 * WC * j;
@@ -582,22 +597,19 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                         for (int q = 0; q < 4; ++q) cin[j][q] = col + q < p.N ? crow[col + q] : 0.f;
                     }
                 }
-            }
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const int col = tn * BN + col0 + 4 * WC * j;
-                float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+                for (int j = 0; j < NJ; ++j) {
+                    const int col = tn * BN + col0 + 4 * WC * j;
+                    float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if constexpr (BETA_ZERO) v[q] = alpha * v[q];
-                    else v[q] = fmaf(beta, cin[j][q], alpha * v[q]);
-                }
-                if (C_VEC && col + 3 < p.N) {
-                    *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
+                    for (int q = 0; q < 4; ++q) v[q] = fmaf(beta, cin[j][q], alpha * v[q]);
+                    if (C_VEC && col + 3 < p.N) {
+                        *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (col + q < p.N) crow[col + q] = v[q];
+                        for (int q = 0; q < 4; ++q)
+                            if (col + q < p.N) crow[col + q] = v[q];
+                    }
                 }
             }
         }
