@@ -48,6 +48,8 @@ void init_kernel_table() {
     sg::fill_algo11(g_kernels[10]);
     sg::fill_algo12(g_kernels[11]);
     sg::fill_algo13(g_kernels[12]);
+    sg::fill_algo14(g_kernels[13]);
+    sg::fill_algo15(g_kernels[14]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -202,18 +204,26 @@ struct Plan {
     sg::SkinnyTmaGeom skinny_geom;
 };
 
-// Configuration 10 (BK = 32, 3 stages, TMA issued by a compute thread, two
-// CTAs per SM, double-buffered 8-byte A and 16-byte B fragments) measured
-// fastest at 1024^3 to 8192^3; it is the automatic choice for every shape.
-constexpr int kDefaultAlgo = 10;
+// Configuration 15 (256 x 128 tile, eight consumer warps, one CTA per SM,
+// BK = 32, 4 stages, TMA issued by a compute thread, double-buffered 8-byte
+// A and 16-byte B fragments) measured fastest from 1024^3 to 8192^3.
+constexpr int kDefaultAlgo = 15;
 
-// Products with at most 64 rows (columns) take the 64 x 256 (256 x 64)
-// tile, which computes no padding rows (columns) beyond 64; the rest the
-// 128 x 128 default.
+// Tile configuration by shape.  Products with at most 64 rows (columns)
+// take the 64 x 256 (256 x 64) tile, which computes no padding rows
+// (columns) beyond 64.  Everything else takes one CTA of eight consumer
+// warps per SM (256 x 128, or 128 x 256 when the product is under 256 rows
+// or more than twice as wide as tall): two CTAs of four warps per SM run
+// mostly one at a time (measured: the warp scheduler favours the older
+// CTA, whose inline TMA issuer keeps it fed while the other CTA's ring
+// starves), whereas warps of one CTA are held together by the shared ring.
+// Tiny products (both sides <= 128) keep the single 128 x 128 tile.
 int choose_algo(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
     if (q.M <= 64 && q.M <= q.N) return 12 - 1;
     if (q.N <= 64) return 13 - 1;
+    if (q.M <= 128 && q.N <= 128) return 10 - 1;
+    if (q.M < 256 || q.N > 2 * q.M) return 14 - 1;
     return kDefaultAlgo - 1;
 }
 
