@@ -1,9 +1,11 @@
 // FP32 SGEMM main kernel for sm_103a: C = alpha * A.B + beta * C, row major.
 //
-// Structure (one persistent CTA per SM slot, tiles taken round robin):
-//   * one producer warp: one elected lane streams the K slices of A and B
-//     into an S-stage shared-memory ring with TMA tile loads; each stage has
-//     a "full" mbarrier (TMA transaction bytes) and an "empty" mbarrier (one
+// Structure (persistent CTAs, one per SM slot; tiles taken round robin,
+// then stream-K units):
+//   * a producer: thread 0 of the first consumer warp (or, in some
+//     configurations, a dedicated warp) streams the K slices of A and B into
+//     an S-stage shared-memory ring with TMA tile loads; each stage has a
+//     "full" mbarrier (TMA transaction bytes) and an "empty" mbarrier (one
 //     arrival per consumer warp).  Out-of-range rows/columns of partial tiles
 //     arrive as zeros (TMA out-of-bounds fill), so M, N, K need not be tile
 //     multiples.
@@ -79,7 +81,7 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 //   (lane grid WR x (32/WR) inside a warp);
 //   KA: k values per vector read of A (4 -> 16 B, 2 -> 8 B);
 //   PRODUCER_WARP: 1 = a dedicated TMA warp, 0 = thread 0 of the first
-//   consumer warp issues the loads (no extra warp, so two CTAs fit per SM);
+//   consumer warp issues the loads (no extra warp);
 //   PIPE: 1 = fragments of the next k are read while this k's FMAs run
 //   (explicit register double buffering), 0 = left to the compiler;
 //   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2).
