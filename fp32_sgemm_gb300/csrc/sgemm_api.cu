@@ -50,6 +50,8 @@ void init_kernel_table() {
     sg::fill_algo13(g_kernels[12]);
     sg::fill_algo14(g_kernels[13]);
     sg::fill_algo15(g_kernels[14]);
+    sg::fill_algo16(g_kernels[15]);
+    sg::fill_algo17(g_kernels[16]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -210,18 +212,19 @@ struct Plan {
 constexpr int kDefaultAlgo = 15;
 
 // Tile configuration by shape.  Products with at most 64 rows (columns)
-// take the 64 x 256 (256 x 64) tile, which computes no padding rows
-// (columns) beyond 64.  Everything else takes one CTA of eight consumer
-// warps per SM (256 x 128, or 128 x 256 when the product is under 256 rows
-// or more than twice as wide as tall): two CTAs of four warps per SM run
+// take the 64 x 512 (512 x 64) tile, which computes no padding rows
+// (columns) beyond 64.  Everything else takes 256 x 128, or 128 x 256 when
+// the product is under 256 rows or more than twice as wide as tall.  All of
+// these are one CTA of eight consumer warps per SM: two CTAs of four warps
+// per SM run
 // mostly one at a time (measured: the warp scheduler favours the older
 // CTA, whose inline TMA issuer keeps it fed while the other CTA's ring
 // starves), whereas warps of one CTA are held together by the shared ring.
 // Tiny products (both sides <= 128) keep the single 128 x 128 tile.
 int choose_algo(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
-    if (q.M <= 64 && q.M <= q.N) return 12 - 1;
-    if (q.N <= 64) return 13 - 1;
+    if (q.M <= 64 && q.M <= q.N) return 16 - 1;
+    if (q.N <= 64) return 17 - 1;
     if (q.M <= 128 && q.N <= 128) return 10 - 1;
     if (q.M < 256 || q.N > 2 * q.M) return 14 - 1;
     return kDefaultAlgo - 1;
@@ -665,9 +668,10 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
 
     CUtensorMap tmA, tmB;
-    st = encode_3d(&tmA, Ause, q.K, q.M, q.batch, pl.lda_p, pl.sa_p, e.bk, e.bm, swizzle_for_bk(e.bk));
+    // Boxes of at most 256 rows / columns; wider tiles load several.
+    st = encode_3d(&tmA, Ause, q.K, q.M, q.batch, pl.lda_p, pl.sa_p, e.bk, std::min(e.bm, 256), swizzle_for_bk(e.bk));
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    st = encode_3d(&tmB, Buse, q.N, q.K, q.batch, pl.ldb_p, pl.sb_p, e.bn, e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = encode_3d(&tmB, Buse, q.N, q.K, q.batch, pl.ldb_p, pl.sb_p, std::min(e.bn, 256), e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != SGEMM_STATUS_SUCCESS) return st;
 
     sg::GemmArgs args{};

@@ -110,12 +110,18 @@ struct FfmaConfig {
     static constexpr int SWZ_MASK = ROW_BYTES_A / 16 - 1;      // 7, 3, 1
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 128 + 1024;
     static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
+    // TMA boxes are at most 256 elements a side: wider tiles take several.
+    // A's boxes stack rows (the stage layout is unchanged); B's boxes sit one
+    // after another, each BK rows of BOX_N columns.
+    static constexpr int BOX_M = BM < 256 ? BM : 256, A_BOXES = BM / BOX_M;
+    static constexpr int BOX_N = BN < 256 ? BN : 256, B_BOXES = BN / BOX_N;
 
     static_assert(BK == 8 || BK == 16 || BK == 32, "A slice row must match a TMA swizzle span");
     static_assert(WR == 1 || WR == 2 || WR == 4 || WR == 8 || WR == 16 || WR == 32, "WR");
     static_assert(BM == WARPS_M * WTM && BN == WARPS_N * WTN, "tile / warp grid mismatch");
     static_assert(WTM * ROW_BYTES_A >= 1024, "warp row block must cover a swizzle period");
-    static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box dimension limit");
+    static_assert(BM <= 512 && BN <= 512 && BM % BOX_M == 0 && BN % BOX_N == 0, "TMA boxes per tile");
+    static_assert(BOX_N % WTN == 0, "a warp's columns lie in one B box");
     static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(KA == 2 || KA == 4, "A vector width");
     static_assert(NKQ % KQ_UNROLL == 0, "unroll must divide the slice");
@@ -253,8 +259,14 @@ __device__ __forceinline__ bool issue_slice(SliceCursor *sc, const GemmArgs &p,
     SliceCursor c = cursor_load(sc);
     if (!mbar_wait_bounded(&empty[c.stage], c.phase ^ 1u, p.timeout_ns)) return false;
     mbar_arrive_expect_tx(&full[c.stage], Cfg::STAGE_BYTES);
-    tma_load_3d(sA + c.stage * Cfg::A_STAGE_BYTES, tmA, &full[c.stage], c.kb * Cfg::BK, c.tm * Cfg::BM, c.bt);
-    tma_load_3d(sB + c.stage * Cfg::B_STAGE_BYTES, tmB, &full[c.stage], c.tn * Cfg::BN, c.kb * Cfg::BK, c.bt);
+#pragma unroll
+    for (int q = 0; q < Cfg::A_BOXES; ++q)
+        tma_load_3d(sA + c.stage * Cfg::A_STAGE_BYTES + q * (Cfg::BOX_M * Cfg::BK * 4), tmA, &full[c.stage],
+                    c.kb * Cfg::BK, c.tm * Cfg::BM + q * Cfg::BOX_M, c.bt);
+#pragma unroll
+    for (int q = 0; q < Cfg::B_BOXES; ++q)
+        tma_load_3d(sB + c.stage * Cfg::B_STAGE_BYTES + q * (Cfg::BK * Cfg::BOX_N * 4), tmB, &full[c.stage],
+                    c.tn * Cfg::BN + q * Cfg::BOX_N, c.kb * Cfg::BK, c.bt);
     ++c.issued;
     if (++c.stage == Cfg::STAGES) { c.stage = 0; c.phase ^= 1u; }
     if (++c.kb == c.seg.kb1) {
@@ -357,6 +369,9 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     const int row0 = wm * Cfg::WTM + lr;
     // Columns: n_j = col0 + 4*WC*j (+0..3).
     const int col0 = wn * Cfg::WTN + lc * 4;
+    // This lane's first column inside the stage's B boxes.
+    int b_off = col0;
+    if constexpr (Cfg::B_BOXES > 1) b_off = (col0 / Cfg::BOX_N) * (Cfg::BK * Cfg::BOX_N) + col0 % Cfg::BOX_N;
     // Swizzle term of row0's A row; rows of other i differ by a compile-time
     // constant d_i because lr*ROW_BYTES_A and WR*i*ROW_BYTES_A occupy disjoint bits.
     const uint32_t a_x0 = ((uint32_t)(lr * Cfg::ROW_BYTES_A) >> 7) & Cfg::SWZ_MASK;
@@ -377,7 +392,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     };
     // B: 16 values of row k, in 4 groups of 4 consecutive columns.
     auto load_b = [&](const float *Bs, int k, float4 (&b)[NJ]) {
-        const float *brow = Bs + k * BN;
+        const float *brow = Bs + k * Cfg::BOX_N;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) b[j] = *reinterpret_cast<const float4 *>(brow + j * 4 * WC);
     };
@@ -455,7 +470,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 return;
             }
             const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
-            const float *Bs = reinterpret_cast<const float *>(sB + stage * Cfg::B_STAGE_BYTES) + col0;
+            const float *Bs = reinterpret_cast<const float *>(sB + stage * Cfg::B_STAGE_BYTES) + b_off;
 
             if constexpr (Cfg::PIPE) {
                 // Register double buffering: while the FMAs of k run, the B
