@@ -42,7 +42,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 17;
+constexpr int kNumAlgos = 19;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -60,6 +60,8 @@ void fill_algo14(KernelEntry *v);
 void fill_algo15(KernelEntry *v);
 void fill_algo16(KernelEntry *v);
 void fill_algo17(KernelEntry *v);
+void fill_algo18(KernelEntry *v);
+void fill_algo19(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {

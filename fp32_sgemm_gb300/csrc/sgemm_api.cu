@@ -52,6 +52,8 @@ void init_kernel_table() {
     sg::fill_algo15(g_kernels[14]);
     sg::fill_algo16(g_kernels[15]);
     sg::fill_algo17(g_kernels[16]);
+    sg::fill_algo18(g_kernels[17]);
+    sg::fill_algo19(g_kernels[18]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -211,6 +213,18 @@ struct Plan {
 // A and 16-byte B fragments) measured fastest from 1024^3 to 8192^3.
 constexpr int kDefaultAlgo = 15;
 
+// 17 to 32 rows (columns), large enough to give every SM at least 8 K slices
+// of 32 x 1024 (1024 x 32) tiles: there the FFMA kernel with those tiles runs
+// at ~70% of the FMA peak and the streaming kernel's 32-row variant at ~50%
+// (measured at 16384-long K and N: 310 vs 408-416 us).  Smaller products
+// stay on the streaming kernel, which spreads them over every SM.
+bool thin_ffma_preferred(const sgemmContext *h, const Problem &q) {
+    if (h->algo != 0 || h->math != 0) return false;
+    const int64_t small = std::min(q.M, q.N), big = std::max(q.M, q.N);
+    if (small <= 16 || small > 32) return false;
+    return ceil_div(big, 1024) * ceil_div(q.K, 16) >= 8 * int64_t(h->sm_count);
+}
+
 // Tile configuration by shape.  Products with at most 64 rows (columns)
 // take the 64 x 512 (512 x 64) tile, which computes no padding rows
 // (columns) beyond 64.  Everything else takes 256 x 128, or 128 x 256 when
@@ -223,6 +237,8 @@ constexpr int kDefaultAlgo = 15;
 // Tiny products (both sides <= 128) keep the single 128 x 128 tile.
 int choose_algo(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
+    if (q.M <= 32 && q.M <= q.N) return 18 - 1;
+    if (q.N <= 32) return 19 - 1;
     if (q.M <= 64 && q.M <= q.N) return 16 - 1;
     if (q.N <= 64) return 17 - 1;
     if (q.M <= 128 && q.N <= 128) return 10 - 1;
@@ -379,7 +395,8 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     std::call_once(g_kernels_once, init_kernel_table);
     // Few rows or few columns: streaming kernels bound by HBM (either math
     // mode; their FMAs are FP32), when the workspace holds their partial sums.
-    if (q.opA == 0 && q.opB == 0 && q.batch == 1 && (q.M <= sg::kSkinnyMax || q.N <= sg::kSkinnyMax)) {
+    if (q.opA == 0 && q.opB == 0 && q.batch == 1 && (q.M <= sg::kSkinnyMax || q.N <= sg::kSkinnyMax) &&
+        !thin_ffma_preferred(h, q)) {
         const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
         if (skinny_tma_eligible(q, small_m)) {
             const sg::SkinnyTmaGeom g = sg::skinny_tma_geometry(small_m, int(q.M), int(q.N), int(q.K),
@@ -721,6 +738,7 @@ size_t workspace_bytes(const Plan &pl) {
 // query reports what they would use so that callers can provide it.
 size_t skinny_query_bytes(const sgemmContext *h, const Problem &q) {
     if (q.opA != 0 || q.opB != 0 || q.batch != 1 || q.empty() || q.K == 0 || q.alpha == 0.0f) return 0;
+    if (thin_ffma_preferred(h, q)) return 0;
     if (q.M > sg::kSkinnyMax && q.N > sg::kSkinnyMax) return 0;
     const bool small_m = q.M <= sg::kSkinnyMax && (q.M <= q.N || q.N > sg::kSkinnyMax);
     const int splits = sg::skinny_splits(small_m, int(q.M), int(q.N), int(q.K), h->sm_count);

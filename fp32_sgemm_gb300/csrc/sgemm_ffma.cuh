@@ -120,7 +120,7 @@ struct FfmaConfig {
     static_assert(WR == 1 || WR == 2 || WR == 4 || WR == 8 || WR == 16 || WR == 32, "WR");
     static_assert(BM == WARPS_M * WTM && BN == WARPS_N * WTN, "tile / warp grid mismatch");
     static_assert(WTM * ROW_BYTES_A >= 1024, "warp row block must cover a swizzle period");
-    static_assert(BM <= 512 && BN <= 512 && BM % BOX_M == 0 && BN % BOX_N == 0, "TMA boxes per tile");
+    static_assert(BM <= 1024 && BN <= 1024 && BM % BOX_M == 0 && BN % BOX_N == 0, "TMA boxes per tile");
     static_assert(BOX_N % WTN == 0, "a warp's columns lie in one B box");
     static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(KA == 2 || KA == 4, "A vector width");

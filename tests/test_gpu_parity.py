@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 18)))
+@pytest.mark.parametrize("algo", list(range(1, 20)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
@@ -464,9 +464,11 @@ def test_cuda_graph_capture_and_replay(sg, math):
 
 
 @pytest.mark.parametrize("M,N,K", [(33, 4000, 1500), (64, 2048, 777), (48, 300, 5000),
-                                   (4000, 40, 1500), (2500, 64, 999), (700, 33, 3000)])
+                                   (4000, 40, 1500), (2500, 64, 999), (700, 33, 3000),
+                                   (24, 16384, 4096), (32, 10000, 2500), (16384, 20, 4096)])
 def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
-    # 33..64 rows (columns): the 64 x 512 (512 x 64) tile configuration.
+    # 33..64 rows (columns): the 64 x 512 (512 x 64) tile configuration;
+    # 17..32 rows (columns), when large: 32 x 1024 (1024 x 32).
     p = inputs.make_problem(M, N, K, seed=M + N + K, alpha=0.5, beta=0.25)
     got = _gpu(sg, handle, p)[:, :N]
     _assert_close(got, _ref(p))
@@ -476,4 +478,6 @@ def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
     B = _to_dev(p.B)[:, :N]
     C = torch.empty((M, N), device="cuda")
     plan = handle.plan(A, B, C)
-    assert plan["kind"] == 1 and (plan["tile_m"], plan["tile_n"]) == ((64, 512) if M <= N else (512, 64))
+    small = min(M, N)
+    want = (64, 512) if small > 32 else (32, 1024)
+    assert plan["kind"] == 1 and (plan["tile_m"], plan["tile_n"]) == (want if M <= N else want[::-1])
