@@ -201,8 +201,9 @@ sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K,
  * operands are copied into `dev_workspace` (device memory of at least
  * sgemmHostWorkspaceSize() bytes, owned by the caller), the product runs
  * there, and the M x N result is copied back into C.  The copies overlap the
- * arithmetic: C is computed in pieces (up to four row blocks, the first one
- * cut into two column halves when M and N are at least 2048), each
+ * arithmetic: C is computed in pieces (a first block of 1024 rows cut into
+ * up to four column pieces when M is at least 2048, then up to three row
+ * blocks, the last at most 512 rows high), each
  * multiplied on `stream` as soon as its parts of A and B are up, while the
  * next parts are copied in and finished pieces copied out (on two streams
  * the handle owns).  The call returns before
