@@ -234,14 +234,15 @@ bool thin_ffma_preferred(const sgemmContext *h, const Problem &q) {
 // mostly one at a time (measured: the warp scheduler favours the older
 // CTA, whose inline TMA issuer keeps it fed while the other CTA's ring
 // starves), whereas warps of one CTA are held together by the shared ring.
-// Tiny products (both sides <= 128) keep the single 128 x 128 tile.
+// Small matrices (both sides <= 128, e.g. the entries of a batch of small
+// products) take the 128 x 128 tile, which wastes the least of its lanes.
 int choose_algo(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
+    if (q.M <= 128 && q.N <= 128) return 10 - 1;
     if (q.M <= 32 && q.M <= q.N) return 18 - 1;
     if (q.N <= 32) return 19 - 1;
     if (q.M <= 64 && q.M <= q.N) return 16 - 1;
     if (q.N <= 64) return 17 - 1;
-    if (q.M <= 128 && q.N <= 128) return 10 - 1;
     if (q.M < 256 || q.N > 2 * q.M) return 14 - 1;
     return kDefaultAlgo - 1;
 }

@@ -252,10 +252,10 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
 
 /*
  * Pin the main kernel's tile configuration for calls on this handle:
- * 0 = automatic choice by shape (default: 18 / 19 for large products of 17
- * to 32 rows / columns, 16 for at most 64 rows, 17 for at most 64 columns,
- * 10 when both sides are at most 128, 14 under 256 rows or
- * for products more than twice as wide as tall, else 15); 1..11 = a fixed
+ * 0 = automatic choice by shape (default: 10 when both sides are at most
+ * 128, 18 / 19 for large products of 17 to 32 rows / columns, 16 for at
+ * most 64 rows, 17 for at most 64 columns, 14 under 256 rows or for
+ * products more than twice as wide as tall, else 15); 1..11 = a fixed
  * configuration of the 128 x 128 output tile (K slice 16 or 32, 3 or 4
  * pipeline stages, a dedicated TMA warp or TMA issued by a compute thread,
  * one or two CTAs per SM, packed or scalar FMAs); 12 = 64 x 256,
