@@ -359,7 +359,8 @@ def test_host_buffer_entry_point(sg, handle):
     (4099, 515, 257, 0.5, 0.25),     # four row chunks of unequal height
     (2047, 1029, 130, 1.0, 0.0),     # one chunk; C starts as NaN and is never read
     (3072, 96, 1000, -2.0, 1.0),     # three chunks
-    (2500, 2100, 300, 0.5, -0.75),   # first row block cut into two column halves
+    (2500, 2100, 300, 0.5, -0.75),   # first row block cut into two column pieces
+    (2100, 4500, 100, 1.0, 0.5),     # four column pieces, cuts off the 1125-column grid
 ])
 def test_host_entry_point_chunked_copies(sg, M, N, K, alpha, beta, math):
     h = sg.Handle()
