@@ -42,7 +42,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 19;
+constexpr int kNumAlgos = 21;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -62,6 +62,8 @@ void fill_algo16(KernelEntry *v);
 void fill_algo17(KernelEntry *v);
 void fill_algo18(KernelEntry *v);
 void fill_algo19(KernelEntry *v);
+void fill_algo20(KernelEntry *v);
+void fill_algo21(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {

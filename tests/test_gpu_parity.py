@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 20)))
+@pytest.mark.parametrize("algo", list(range(1, 22)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
@@ -482,3 +482,15 @@ def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
     small = min(M, N)
     want = (64, 512) if small > 32 else (32, 1024)
     assert plan["kind"] == 1 and (plan["tile_m"], plan["tile_n"]) == (want if M <= N else want[::-1])
+
+
+@pytest.mark.parametrize("K", [1, 5, 8, 16, 24, 40, 48, 56])
+def test_short_k_takes_shallow_slices(sg, handle, K):
+    # K <= 64 and not a multiple of 32: 16- or 8-deep K slices.
+    M, N = 1000, 1100
+    p = inputs.make_problem(M, N, K, seed=K + 7, kind="integer", alpha=0.5, beta=0.25)
+    np.testing.assert_array_equal(_gpu(sg, handle, p)[:, :N].astype(np.float64), _ref(p))
+    q = inputs.make_problem(M, N, K, seed=K + 8, alpha=-1.0, beta=0.0)
+    _assert_close(_gpu(sg, handle, q)[:, :N], _ref(q))
+    plan = handle.plan(_to_dev(q.A)[:, :K], _to_dev(q.B)[:, :N], torch.empty((M, N), device="cuda"))
+    assert plan["tile_k"] == (16 if (K % 16 == 0 or K > 32) else 8)
