@@ -17,6 +17,7 @@ struct KernelEntry {
     int threads;
     int smem;
     int bm, bn, bk, stages;
+    int c_box_rows, c_box_cols;   // > 0: beta == 0 vector variant stores C by TMA, boxes of this size
     int occupancy[kMaxDevices];   // CTAs per SM, 0 = not yet queried
 };
 
@@ -31,6 +32,10 @@ KernelEntry make_entry() {
     e.bn = Cfg::BN;
     e.bk = Cfg::BK;
     e.stages = Cfg::STAGES;
+    if (Cfg::STORE_TMA && BZ && CV) {
+        e.c_box_rows = Cfg::WTM;
+        e.c_box_cols = Cfg::C_BOX_COLS;
+    }
     return e;
 }
 
@@ -42,7 +47,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 21;
+constexpr int kNumAlgos = 26;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -64,6 +69,11 @@ void fill_algo18(KernelEntry *v);
 void fill_algo19(KernelEntry *v);
 void fill_algo20(KernelEntry *v);
 void fill_algo21(KernelEntry *v);
+void fill_algo22(KernelEntry *v);
+void fill_algo23(KernelEntry *v);
+void fill_algo24(KernelEntry *v);
+void fill_algo25(KernelEntry *v);
+void fill_algo26(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {

@@ -14,7 +14,10 @@
 //     8 values of A and 16 values of B with packed two-wide FP32 FMAs
 //     (fma.rn.f32x2: each lane issues one instruction per two products).
 //   * epilogue straight from registers: alpha*acc (+ beta*C, and C is not
-//     read when beta == 0), 16-byte stores when C's alignment allows.
+//     read when beta == 0), 16-byte stores when C's alignment allows; or, in
+//     the configurations for short K, each warp writes its alpha*acc block
+//     to its own shared-memory staging area and one lane hands it to TMA
+//     tile stores, so that C drains to memory while the next tile computes.
 //
 // What the pages contribute, and what changed for this chip:
 //   * the per-thread outer-product register tile and the K loop over staged
@@ -84,10 +87,16 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 //   consumer warp issues the loads (no extra warp);
 //   PIPE: 1 = fragments of the next k are read while this k's FMAs run
 //   (explicit register double buffering), 0 = left to the compiler;
-//   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2).
+//   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2);
+//   STORE_TMA: 1 = beta == 0 tiles leave through a per-warp shared-memory
+//   staging area and TMA tile stores (64 x 16 boxes) instead of st.global;
+//   REFILL_LAG (inline producer): after consuming slice g, thread 0 refills
+//   the stage of slice g - REFILL_LAG.  1 never waits for a slower warp; 0
+//   waits for all warps to release slice g but keeps STAGES - 1 slices in
+//   flight instead of STAGES - 2 (what a 2-stage ring needs).
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_,
           int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4, int PRODUCER_WARP_ = 1,
-          int PIPE_ = 0, int SCALAR_FMA_ = 0>
+          int PIPE_ = 0, int SCALAR_FMA_ = 0, int STORE_TMA_ = 0, int REFILL_LAG_ = 1>
 struct FfmaConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -100,6 +109,8 @@ struct FfmaConfig {
     static constexpr bool PRODUCER_WARP = PRODUCER_WARP_ != 0;
     static constexpr bool PIPE = PIPE_ != 0;
     static constexpr bool SCALAR_FMA = SCALAR_FMA_ != 0;   // fmaf instead of packed fma.rn.f32x2
+    static constexpr bool STORE_TMA = STORE_TMA_ != 0;
+    static constexpr int REFILL_LAG = REFILL_LAG_;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     static constexpr int THREADS = (CONSUMER_WARPS + (PRODUCER_WARP ? 1 : 0)) * 32;
     static constexpr int ROW_BYTES_A = BK * 4;                 // one row of the A slice
@@ -108,7 +119,11 @@ struct FfmaConfig {
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     // TMA swizzle span equals the A row: 128 B (BK=32), 64 B (BK=16), 32 B (BK=8).
     static constexpr int SWZ_MASK = ROW_BYTES_A / 16 - 1;      // 7, 3, 1
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (2 * STAGES + 1) * 8 + 128 + 1024;
+    // C staging for TMA stores: one WTM x WTN block per consumer warp, kept
+    // as NJ boxes of WTM rows x 4*WC columns (box j = the lane columns of j).
+    static constexpr int C_BOX_COLS = 4 * WC, C_BOX_BYTES = WTM * C_BOX_COLS * 4;
+    static constexpr int STORE_BYTES = STORE_TMA ? CONSUMER_WARPS * WTM * WTN * 4 : 0;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STORE_BYTES + (2 * STAGES + 1) * 8 + 128 + 1024;
     static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
     // TMA boxes are at most 256 elements a side: wider tiles take several.
     // A's boxes stack rows (the stage layout is unchanged); B's boxes sit one
@@ -127,6 +142,11 @@ struct FfmaConfig {
     static_assert(NKQ % KQ_UNROLL == 0, "unroll must divide the slice");
     static_assert(!PIPE || KQ_UNROLL % 2 == 0, "pipelined fragments alternate two buffers");
     static_assert(STAGES >= 2, "ring depth");
+    static_assert(REFILL_LAG == 0 || REFILL_LAG == 1, "refill lag");
+    // Staging writes are conflict-free when the 8 lanes of a quarter warp
+    // cover two rows 64 bytes apart and four consecutive 16-byte chunks.
+    static_assert(!STORE_TMA || (WR == 8 && WC == 4), "TMA store staging layout");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // Tile t -> (batch b, tile row tm, tile column tn).  Inside a batch, tiles
@@ -290,12 +310,36 @@ __device__ __forceinline__ void drain_slices(int from, int to, uint64_t *full, u
         mbar_wait_bounded(&full[g % Cfg::STAGES], (uint32_t)(g / Cfg::STAGES) & 1u, timeout_ns);
 }
 
+// TMA tile store of a shared-memory box to C (3-D map {N, M, batch});
+// elements outside the map's extent are not written.  The stores of one
+// thread form bulk groups: commit after issuing, wait before the source is
+// reused (".read": the box has been read out of shared memory) or before
+// the CTA exits (all writes done).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src,
+                                             int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 :: "l"(map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory, made visible to the TMA engine.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <class Cfg, bool BETA_ZERO, bool C_VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
 sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC,
                       const GemmArgs p)
 {
+    // tmC is read only by configurations with STORE_TMA, for beta == 0 and
+    // a 16-byte aligned C (the host encodes it then; otherwise it is unused).
+    constexpr bool TMA_EPILOGUE = Cfg::STORE_TMA && BETA_ZERO && C_VEC;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN, WR = Cfg::WR, WC = Cfg::WC;
     constexpr int NJ = TN / 4;   // 16-byte column groups per lane
@@ -311,7 +355,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     unsigned char *smem = smem_raw + pad;
     unsigned char *sA = smem;
     unsigned char *sB = smem + STAGES * Cfg::A_STAGE_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    unsigned char *sC = smem + STAGES * Cfg::STAGE_BYTES;   // STORE_BYTES of C staging
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::STORE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *cta_bar = empty + STAGES;   // consumer-warp rendezvous (stream-K fixup)
     SliceCursor *cursor = reinterpret_cast<SliceCursor *>(cta_bar + 1);
@@ -351,11 +396,13 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---------------- consumers ----------------
     // Inline producer: thread 0 issues the first STAGES slices up front, then
     // after consuming slice g (g >= 1) refills the stage of slice g - 1, which
-    // every warp has released by the time thread 0 is done with slice g.
+    // every warp has released by the time thread 0 is done with slice g (with
+    // REFILL_LAG 0: the stage of slice g itself, once every warp released it).
     const bool producer = !Cfg::PRODUCER_WARP && threadIdx.x == 0;
     if (producer) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if constexpr (TMA_EPILOGUE) prefetch_tensormap(&tmC);
         cursor_begin(cursor, p);
         while (cursor_valid(cursor) && cursor_issued(cursor) < STAGES)
             issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty);   // fresh stages: never waits
@@ -467,6 +514,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
                 record_error(p.err, kSiteConsumerFull);
                 if (producer) drain_slices<Cfg>(g, cursor_issued(cursor), full, p.timeout_ns);
+                if constexpr (TMA_EPILOGUE) { if (lane == 0) bulk_wait_all(); }
                 return;
             }
             const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
@@ -518,10 +566,11 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            if (producer && g >= 1 && cursor_valid(cursor)) {
+            if (producer && g >= Cfg::REFILL_LAG && cursor_valid(cursor)) {
                 if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
                     drain_slices<Cfg>(g + 1, cursor_issued(cursor), full, p.timeout_ns);
+                    if constexpr (TMA_EPILOGUE) bulk_wait_all();
                     return;
                 }
             }
@@ -578,59 +627,99 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         // ---------------- epilogue ----------------
         const float alpha = p.alpha;
         const float beta = p.beta;
+        if constexpr (TMA_EPILOGUE) {
+            // The warp's WTM x WTN block goes to its staging area as NJ boxes
+            // of WTM rows x 16 columns (row pitch 64 bytes), then lane 0
+            // issues one TMA store per box.  Lane (lr, lc) writes row
+            // lr + 8i, chunk lc of box j: a quarter warp covers two rows and
+            // four chunks, eight distinct bank groups.  Before overwriting,
+            // lane 0 waits until its previous tile's boxes have been read.
+            unsigned char *stg = sC + warp * (Cfg::WTM * Cfg::WTN * 4);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int row = tm * BM + row0 + WR * i;
-            if (row >= p.M) continue;
-            float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
-            if constexpr (BETA_ZERO) {
-                // C is only written: alpha * acc, 16 bytes at a time when allowed.
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
-                    const int col = tn * BN + col0 + 4 * WC * j;
-                    float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
-                    if (C_VEC && col + 3 < p.N) {
-                        *reinterpret_cast<float4 *>(crow + col) =
-                            make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (col + q < p.N) crow[col + q] = alpha * v[q];
-                    }
+                    const int cw = lc * 4 + 4 * WC * j;   // column inside the warp tile
+                    *reinterpret_cast<float4 *>(stg + (cw / Cfg::C_BOX_COLS) * Cfg::C_BOX_BYTES +
+                                                (lr + WR * i) * (Cfg::C_BOX_COLS * 4) + (cw % Cfg::C_BOX_COLS) * 4) =
+                        make_float4(alpha * acc[i][2 * j].x, alpha * acc[i][2 * j].y,
+                                    alpha * acc[i][2 * j + 1].x, alpha * acc[i][2 * j + 1].y);
                 }
-            } else {
-                // Reading C: all of this row's loads are issued before its
-                // stores, so that their latencies overlap (a store followed
-                // by the next load of the same thread would serialise them).
-                float cin[NJ][4];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // Boxes that start past the last row or column hold nothing
+                // of C and are not issued; the others are clipped by TMA.
+                const int y = tm * BM + wm * Cfg::WTM;
+                const int x = tn * BN + wn * Cfg::WTN;
+                if (y < p.M) {
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const int col = tn * BN + col0 + 4 * WC * j;
-                    if (C_VEC && col + 3 < p.N) {
-                        const float4 c = *reinterpret_cast<const float4 *>(crow + col);
-                        cin[j][0] = c.x; cin[j][1] = c.y; cin[j][2] = c.z; cin[j][3] = c.w;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) cin[j][q] = col + q < p.N ? crow[col + q] : 0.f;
-                    }
+                    for (int j = 0; j < Cfg::WTN / Cfg::C_BOX_COLS; ++j)
+                        if (x + j * Cfg::C_BOX_COLS < p.N)
+                            tma_store_3d(&tmC, stg + j * Cfg::C_BOX_BYTES, x + j * Cfg::C_BOX_COLS, y, bt);
                 }
+                bulk_commit();
+            }
+        } else {
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const int col = tn * BN + col0 + 4 * WC * j;
-                    float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+            for (int i = 0; i < TM; ++i) {
+                const int row = tm * BM + row0 + WR * i;
+                if (row >= p.M) continue;
+                float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
+                if constexpr (BETA_ZERO) {
+                    // C is only written: alpha * acc, 16 bytes at a time when allowed.
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = fmaf(beta, cin[j][q], alpha * v[q]);
-                    if (C_VEC && col + 3 < p.N) {
-                        *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
-                    } else {
+                    for (int j = 0; j < NJ; ++j) {
+                        const int col = tn * BN + col0 + 4 * WC * j;
+                        float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+                        if (C_VEC && col + 3 < p.N) {
+                            *reinterpret_cast<float4 *>(crow + col) =
+                                make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+                        } else {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (col + q < p.N) crow[col + q] = v[q];
+                            for (int q = 0; q < 4; ++q)
+                                if (col + q < p.N) crow[col + q] = alpha * v[q];
+                        }
+                    }
+                } else {
+                    // Reading C: all of this row's loads are issued before its
+                    // stores, so that their latencies overlap (a store followed
+                    // by the next load of the same thread would serialise them).
+                    float cin[NJ][4];
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        const int col = tn * BN + col0 + 4 * WC * j;
+                        if (C_VEC && col + 3 < p.N) {
+                            const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+                            cin[j][0] = c.x; cin[j][1] = c.y; cin[j][2] = c.z; cin[j][3] = c.w;
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) cin[j][q] = col + q < p.N ? crow[col + q] : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) {
+                        const int col = tn * BN + col0 + 4 * WC * j;
+                        float v[4] = {acc[i][2 * j].x, acc[i][2 * j].y, acc[i][2 * j + 1].x, acc[i][2 * j + 1].y};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) v[q] = fmaf(beta, cin[j][q], alpha * v[q]);
+                        if (C_VEC && col + 3 < p.N) {
+                            *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (col + q < p.N) crow[col + q] = v[q];
+                        }
                     }
                 }
             }
         }
         it.advance(p, seg);
+    }
+    if constexpr (TMA_EPILOGUE) {
+        if (lane == 0) bulk_wait_all();
     }
 }
 

@@ -254,20 +254,26 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * Pin the main kernel's tile configuration for calls on this handle:
  * 0 = automatic choice by shape (default: 10 when both sides are at most
  * 128, 18 / 19 for large products of 17 to 32 rows / columns, 16 for at
- * most 64 rows, 17 for at most 64 columns, 14 under 256 rows or for
- * products more than twice as wide as tall, 20 / 21 for K of at most 64
- * that is not a multiple of 32, else 15); 1..11 = a fixed
+ * most 64 rows, 17 for at most 64 columns; then, when beta == 0 and C is
+ * 16-byte aligned, 26 under 256 rows or for products more than twice as
+ * wide as tall, 23 / 24 for K of at most 64 that is a multiple of 16 / not
+ * a multiple of 16 (multiples of 32 excepted), else 22; otherwise 14 under
+ * 256 rows or for wide products, 20 / 21 for K of at most 64 that is not a
+ * multiple of 32, else 15); 1..11 = a fixed
  * configuration of the 128 x 128 output tile (K slice 16 or 32, 3 or 4
  * pipeline stages, a dedicated TMA warp or TMA issued by a compute thread,
  * one or two CTAs per SM, packed or scalar FMAs); 12 = 64 x 256,
  * 13 = 256 x 64 (four warps, two CTAs per SM); 14 = 128 x 256,
  * 15 = 256 x 128, 16 = 64 x 512, 17 = 512 x 64, 18 = 32 x 1024,
  * 19 = 1024 x 32, 20 / 21 = 256 x 128 with K slices of 16 / 8 and
- * 6 / 8 stages (eight warps, one CTA per SM) (see
- * fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1 (3xTF32)
- * the values 1..3 pick the tensor-core tile instead: 128 x 128, 128 x 192
- * or 128 x 256.  Every configuration computes the same result up to
- * summation order.
+ * 6 / 8 stages (eight warps, one CTA per SM); 22 = 256 x 128 and
+ * 26 = 128 x 256 with 2 stages, 23 / 25 = 256 x 128 with K slices of 16
+ * and 4 stages, 24 = 256 x 128 with K slices of 8 and 8 stages, all five
+ * storing C through shared memory and TMA when beta == 0 and C is 16-byte
+ * aligned (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1
+ * (3xTF32) the values 1..3 pick the tensor-core tile instead: 128 x 128,
+ * 128 x 192 or 128 x 256.  Every configuration computes the same result up
+ * to summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
 

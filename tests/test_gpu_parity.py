@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 22)))
+@pytest.mark.parametrize("algo", list(range(1, 27)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
@@ -486,11 +486,74 @@ def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
 
 @pytest.mark.parametrize("K", [1, 5, 8, 16, 24, 40, 48, 56])
 def test_short_k_takes_shallow_slices(sg, handle, K):
-    # K <= 64 and not a multiple of 32: 16- or 8-deep K slices.
+    # K <= 64 and not a multiple of 32: 16- or 8-deep K slices; beta == 0
+    # with an aligned C also goes through the TMA-store configurations.
     M, N = 1000, 1100
     p = inputs.make_problem(M, N, K, seed=K + 7, kind="integer", alpha=0.5, beta=0.25)
     np.testing.assert_array_equal(_gpu(sg, handle, p)[:, :N].astype(np.float64), _ref(p))
     q = inputs.make_problem(M, N, K, seed=K + 8, alpha=-1.0, beta=0.0)
     _assert_close(_gpu(sg, handle, q)[:, :N], _ref(q))
-    plan = handle.plan(_to_dev(q.A)[:, :K], _to_dev(q.B)[:, :N], torch.empty((M, N), device="cuda"))
-    assert plan["tile_k"] == (16 if (K % 16 == 0 or K > 32) else 8)
+    A, B, C = _to_dev(q.A)[:, :K], _to_dev(q.B)[:, :N], torch.empty((M, N), device="cuda")
+    # beta == 0, aligned C (TMA-stored tiles): the slice depth that divides K.
+    assert handle.plan(A, B, C)["tile_k"] == (16 if K % 16 == 0 else 8)
+    # C read: 16-deep slices from K = 33 on as well (no TMA store).
+    assert handle.plan(A, B, C, 1.0, 0.5)["tile_k"] == (16 if (K % 16 == 0 or K > 32) else 8)
+
+
+@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26])
+@pytest.mark.parametrize("M,N,K,ldc,schedule", [(1024, 1024, 1024, 1024, 0), (300, 520, 263, 520, 0),
+                                                (257, 1000, 40, 1012, 0), (70, 36, 8, 40, 0),
+                                                (1500, 704, 2000, 708, 2)])
+def test_tma_store_epilogue(sg, handle, algo, M, N, K, ldc, schedule):
+    # Configurations 22-26 with beta == 0 and a 16-byte aligned C: each warp
+    # stages its block in shared memory and TMA stores it, clipped at M and
+    # N.  C starts as NaN canaries (never read); the ldc padding and the rows
+    # around C must keep them.  Schedule 2 cuts tiles between CTAs (stream-K),
+    # so finished tiles also leave through the staging area after the fixup.
+    canary = np.frombuffer(np.uint32(0x7FC0BEEF).tobytes() * ((M + 8) * ldc),
+                           dtype=np.float32).reshape(M + 8, ldc).copy()
+    for kind, alpha in (("uniform", -0.75), ("integer", 0.5)):
+        p = inputs.make_problem(M, N, K, seed=M + N + K + algo, kind=kind, alpha=alpha, beta=0.0)
+        buf = _to_dev(canary)
+        C = buf[4:4 + M, :N]
+        A, B = _to_dev(p.A)[:, :K], _to_dev(p.B)[:, :N]
+        handle.set_algo(algo)
+        handle.set_schedule(schedule)
+        plan = handle.plan(A, B, C, alpha, 0.0)
+        handle.gemm(A, B, C, alpha, 0.0)
+        torch.cuda.synchronize()
+        handle.set_schedule(0)
+        handle.set_algo(0)
+        assert handle.device_error() == 0
+        assert plan["vector_epilogue"] == 1 and plan["tile_k"] == {22: 32, 23: 16, 24: 8, 25: 16, 26: 32}[algo]
+        out = buf.cpu().numpy()
+        mask = np.ones(out.shape, bool)
+        mask[4:4 + M, :N] = False
+        assert (out.view(np.uint32)[mask] == 0x7FC0BEEF).all()
+        if kind == "integer":
+            np.testing.assert_array_equal(out[4:4 + M, :N].astype(np.float64), _ref(p))
+        else:
+            _assert_close(out[4:4 + M, :N], _ref(p))
+
+
+def test_tma_store_epilogue_batched(sg, handle):
+    # Strided batches through configuration 24: the store map's third
+    # dimension walks the batch stride (a multiple of 4 elements).
+    M, N, K, batch, ldc = 200, 136, 8, 3, 140
+    sc = M * ldc + 12
+    p = [inputs.make_problem(M, N, K, seed=90 + z, kind="integer", alpha=2.0, beta=0.0) for z in range(batch)]
+    A = torch.stack([_to_dev(q.A)[:, :K] for q in p])
+    B = torch.stack([_to_dev(q.B)[:, :N] for q in p])
+    flat = torch.full((batch * sc + 8,), float("nan"), device="cuda")
+    C = torch.as_strided(flat, (batch, M, N), (sc, ldc, 1))
+    handle.set_algo(24)
+    handle.gemm_batched(A, B, C, 2.0, 0.0)
+    torch.cuda.synchronize()
+    handle.set_algo(0)
+    assert handle.device_error() == 0
+    got = C.cpu().numpy()
+    for z in range(batch):
+        np.testing.assert_array_equal(got[z].astype(np.float64), _ref(p[z]))
+    pad = torch.as_strided(flat, (batch, M, ldc - N), (sc, ldc, 1), N)
+    assert torch.isnan(pad).all()
+
