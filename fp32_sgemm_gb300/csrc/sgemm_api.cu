@@ -235,6 +235,23 @@ bool thin_ffma_preferred(const sgemmContext *h, const Problem &q) {
     return ceil_div(big, 1024) * ceil_div(q.K, 16) >= 8 * int64_t(h->sm_count);
 }
 
+// Small products take the 32 x 32 block kernel (one CTA per block, no
+// persistent grid, no TMA, no stream-K exchange): at most kSmallMaxDim rows
+// and columns per matrix, and little work in the whole call, where the tile
+// kernel is bound by its start-up latency and leaves most SMs idle.  Only
+// in the automatic FFMA setting (a pinned tile configuration or schedule, or
+// math mode 1, keeps the kernel asked for).
+constexpr int64_t kSmallMaxDim = 512;
+constexpr int64_t kSmallMaxWork = int64_t(1) << 27;   // batch x M x N x K multiply-adds
+constexpr int64_t kSmallMaxK = 2048;
+
+bool small_preferred(const sgemmContext *h, const Problem &q) {
+    if (h->algo != 0 || h->schedule != 0 || h->math != 0) return false;
+    if (q.M > kSmallMaxDim || q.N > kSmallMaxDim || q.K > kSmallMaxK) return false;
+    if (q.batch * q.M * q.N * q.K > kSmallMaxWork) return false;
+    return sg::small_blocks(int(q.M), int(q.N), int(q.batch)) > 0;
+}
+
 // Tile configuration by shape.  Products with at most 64 rows (columns)
 // take the 64 x 512 (512 x 64) tile, which computes no padding rows
 // (columns) beyond 64.  Everything else takes 256 x 128, or 128 x 256 when
@@ -458,6 +475,15 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
             return SGEMM_STATUS_SUCCESS;
         }
     }
+    if (small_preferred(h, q)) {
+        pl.pub.kind = 5;
+        pl.pub.launches = 1;
+        pl.pub.tile_m = pl.pub.tile_n = sg::kSmallTile;
+        pl.pub.tile_k = sg::kSmallPiece;
+        pl.pub.stages = 1;
+        pl.pub.ctas = sg::small_blocks(int(q.M), int(q.N), int(q.batch));
+        return SGEMM_STATUS_SUCCESS;
+    }
     if (h->math == 1) return make_plan_tf32x3(h, q, pl);
     pl.pub.kind = 1;
     // A as TMA reads it: [batch][M][K] rows of K.
@@ -657,6 +683,30 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
         return last_launch();
     }
     if (pl.pub.kind == 3) return run_tf32x3(h, pl, q, stream);
+    if (pl.pub.kind == 5) {
+        sg::SmallArgs a{};
+        a.M = int(q.M);
+        a.N = int(q.N);
+        a.K = int(q.K);
+        a.alpha = q.alpha;
+        a.beta = q.beta;
+        a.A = q.A;
+        a.lda = q.lda;
+        a.sa = q.sa;
+        a.B = q.B;
+        a.ldb = q.ldb;
+        a.sb = q.sb;
+        a.C = q.C;
+        a.ldc = q.ldc;
+        a.sc = q.sc;
+        if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        sg::launch_small(a, q.opA, q.opB, int(q.batch), stream);
+        if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
+        if (h->ev_stop != nullptr && cudaEventRecord(h->ev_stop, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
+        return SGEMM_STATUS_SUCCESS;
+    }
     if (pl.pub.kind == 4) {
         if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
             return SGEMM_STATUS_LAUNCH_FAILED;

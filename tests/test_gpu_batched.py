@@ -57,9 +57,14 @@ CASES = [
 ]
 
 
+# algo 0: the automatic choice (in FFMA mode the small-product kernel for
+# these sizes, which reads transposed operands in place); 15: the main
+# kernel's 256 x 128 tile pinned (transposed operands go through the
+# workspace).  In math mode 1 a value above 3 leaves the automatic choice.
+@pytest.mark.parametrize("algo", [0, 15])
 @pytest.mark.parametrize("opA,opB,M,N,K,batch,pad,odd", CASES)
 @pytest.mark.parametrize("kind", ["uniform", "integer"])
-def test_forms_and_batches(handle, opA, opB, M, N, K, batch, pad, odd, kind):
+def test_forms_and_batches(handle, opA, opB, M, N, K, batch, pad, odd, kind, algo):
     ar, ac = (K, M) if opA else (M, K)
     br, bc = (N, K) if opB else (K, N)
     lda, ldb, ldc = ac + pad, bc + pad, N + pad
@@ -73,7 +78,9 @@ def test_forms_and_batches(handle, opA, opB, M, N, K, batch, pad, odd, kind):
     B, Bh = _stored(br, bc, ldb, batch, sb, seed + 1, kind)
     C, C0 = _stored(M, N, ldc, batch, sc, seed + 2, kind)
     alpha, beta = 0.5, -1.25
+    handle.set_algo(algo)
     handle.gemm_batched(A, B, C, alpha, beta, trans_a=bool(opA), trans_b=bool(opB))
+    handle.set_algo(0)
     torch.cuda.synchronize()
     assert handle.device_error() == 0
     got = C.contiguous().cpu().numpy()

@@ -170,21 +170,25 @@ _SMALL = [1, 2, 3, 5, 8, 9]
 _EDGES = [15, 16, 17, 31, 32, 33, 127, 128, 129]
 
 
-def test_tiny_shapes_integer_exact(sg, handle):
+# algo 0: the automatic choice (the small-product kernel for most of these
+# shapes); 15: the 256 x 128 tile of the main kernel pinned.
+@pytest.mark.parametrize("algo", [0, 15])
+def test_tiny_shapes_integer_exact(sg, handle, algo):
     for M, N, K in itertools.product(_SMALL, _SMALL, _SMALL):
         p = inputs.make_problem(M, N, K, seed=M * 97 + N * 13 + K, kind="integer",
                                 alpha=1.0, beta=0.5, with_c=True,
                                 lda=K + (M % 3), ldb=N + (K % 2), ldc=N + 1)
-        got = _gpu(sg, handle, p)
+        got = _gpu(sg, handle, p, algo=algo)
         np.testing.assert_array_equal(got[:, :N].astype(np.float64), _ref(p),
                                       err_msg=f"shape {(M, N, K)}")
         assert np.isnan(got[:, N:]).all(), "ldc padding was written"
 
 
-def test_edge_shapes_uniform(sg, handle):
+@pytest.mark.parametrize("algo", [0, 15])
+def test_edge_shapes_uniform(sg, handle, algo):
     for M, N, K in itertools.product(_EDGES[::2], _EDGES[1::2], _EDGES):
         p = inputs.make_problem(M, N, K, seed=M + 7 * N + 11 * K, alpha=-1.25, beta=0.75)
-        _assert_close(_gpu(sg, handle, p)[:, :N], _ref(p))
+        _assert_close(_gpu(sg, handle, p, algo=algo)[:, :N], _ref(p))
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
@@ -193,19 +197,22 @@ def test_edge_shapes_uniform(sg, handle):
     (130, 126, 64, 68, 127, 129),         # A in place, B repacked, scalar C
     (129, 131, 513, 515, 132, 136),       # A repacked, B in place, vector C
 ])
-def test_leading_dimensions_and_packing(sg, handle, M, N, K, lda, ldb, ldc):
+@pytest.mark.parametrize("algo", [0, 15])
+def test_leading_dimensions_and_packing(sg, handle, M, N, K, lda, ldb, ldc, algo):
     p = inputs.make_problem(M, N, K, seed=M * N, alpha=1.5, beta=-0.5, lda=lda, ldb=ldb, ldc=ldc)
-    got = _gpu(sg, handle, p)
+    got = _gpu(sg, handle, p, algo=algo)
     _assert_close(got[:, :N], _ref(p))
     assert np.isnan(got[:, N:]).all()
     q = inputs.make_problem(M, N, K, seed=M * N + 1, kind="integer", alpha=1.5, beta=-0.5,
                             lda=lda, ldb=ldb, ldc=ldc)
-    np.testing.assert_array_equal(_gpu(sg, handle, q)[:, :N].astype(np.float64), _ref(q))
+    np.testing.assert_array_equal(_gpu(sg, handle, q, algo=algo)[:, :N].astype(np.float64), _ref(q))
 
 
-def test_unaligned_base_pointers(sg, handle):
+@pytest.mark.parametrize("algo", [0, 15])
+def test_unaligned_base_pointers(sg, handle, algo):
     # Views that start one float into their buffers: 4-byte but not 16-byte
-    # aligned, so A and B are repacked and C is written with scalar stores.
+    # aligned, so the tile kernel repacks A and B and writes C with scalar
+    # stores (the small-product kernel, algo 0, reads them in place).
     M, N, K = 200, 190, 170
     p = inputs.make_problem(M, N, K, seed=77, alpha=1.0, beta=1.0)
     Ab = torch.zeros(M * K + 1, device="cuda")
@@ -214,10 +221,14 @@ def test_unaligned_base_pointers(sg, handle):
     A = Ab[1:].view(M, K); A.copy_(torch.from_numpy(p.A))
     B = Bb[1:].view(K, N); B.copy_(torch.from_numpy(p.B))
     C = Cb[1:].view(M, N); C.copy_(torch.from_numpy(p.C0))
+    handle.set_algo(algo)
     plan = handle.plan(A, B, C, 1.0, 1.0)
-    assert plan["packs_a"] == 1 and plan["packs_b"] == 1 and plan["vector_epilogue"] == 0
-    handle.set_algo(0)
+    if algo:
+        assert plan["packs_a"] == 1 and plan["packs_b"] == 1 and plan["vector_epilogue"] == 0
+    else:
+        assert plan["kind"] == 5
     handle.gemm(A, B, C, 1.0, 1.0)
+    handle.set_algo(0)
     _assert_close(C.cpu().numpy(), _ref(p))
     assert float(Cb[0]) == 0.0
 
@@ -249,7 +260,8 @@ def test_empty_output_untouched(sg, handle):
     torch.cuda.synchronize()
 
 
-def test_guard_bands_untouched(sg, handle):
+@pytest.mark.parametrize("algo", [0, 15])
+def test_guard_bands_untouched(sg, handle, algo):
     # C lives inside a larger canary-filled buffer: rows above/below, columns
     # past N (ldc padding) must keep their exact bit patterns.
     M, N, K, ldc = 257, 250, 96, 260
@@ -259,8 +271,9 @@ def test_guard_bands_untouched(sg, handle):
     canary[4:4 + M, :N] = p.C0[:, :N]
     buf = _to_dev(canary)
     C = buf[4:4 + M, :N]
-    handle.set_algo(0)
+    handle.set_algo(algo)
     handle.gemm(_to_dev(p.A), _to_dev(p.B), C, 1.0, 0.5)
+    handle.set_algo(0)
     out = buf.cpu().numpy()
     mask = np.ones(out.shape, bool)
     mask[4:4 + M, :N] = False
@@ -319,6 +332,12 @@ def test_workspace_required_without_workspace(sg):
     A = torch.zeros(100 * 33, device="cuda")
     B = torch.zeros(33 * 64, device="cuda")
     C = torch.zeros(100 * 64, device="cuda")
+    # The automatic choice runs a product this small in the small-product
+    # kernel, which reads A in place and needs no workspace ...
+    assert lib.sgemmEx(h.ptr, 100, 64, 33, 1.0, A.data_ptr(), 33, B.data_ptr(), 64, 0.0,
+                       C.data_ptr(), 64, None) == 0
+    # ... the tile kernel must repack A (a pitch of 33 floats is not TMA-addressable).
+    h.set_algo(15)
     st = lib.sgemmEx(h.ptr, 100, 64, 33, 1.0, A.data_ptr(), 33, B.data_ptr(), 64, 0.0,
                      C.data_ptr(), 64, None)
     assert st == sg.Status.WORKSPACE_REQUIRED
