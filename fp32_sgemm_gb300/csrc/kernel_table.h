@@ -109,11 +109,12 @@ void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *
                    const float *B, int64_t ldb, float beta, float *C, int64_t ldc, float *part,
                    int splits, cudaStream_t s);
 
-// Small products (sgemm_small.cu): one CTA of 64 threads per 32 x 32 block
-// of each C matrix, plain loads, K in 32-deep pieces.  Operands may be
+// Small products (sgemm_small.cu): one CTA of 64 threads (or a cluster of
+// `splits` CTAs sharing K) per 32 x 32 block of each C matrix, plain loads,
+// K in 32-deep pieces.  Operands may be
 // stored transposed (trans_a: A stored K x M; trans_b: B stored N x K);
 // matrix z of an operand starts at base + z * stride.
-constexpr int kSmallTile = 32, kSmallPiece = 32;
+constexpr int kSmallTile = 32, kSmallPiece = 32, kSmallMaxSplits = 8;
 struct SmallArgs {
     int M, N, K;
     float alpha, beta;
@@ -123,9 +124,14 @@ struct SmallArgs {
     int64_t ldb, sb;
     float *C;
     int64_t ldc, sc;
+    int splits;             // CTAs per block of C (a cluster), 1..kSmallMaxSplits
+    int sms;                // SMs of the device
     int tiles_m, tiles_n;   // set by launch_small
 };
-int small_blocks(int M, int N, int batch);   // CTAs of one launch (0: too many)
+int small_blocks(int M, int N, int batch);   // blocks of C in one launch (0: too many)
+// K ranges per block: doubled while the pieces last and the launch stays
+// within 4 CTAs per SM.
+int small_splits(int M, int N, int K, int batch, int sms);
 void launch_small(SmallArgs p, int trans_a, int trans_b, int batch, cudaStream_t s);
 
 // TMA-fed skinny kernels (sgemm_skinny_tma.cu), for operands TMA reads in

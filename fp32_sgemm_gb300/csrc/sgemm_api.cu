@@ -213,6 +213,7 @@ struct Plan {
     size_t ws_skinny = 0;
     bool skinny_tma = false;        // TMA-fed skinny kernels (operands read in place)
     sg::SkinnyTmaGeom skinny_geom;
+    int small_splits = 1;           // small-product kernel (kind 5): CTAs per block of C
 };
 
 // Configuration 15 (256 x 128 tile, eight consumer warps, one CTA per SM,
@@ -235,21 +236,31 @@ bool thin_ffma_preferred(const sgemmContext *h, const Problem &q) {
     return ceil_div(big, 1024) * ceil_div(q.K, 16) >= 8 * int64_t(h->sm_count);
 }
 
-// Small products take the 32 x 32 block kernel (one CTA per block, no
-// persistent grid, no TMA, no stream-K exchange): at most kSmallMaxDim rows
-// and columns per matrix, and little work in the whole call, where the tile
-// kernel is bound by its start-up latency and leaves most SMs idle.  Only
-// in the automatic FFMA setting (a pinned tile configuration or schedule, or
-// math mode 1, keeps the kernel asked for).
-constexpr int64_t kSmallMaxDim = 512;
+// Small products take the 32 x 32 block kernel (one CTA, or a cluster of
+// CTAs sharing K, per block; no persistent grid, no TMA, no stream-K
+// exchange): matrices of at most kSmallMaxDim rows and columns, K at most
+// kSmallMaxK, and at most 2^27 multiply-adds in the call (2^28 while the
+// blocks fill at most two CTAs per SM; any number for matrices of at most
+// 64 x 64, e.g. 1000 x 64^3: 61.1 -> 28.2 us).  There the tile kernel is bound by
+// its start-up latency and leaves SMs idle; measured per call (CUDA graph
+// replay): 128^3 16.4 -> 4.6 us, 256^3 20.5 -> 5.4, 512^3 36.9 -> 19.6,
+// 128 x 128 x 8192 81.9 -> 41.7, 1000 x 64^3 61.3 -> 28.2; beyond, e.g.
+// 128 x 128^3 (2^28) 22.7 vs 27.4 us, the tile kernel wins.  Only in the
+// automatic FFMA setting (a pinned tile configuration or schedule, or math
+// mode 1, keeps the kernel asked for).
+constexpr int64_t kSmallMaxDim = 1024;
+constexpr int64_t kSmallMaxK = 8192;
 constexpr int64_t kSmallMaxWork = int64_t(1) << 27;   // batch x M x N x K multiply-adds
-constexpr int64_t kSmallMaxK = 2048;
 
 bool small_preferred(const sgemmContext *h, const Problem &q) {
     if (h->algo != 0 || h->schedule != 0 || h->math != 0) return false;
     if (q.M > kSmallMaxDim || q.N > kSmallMaxDim || q.K > kSmallMaxK) return false;
-    if (q.batch * q.M * q.N * q.K > kSmallMaxWork) return false;
-    return sg::small_blocks(int(q.M), int(q.N), int(q.batch)) > 0;
+    const int64_t blocks = sg::small_blocks(int(q.M), int(q.N), int(q.batch));
+    if (blocks == 0) return false;
+    // Matrices of at most 64 x 64 would leave 3/4 of a 128 x 128 tile idle.
+    if (q.M <= 64 && q.N <= 64) return true;
+    const int64_t work = q.batch * q.M * q.N * q.K;
+    return work <= kSmallMaxWork || (work <= 2 * kSmallMaxWork && blocks <= 2 * int64_t(h->sm_count));
 }
 
 // Tile configuration by shape.  Products with at most 64 rows (columns)
@@ -481,7 +492,8 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
         pl.pub.tile_m = pl.pub.tile_n = sg::kSmallTile;
         pl.pub.tile_k = sg::kSmallPiece;
         pl.pub.stages = 1;
-        pl.pub.ctas = sg::small_blocks(int(q.M), int(q.N), int(q.batch));
+        pl.small_splits = sg::small_splits(int(q.M), int(q.N), int(q.K), int(q.batch), h->sm_count);
+        pl.pub.ctas = sg::small_blocks(int(q.M), int(q.N), int(q.batch)) * pl.small_splits;
         return SGEMM_STATUS_SUCCESS;
     }
     if (h->math == 1) return make_plan_tf32x3(h, q, pl);
@@ -699,6 +711,8 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
         a.C = q.C;
         a.ldc = q.ldc;
         a.sc = q.sc;
+        a.splits = pl.small_splits;
+        a.sms = h->sm_count;
         if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
             return SGEMM_STATUS_LAUNCH_FAILED;
         sg::launch_small(a, q.opA, q.opB, int(q.batch), stream);

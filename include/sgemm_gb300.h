@@ -239,10 +239,12 @@ typedef struct sgemmPlan {
     int kind;           /* 0 none, 1 FFMA main kernel, 2 scale-only (K == 0 or alpha == 0),
                            3 3xTF32 tensor-core kernel (after the split pre-pass),
                            4 skinny streaming kernel + split reduction (M or N <= 32),
-                           5 small-product kernel: one CTA per 32 x 32 block of C, for
-                           matrices of at most 512 rows and columns and K <= 2048 with
-                           at most 2^27 multiply-adds in the call (FFMA, automatic
-                           tile choice only) */
+                           5 small-product kernel: one CTA (or a cluster of up to 8
+                           sharing K) per 32 x 32 block of C, for matrices of at most
+                           1024 rows and columns, K <= 8192 and at most 2^27
+                           multiply-adds in the call (2^28 while the blocks fill at
+                           most two CTAs per SM; any number for matrices of at most
+                           64 x 64; FFMA, automatic tile choice only) */
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
     int raster_group;   /* tile rows per band of the tile order (tiles running together
                            share rows of A and columns of B in L2); 0 if no tiles */

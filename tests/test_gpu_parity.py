@@ -483,8 +483,8 @@ def test_cuda_graph_capture_and_replay(sg, math):
         h.close()
 
 
-@pytest.mark.parametrize("M,N,K", [(33, 4000, 1500), (64, 2048, 777), (48, 300, 5000),
-                                   (4000, 40, 1500), (2500, 64, 999), (700, 33, 3000),
+@pytest.mark.parametrize("M,N,K", [(33, 4000, 1500), (64, 2048, 777), (48, 1300, 5000),
+                                   (4000, 40, 1500), (2500, 64, 999), (1100, 33, 3000),
                                    (24, 16384, 4096), (32, 10000, 2500), (16384, 20, 4096)])
 def test_medium_thin_products_take_the_narrow_tiles(sg, handle, M, N, K):
     # 33..64 rows (columns): the 64 x 512 (512 x 64) tile configuration;

@@ -1,5 +1,6 @@
-"""The small-product kernel (plan kind 5: one CTA per 32 x 32 block of C)
-against the fp64 oracle: ragged and tile-sized shapes, all four operand
+"""The small-product kernel (plan kind 5: one CTA, or a cluster of up to 8
+sharing K, per 32 x 32 block of C) against the fp64 oracle: ragged and
+tile-sized shapes, K split over clusters of 1, 2, 4 and 8, all four operand
 forms read in place, batches with padded and odd pitches and strides, beta
 semantics (C never read when beta == 0), the ldc padding, and the limits
 of the automatic choice.  Integer inputs must match bit for bit."""
@@ -117,12 +118,21 @@ def test_automatic_choice_limits(handle):
         if batch == 1:
             return handle.plan(A[0], B[0], C[0], **kw)
         return None
+    # 16 blocks of 32 x 32, each shared by a cluster of 4 CTAs (one 32-deep
+    # K piece each): as many K ranges as pieces, at most 8, at most 4 CTAs
+    # per SM.
     p = plan(128, 128, 128)
-    assert p["kind"] == 5 and (p["tile_m"], p["tile_n"], p["ctas"]) == (32, 32, 16)
-    assert plan(512, 512, 512)["kind"] == 5
-    assert plan(513, 512, 256)["kind"] == 1          # a side above 512
-    assert plan(256, 256, 4096)["kind"] == 1         # K above 2048
-    assert plan(512, 512, 1024)["kind"] == 1         # more than 2^27 multiply-adds
+    assert p["kind"] == 5 and (p["tile_m"], p["tile_n"], p["ctas"]) == (32, 32, 64)
+    assert plan(40, 40, 2048)["ctas"] == 4 * 8
+    assert plan(64, 96, 33)["ctas"] == 6 * 2
+    assert plan(512, 512, 512)["ctas"] == 256 * 2
+    assert plan(512, 512, 512)["kind"] == 5         # 2^27 multiply-adds
+    assert plan(1024, 1024, 128)["kind"] == 5
+    assert plan(256, 256, 4096)["kind"] == 5        # 2^28, 64 blocks
+    assert plan(1025, 512, 64)["kind"] == 1         # a side above 1024
+    assert plan(128, 128, 16384)["kind"] == 1       # K above 8192
+    assert plan(1024, 1024, 256)["kind"] == 1       # 2^28 in 1024 blocks
+    assert plan(1024, 1024, 512)["kind"] == 1       # 2^29
     handle.set_algo(10)                              # a pinned tile configuration
     assert plan(128, 128, 128)["kind"] == 1
     handle.set_algo(0)
