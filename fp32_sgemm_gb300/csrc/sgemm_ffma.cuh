@@ -340,6 +340,9 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     // tmC is read only by configurations with STORE_TMA, for beta == 0 and
     // a 16-byte aligned C (the host encodes it then; otherwise it is unused).
     constexpr bool TMA_EPILOGUE = Cfg::STORE_TMA && BETA_ZERO && C_VEC;
+    // Same configurations, C not 16-byte aligned: the block still goes
+    // through the staging area, then leaves in row runs (plain stores).
+    constexpr bool STAGED_EPILOGUE = Cfg::STORE_TMA && !C_VEC;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN, WR = Cfg::WR, WC = Cfg::WC;
     constexpr int NJ = TN / 4;   // 16-byte column groups per lane
@@ -627,16 +630,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         // ---------------- epilogue ----------------
         const float alpha = p.alpha;
         const float beta = p.beta;
-        if constexpr (TMA_EPILOGUE) {
-            // The warp's WTM x WTN block goes to its staging area as NJ boxes
-            // of WTM rows x 16 columns (row pitch 64 bytes), then lane 0
-            // issues one TMA store per box.  Lane (lr, lc) writes row
-            // lr + 8i, chunk lc of box j: a quarter warp covers two rows and
-            // four chunks, eight distinct bank groups.  Before overwriting,
-            // lane 0 waits until its previous tile's boxes have been read.
-            unsigned char *stg = sC + warp * (Cfg::WTM * Cfg::WTN * 4);
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+        // The warp's WTM x WTN block (alpha * acc) into its staging area as
+        // NJ boxes of WTM rows x 16 columns (row pitch 64 bytes).  Lane
+        // (lr, lc) writes row lr + 8i, chunk lc of box j: a quarter warp
+        // covers two rows and four chunks, eight distinct bank groups.
+        unsigned char *stg = sC + warp * (Cfg::WTM * Cfg::WTN * 4);
+        auto stage_block = [&]() {
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -647,6 +646,13 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                         make_float4(alpha * acc[i][2 * j].x, alpha * acc[i][2 * j].y,
                                     alpha * acc[i][2 * j + 1].x, alpha * acc[i][2 * j + 1].y);
                 }
+        };
+        if constexpr (TMA_EPILOGUE) {
+            // Lane 0 then issues one TMA store per box.  Before overwriting,
+            // lane 0 waits until its previous tile's boxes have been read.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            stage_block();
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -662,6 +668,46 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
                 bulk_commit();
             }
+        } else if constexpr (STAGED_EPILOGUE) {
+            // C not 16-byte aligned: after staging, each instruction covers
+            // two rows x 16 columns (lanes 0-15 a run of one row, 16-31 the
+            // next; conflict-free reads of one box), so a warp touches
+            // 64-byte runs of C instead of 16-byte pieces of eight rows.
+            // With beta != 0 the C values of eight instructions are loaded
+            // before any is used.
+            __syncwarp();
+            stage_block();
+            __syncwarp();
+            const float *stf = reinterpret_cast<const float *>(stg);
+            const int half = lane >> 4, c16 = lane & 15;
+            const int row_w = tm * BM + wm * Cfg::WTM;
+            const int col_w = tn * BN + wn * Cfg::WTN;
+            float *cb = p.C + (int64_t)bt * p.stride_c;
+#pragma unroll 1
+            for (int j = 0; j < Cfg::WTN / Cfg::C_BOX_COLS; ++j) {
+                const int col = col_w + Cfg::C_BOX_COLS * j + c16;
+                const bool col_ok = col < p.N;
+#pragma unroll 1
+                for (int rp0 = 0; rp0 < Cfg::WTM / 2; rp0 += 8) {
+                    float cin[8];
+                    if constexpr (!BETA_ZERO) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int row = row_w + 2 * (rp0 + u) + half;
+                            cin[u] = (col_ok && row < p.M) ? cb[(int64_t)row * p.ldc + col] : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int r = 2 * (rp0 + u) + half;
+                        const int row = row_w + r;
+                        float v = stf[j * (Cfg::C_BOX_BYTES / 4) + r * Cfg::C_BOX_COLS + c16];
+                        if constexpr (!BETA_ZERO) v = fmaf(beta, cin[u], v);
+                        if (col_ok && row < p.M) cb[(int64_t)row * p.ldc + col] = v;
+                    }
+                }
+            }
+            __syncwarp();   // the staging area is read before the next tile refills it
         } else {
 #pragma unroll
             for (int i = 0; i < TM; ++i) {
