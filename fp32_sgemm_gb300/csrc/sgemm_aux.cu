@@ -24,16 +24,31 @@ __global__ void sgemm_scale_c_kernel(int M, int N, float beta, float *C, int64_t
 }
 
 // Copy rows x cols row-major matrices into buffers with row pitch ld_dst (a
-// multiple of 4 floats), so that TMA can address them.
-__global__ void sgemm_pack_rows_kernel(const float *src, int64_t ld_src, int64_t s_src, float *dst,
-                                       int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch) {
-    for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
-        for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-            const float *sr = src + z * s_src + r * ld_src;
-            float *d = dst + z * s_dst + r * ld_dst;
-            for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x)
-                d[c] = sr[c];
-        }
+// multiple of 4 floats, 16-byte aligned rows), so that TMA can address them.
+// A thread moves 4 consecutive elements of a row per step: four 4-byte
+// loads (the source pitch may be odd) and one 16-byte store; the padding
+// columns up to the next multiple of 4 are written as zeros.  One flat
+// grid-stride loop over (matrix, row, 4-column group) keeps every CTA busy
+// whatever the shape (a CTA per row left most of a short row's CTA idle).
+__global__ void __launch_bounds__(256)
+sgemm_pack_rows_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
+                       float *__restrict__ dst, int64_t ld_dst, int64_t s_dst, int rows, int cols,
+                       int batch) {
+    const int64_t groups = (cols + 3) / 4;
+    const int64_t units = (int64_t)batch * rows * groups;
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t zr = u / groups;
+        const int c = (int)(u - zr * groups) * 4;
+        const int64_t z = zr / rows, r = zr - z * rows;
+        const float *sr = src + z * s_src + r * ld_src + c;
+        float4 v;
+        v.x = sr[0];
+        v.y = c + 1 < cols ? sr[1] : 0.f;
+        v.z = c + 2 < cols ? sr[2] : 0.f;
+        v.w = c + 3 < cols ? sr[3] : 0.f;
+        *reinterpret_cast<float4 *>(dst + z * s_dst + r * ld_dst + c) = v;
+    }
 }
 
 // Transpose rows x cols matrices src[r][c] -> dst[c][r] through 64 x 64
@@ -202,8 +217,9 @@ void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t str
 
 void launch_pack_rows(const float *src, int64_t ld_src, int64_t s_src, float *dst, int64_t ld_dst,
                       int64_t s_dst, int rows, int cols, int batch, cudaStream_t s) {
-    dim3 grid(unsigned(std::min<int64_t>(cdiv(cols, 256), 8)), unsigned(std::min<int64_t>(rows, 65535)), zdim(batch));
-    sgemm_pack_rows_kernel<<<grid, 256, 0, s>>>(src, ld_src, s_src, dst, ld_dst, s_dst, rows, cols, batch);
+    const int64_t units = int64_t(batch) * rows * cdiv(cols, 4);
+    const unsigned blocks = unsigned(std::max<int64_t>(1, std::min<int64_t>(cdiv(units, 256), 4096)));
+    sgemm_pack_rows_kernel<<<blocks, 256, 0, s>>>(src, ld_src, s_src, dst, ld_dst, s_dst, rows, cols, batch);
 }
 
 void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
