@@ -634,17 +634,22 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         // NJ boxes of WTM rows x 16 columns (row pitch 64 bytes).  Lane
         // (lr, lc) writes row lr + 8i, chunk lc of box j: a quarter warp
         // covers two rows and four chunks, eight distinct bank groups.
+        // alpha * acc is formed with packed multiplies (one instruction per
+        // two products; with short K the scaling is a noticeable share of the
+        // FMA pipe's work on a tile).
         unsigned char *stg = sC + warp * (Cfg::WTM * Cfg::WTN * 4);
         auto stage_block = [&]() {
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     const int cw = lc * 4 + 4 * WC * j;   // column inside the warp tile
+                    const float2 v0 = __fmul2_rn(a2, acc[i][2 * j]);
+                    const float2 v1 = __fmul2_rn(a2, acc[i][2 * j + 1]);
                     *reinterpret_cast<float4 *>(stg + (cw / Cfg::C_BOX_COLS) * Cfg::C_BOX_BYTES +
                                                 (lr + WR * i) * (Cfg::C_BOX_COLS * 4) + (cw % Cfg::C_BOX_COLS) * 4) =
-                        make_float4(alpha * acc[i][2 * j].x, alpha * acc[i][2 * j].y,
-                                    alpha * acc[i][2 * j + 1].x, alpha * acc[i][2 * j + 1].y);
+                        make_float4(v0.x, v0.y, v1.x, v1.y);
                 }
         };
         if constexpr (TMA_EPILOGUE) {
