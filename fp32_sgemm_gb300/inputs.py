@@ -173,6 +173,9 @@ EXTRA_WORKLOADS = {
     "skinny_m1": Workload("skinny_m1", 1, 16384, 16384, 1.0, 0.0, 11, True),
     "skinny_m8": Workload("skinny_m8", 8, 16384, 16384, 1.0, 0.0, 12, True),
     "skinny_n8": Workload("skinny_n8", 16384, 8, 16384, 1.0, 0.0, 13, True),
+    # Short K at large M and N: writing C (1 GiB) bounds these.
+    "shortk_k8": Workload("shortk_k8", 16384, 16384, 8, 1.0, 0.0, 14, False),
+    "shortk_k16": Workload("shortk_k16", 16384, 16384, 16, 1.0, 0.0, 15, False),
 }
 
 def pattern(rows, cols, seed: int = 0):
