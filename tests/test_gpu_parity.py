@@ -555,6 +555,42 @@ def test_tma_store_epilogue(sg, handle, algo, M, N, K, ldc, schedule):
             _assert_close(out[4:4 + M, :N], _ref(p))
 
 
+@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26])
+@pytest.mark.parametrize("M,N,K,ldc,beta", [(300, 517, 263, 519, 0.0), (257, 1000, 40, 1001, 0.5),
+                                            (70, 36, 8, 37, -1.0), (1500, 707, 2000, 709, 0.25)])
+def test_staged_row_run_epilogue(sg, handle, algo, M, N, K, ldc, beta):
+    # The same configurations with a C that TMA cannot address (odd ldc): the
+    # staged block leaves in row runs of plain stores, reading C first when
+    # beta != 0 (NaN canaries when beta == 0: never read).  The ldc padding
+    # and the rows around C keep their canaries.
+    for kind, alpha in (("uniform", 0.75), ("integer", 2.0)):
+        p = inputs.make_problem(M, N, K, seed=M + 3 * N + K + algo, kind=kind, alpha=alpha, beta=beta,
+                                with_c=True)
+        canary = np.frombuffer(np.uint32(0x7FC0BEEF).tobytes() * ((M + 8) * ldc),
+                               dtype=np.float32).reshape(M + 8, ldc).copy()
+        if beta != 0.0:
+            canary[4:4 + M, :N] = p.C0[:, :N]
+        buf = _to_dev(canary)
+        C = buf[4:4 + M, :N]
+        A, B = _to_dev(p.A)[:, :K], _to_dev(p.B)[:, :N]
+        handle.set_algo(algo)
+        plan = handle.plan(A, B, C, alpha, beta)
+        handle.gemm(A, B, C, alpha, beta)
+        torch.cuda.synchronize()
+        handle.set_algo(0)
+        assert handle.device_error() == 0
+        assert plan["vector_epilogue"] == 0 and plan["kind"] == 1
+        out = buf.cpu().numpy()
+        mask = np.ones(out.shape, bool)
+        mask[4:4 + M, :N] = False
+        assert (out.view(np.uint32)[mask] == 0x7FC0BEEF).all()
+        ref = oracle.sgemm_ref(M, N, K, alpha, p.A, p.B, beta, p.C0 if beta != 0.0 else None)
+        if kind == "integer":
+            np.testing.assert_array_equal(out[4:4 + M, :N].astype(np.float64), ref)
+        else:
+            _assert_close(out[4:4 + M, :N], ref)
+
+
 def test_tma_store_epilogue_batched(sg, handle):
     # Strided batches through configuration 24: the store map's third
     # dimension walks the batch stride (a multiple of 4 elements).
