@@ -264,24 +264,28 @@ bool small_preferred(const sgemmContext *h, const Problem &q) {
     return work <= kSmallMaxWork || (work <= 2 * kSmallMaxWork && blocks <= 2 * int64_t(h->sm_count));
 }
 
-// Tile configuration by shape.  Products with at most 64 rows (columns)
-// take the 64 x 512 (512 x 64) tile, which computes no padding rows
-// (columns) beyond 64.  Everything else takes 256 x 128, or 128 x 256 when
-// the product is under 256 rows or more than twice as wide as tall.  All of
-// these are one CTA of eight consumer warps per SM: two CTAs of four warps
-// per SM run
+// Tile configuration by shape (for the main kernel; the small-product
+// kernel above takes the smallest calls first).  Products with at most 64
+// rows (columns) take the 64 x 512 (512 x 64) tile, which computes no
+// padding rows (columns) beyond 64; 17 to 32, the 32 x 1024 (1024 x 32)
+// tile.  Everything else takes 256 x 128, or 128 x 256 when the product is
+// under 256 rows or more than twice as wide as tall.  All of these are one
+// CTA of eight consumer warps per SM: two CTAs of four warps per SM run
 // mostly one at a time (measured: the warp scheduler favours the older
 // CTA, whose inline TMA issuer keeps it fed while the other CTA's ring
 // starves), whereas warps of one CTA are held together by the shared ring.
-// Small matrices (both sides <= 128, e.g. the entries of a batch of small
-// products) take the 128 x 128 tile, which wastes the least of its lanes.
+// Matrices with both sides <= 128 that reach the main kernel (large
+// batches of them) take the 128 x 128 tile, which wastes the least of its
+// lanes.
 //
 // When beta == 0 and C is 16-byte aligned, the 256 x 128 and 128 x 256 tiles
 // come in a form whose warps hand C to TMA stores through shared memory, so
 // that C drains while the next tile computes; there the ring has only two
 // stages (the staging area takes the room) and each is refilled as soon as
 // every warp released it (measured at 4096^3: 2184 -> 2159 us; 16384^2 with
-// K = 8 / 16 / 32 / 64: 213 / 278 / 389 / 686 -> 174 / 228 / 350 / 597 us).
+// K = 8 / 16 / 32 / 64: 213 / 278 / 389 / 686 -> 173 / 224 / 346 / 593 us).
+// Short K takes the 16- or 8-deep slices (configurations 23, 24): the slice
+// depth that divides K multiplies no zero padding.
 bool c_vector_ok(const Problem &q) {
     return tma_ok(q.C, q.ldc) && (q.batch == 1 || q.sc % 4 == 0);
 }
