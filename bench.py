@@ -45,11 +45,11 @@ TENSOR_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sgemm_tf32x3_4096_traff
 # A kernel's code (the FFMA kernel with every tile configuration; the
 # tensor-core kernel); how it is launched is checked separately against the
 # plan recorded beside the traffic figure.
-# Sources the profiled FFMA launch is built from (configuration 22, the
+# Sources the profiled FFMA launch is built from (configuration 28, the
 # automatic choice at 4096^3 with beta == 0): a new configuration file does
 # not change it.
 KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_ffma.cuh", "fp32_sgemm_gb300/csrc/ptx.cuh",
-                  "fp32_sgemm_gb300/csrc/sgemm_algo22.cu"]
+                  "fp32_sgemm_gb300/csrc/sgemm_algo28.cu"]
 TENSOR_KERNEL_SOURCES = ["fp32_sgemm_gb300/csrc/sgemm_tf32x3.cu", "fp32_sgemm_gb300/csrc/ptx.cuh"]
 
 

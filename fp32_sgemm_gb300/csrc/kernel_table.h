@@ -47,7 +47,7 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
-constexpr int kNumAlgos = 26;
+constexpr int kNumAlgos = 30;
 void fill_algo1(KernelEntry *v);
 void fill_algo2(KernelEntry *v);
 void fill_algo3(KernelEntry *v);
@@ -74,6 +74,10 @@ void fill_algo23(KernelEntry *v);
 void fill_algo24(KernelEntry *v);
 void fill_algo25(KernelEntry *v);
 void fill_algo26(KernelEntry *v);
+void fill_algo27(KernelEntry *v);
+void fill_algo28(KernelEntry *v);
+void fill_algo29(KernelEntry *v);
+void fill_algo30(KernelEntry *v);
 
 // Tensor-core 3xTF32 path (sgemm_tf32x3.cu).
 struct Tf32x3Args {

@@ -61,6 +61,10 @@ void init_kernel_table() {
     sg::fill_algo24(g_kernels[23]);
     sg::fill_algo25(g_kernels[24]);
     sg::fill_algo26(g_kernels[25]);
+    sg::fill_algo27(g_kernels[26]);
+    sg::fill_algo28(g_kernels[27]);
+    sg::fill_algo29(g_kernels[28]);
+    sg::fill_algo30(g_kernels[29]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -216,14 +220,20 @@ struct Plan {
     int small_splits = 1;           // small-product kernel (kind 5): CTAs per block of C
 };
 
-// Configuration 15 (256 x 128 tile, eight consumer warps, one CTA per SM,
-// BK = 32, 4 stages, TMA issued by a compute thread, double-buffered 8-byte
-// A and 16-byte B fragments) measured fastest from 1024^3 to 8192^3 where C
-// is 16-byte aligned and read (beta != 0); otherwise configuration 22 (the
-// same tile and fragments, a 2-stage ring, C through a shared-memory staging
-// area: TMA stores when beta == 0 and C is aligned, else row runs).
-constexpr int kDefaultAlgo = 15;     // beta != 0, C 16-byte aligned
-constexpr int kStoreTmaAlgo = 22;    // beta == 0 or C not 16-byte aligned
+// Configuration 29 (256 x 128 tile, eight consumer warps, one CTA per SM,
+// BK = 32, 4 stages, TMA issued by a compute thread, 16-byte A reads (four
+// k per read) double buffered one k ahead, each k's B read just before its
+// FMAs) measured fastest from 1024^3 to 8192^3 where C is 16-byte aligned
+// and read (beta != 0); otherwise configuration 28 (the same tile and loop,
+// a 2-stage ring, C through a shared-memory staging area: TMA stores when
+// beta == 0 and C is aligned, else row runs).  Their loop beats the earlier
+// one (8-byte A and 16-byte B reads both double buffered: configurations
+// 15 and 22) by 1-2% (4096^3: 2160 -> 2134 us; 8192^3: 17293 -> 17023 us;
+// beta = 0.5: 2197 -> 2148 us).
+constexpr int kDefaultAlgo = 29;     // beta != 0, C 16-byte aligned
+constexpr int kStoreTmaAlgo = 28;    // beta == 0 or C not 16-byte aligned
+constexpr int kWideStoreTmaAlgo = 27;   // the same, 128 x 256, for wide products
+constexpr int kWideAlgo = 30;           // 128 x 256 reading C from registers
 
 // 17 to 32 rows (columns), large enough to give every SM at least 8 K slices
 // of 32 x 1024 (1024 x 32) tiles: there the FFMA kernel with those tiles runs
@@ -301,12 +311,12 @@ int choose_algo(const sgemmContext *h, const Problem &q) {
     // (C not 16-byte aligned; 4095 x 4097 x 1023 with beta = 0.25:
     // 669 -> 617 us).  Aligned C with beta != 0 keeps the register epilogue.
     if (c_vector_ok(q) ? q.beta == 0.0f : true) {
-        if (q.M < 256 || q.N > 2 * q.M) return 26 - 1;
+        if (q.M < 256 || q.N > 2 * q.M) return kWideStoreTmaAlgo - 1;
         // Short K: the K slice that divides K (32, 16, else 8 deep).
         if (q.K <= 64 && q.K % 32 != 0) return (q.K % 16 == 0 ? 23 : 24) - 1;
         return kStoreTmaAlgo - 1;
     }
-    if (q.M < 256 || q.N > 2 * q.M) return 14 - 1;
+    if (q.M < 256 || q.N > 2 * q.M) return kWideAlgo - 1;
     // Short K (writing C bounds the product): slices no deeper than needed,
     // so that little zero padding is multiplied (measured at 16384^2: K = 8
     // 393 -> 213 us with 8-deep slices, K = 16 393 -> 278 us with 16-deep).

@@ -86,7 +86,10 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 //   PRODUCER_WARP: 1 = a dedicated TMA warp, 0 = thread 0 of the first
 //   consumer warp issues the loads (no extra warp);
 //   PIPE: 1 = fragments of the next k are read while this k's FMAs run
-//   (explicit register double buffering), 0 = left to the compiler;
+//   (explicit register double buffering), 2 = only the A fragments are
+//   double buffered (the next A group read one k ahead; each k's B values
+//   read just before its FMAs, which frees 16 registers for 16-byte A
+//   reads), 0 = left to the compiler;
 //   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2);
 //   STORE_TMA: 1 = beta == 0 tiles leave through a per-warp shared-memory
 //   staging area and TMA tile stores (64 x 16 boxes) instead of st.global;
@@ -108,6 +111,7 @@ struct FfmaConfig {
     static constexpr int KA = KA_;
     static constexpr bool PRODUCER_WARP = PRODUCER_WARP_ != 0;
     static constexpr bool PIPE = PIPE_ != 0;
+    static constexpr bool PIPE_B = PIPE_ == 1;   // B fragments double buffered too
     static constexpr bool SCALAR_FMA = SCALAR_FMA_ != 0;   // fmaf instead of packed fma.rn.f32x2
     static constexpr bool STORE_TMA = STORE_TMA_ != 0;
     static constexpr int REFILL_LAG = REFILL_LAG_;
@@ -531,7 +535,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 AVec a0[TM], a1[TM];
                 float4 b0[NJ], b1[NJ];
                 load_a(As, 0, a0);
-                load_b(Bs, 0, b0);
+                if constexpr (Cfg::PIPE_B) load_b(Bs, 0, b0);
                 constexpr int KSTEPS = Cfg::KQ_UNROLL * KA;
 #pragma unroll 1
                 for (int kq0 = 0; kq0 < NKQ; kq0 += Cfg::KQ_UNROLL) {
@@ -543,10 +547,17 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                         for (int kr = 0; kr < KA; ++kr) {
                             const int ks = u * KA + kr;                 // k step inside the iteration
-                            float4 (&bc)[NJ] = (ks & 1) ? b1 : b0;
+                            float4 (&bc)[NJ] = (Cfg::PIPE_B && (ks & 1)) ? b1 : b0;
                             float4 (&bn)[NJ] = (ks & 1) ? b0 : b1;
                             const bool last = ks == KSTEPS - 1;
-                            if (!last || more) load_b(Bs, kq0 * KA + ks + 1, bn);
+                            if constexpr (Cfg::PIPE_B) {
+                                if (!last || more) load_b(Bs, kq0 * KA + ks + 1, bn);
+                            } else {
+                                // Keep each k's B reads in place: hoisted
+                                // reads of later k would need registers.
+                                asm volatile("" ::: "memory");
+                                load_b(Bs, kq0 * KA + ks, bc);
+                            }
                             if (kr == KA - 2 && (u + 1 < Cfg::KQ_UNROLL || more))
                                 load_a(As, kq0 + u + 1, an);
                             fma_k(ac, kr, bc);

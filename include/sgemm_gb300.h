@@ -262,11 +262,11 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * 128, 18 / 19 for large products of 17 to 32 rows / columns, 16 for at
  * most 64 rows, 17 for at most 64 columns; then, when beta == 0 and C is
  * 16-byte aligned or when C is not 16-byte aligned (C through a
- * shared-memory staging area), 26 under 256 rows or for products more than twice as
- * wide as tall, 23 / 24 for K of at most 64 that is a multiple of 16 / not
- * a multiple of 16 (multiples of 32 excepted), else 22; otherwise 14 under
- * 256 rows or for wide products, 20 / 21 for K of at most 64 that is not a
- * multiple of 32, else 15); 1..11 = a fixed
+ * shared-memory staging area), 27 under 256 rows or for products more than
+ * twice as wide as tall, 23 / 24 for K of at most 64 that is a multiple of
+ * 16 / not a multiple of 16 (multiples of 32 excepted), else 28; otherwise
+ * 30 under 256 rows or for wide products, 20 / 21 for K of at most 64 that
+ * is not a multiple of 32, else 29); 1..11 = a fixed
  * configuration of the 128 x 128 output tile (K slice 16 or 32, 3 or 4
  * pipeline stages, a dedicated TMA warp or TMA issued by a compute thread,
  * one or two CTAs per SM, packed or scalar FMAs); 12 = 64 x 256,
@@ -277,8 +277,10 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * 26 = 128 x 256 with 2 stages, 23 / 25 = 256 x 128 with K slices of 16
  * and 4 stages, 24 = 256 x 128 with K slices of 8 and 8 stages, all five
  * storing C through shared memory: by TMA when beta == 0 and C is 16-byte
- * aligned, in row runs of plain stores when C is not 16-byte aligned
- * (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).  In math mode 1
+ * aligned, in row runs of plain stores when C is not 16-byte aligned;
+ * 27 / 28 / 29 / 30 = 26 / 22 / 15 / 14 with 16-byte A reads and only the
+ * A fragments double buffered (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).
+ * In math mode 1
  * (3xTF32) the values 1..3 pick the tensor-core tile instead: 128 x 128,
  * 128 x 192 or 128 x 256.  Every configuration computes the same result up
  * to summation order.

@@ -111,7 +111,7 @@ def test_workload_8192_sampled_integer_bit_exact(sg, handle):
     np.testing.assert_array_equal(got.astype(np.float64), ref)
 
 
-@pytest.mark.parametrize("algo", list(range(1, 27)))
+@pytest.mark.parametrize("algo", list(range(1, 31)))
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263)])
 def test_every_tile_configuration(sg, handle, algo, shape):
     M, N, K = shape
@@ -519,12 +519,12 @@ def test_short_k_takes_shallow_slices(sg, handle, K):
     assert handle.plan(A, B, C, 1.0, 0.5)["tile_k"] == (16 if (K % 16 == 0 or K > 32) else 8)
 
 
-@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26])
+@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26, 27, 28])
 @pytest.mark.parametrize("M,N,K,ldc,schedule", [(1024, 1024, 1024, 1024, 0), (300, 520, 263, 520, 0),
                                                 (257, 1000, 40, 1012, 0), (70, 36, 8, 40, 0),
                                                 (1500, 704, 2000, 708, 2)])
 def test_tma_store_epilogue(sg, handle, algo, M, N, K, ldc, schedule):
-    # Configurations 22-26 with beta == 0 and a 16-byte aligned C: each warp
+    # Configurations 22-28 with beta == 0 and a 16-byte aligned C: each warp
     # stages its block in shared memory and TMA stores it, clipped at M and
     # N.  C starts as NaN canaries (never read); the ldc padding and the rows
     # around C must keep them.  Schedule 2 cuts tiles between CTAs (stream-K),
@@ -544,7 +544,7 @@ def test_tma_store_epilogue(sg, handle, algo, M, N, K, ldc, schedule):
         handle.set_schedule(0)
         handle.set_algo(0)
         assert handle.device_error() == 0
-        assert plan["vector_epilogue"] == 1 and plan["tile_k"] == {22: 32, 23: 16, 24: 8, 25: 16, 26: 32}[algo]
+        assert plan["vector_epilogue"] == 1 and plan["tile_k"] == {22: 32, 23: 16, 24: 8, 25: 16, 26: 32, 27: 32, 28: 32}[algo]
         out = buf.cpu().numpy()
         mask = np.ones(out.shape, bool)
         mask[4:4 + M, :N] = False
@@ -555,7 +555,7 @@ def test_tma_store_epilogue(sg, handle, algo, M, N, K, ldc, schedule):
             _assert_close(out[4:4 + M, :N], _ref(p))
 
 
-@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26])
+@pytest.mark.parametrize("algo", [22, 23, 24, 25, 26, 27, 28])
 @pytest.mark.parametrize("M,N,K,ldc,beta", [(300, 517, 263, 519, 0.0), (257, 1000, 40, 1001, 0.5),
                                             (70, 36, 8, 37, -1.0), (1500, 707, 2000, 709, 0.25)])
 def test_staged_row_run_epilogue(sg, handle, algo, M, N, K, ldc, beta):
