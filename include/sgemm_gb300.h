@@ -279,7 +279,8 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * storing C through shared memory: by TMA when beta == 0 and C is 16-byte
  * aligned, in row runs of plain stores when C is not 16-byte aligned;
  * 27 / 28 / 29 / 30 = 26 / 22 / 15 / 14 with 16-byte A reads and only the
- * A fragments double buffered (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).
+ * A fragments double buffered, the inner loop that 16, 17, 23 and 24 use
+ * as well (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).
  * In math mode 1
  * (3xTF32) the values 1..3 pick the tensor-core tile instead: 128 x 128,
  * 128 x 192 or 128 x 256.  Every configuration computes the same result up
