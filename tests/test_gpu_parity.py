@@ -122,7 +122,7 @@ def test_every_tile_configuration(sg, handle, algo, shape):
 
 
 @pytest.mark.parametrize("schedule", [1, 2])
-@pytest.mark.parametrize("algo", [1, 3, 5, 8])
+@pytest.mark.parametrize("algo", [1, 3, 5, 8, 28, 29])
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024), (300, 517, 263), (1500, 700, 2000),
                                    (257, 255, 4000)])
 def test_schedules(sg, handle, schedule, algo, shape):
