@@ -45,6 +45,29 @@ def test_binding_signatures_cover_the_header():
     assert set(_binding.SIGNATURES) == _declared_functions()
 
 
+def test_header_is_plain_c(tmp_path):
+    # The boundary is a C ABI: the header must compile as C99 on its own
+    # (no C++ types), and call the library through a C translation unit.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "sgemm_gb300.h"\n'
+                   "int main(void) {\n"
+                   "    sgemmPlan_t plan;\n"
+                   "    int v = 0;\n"
+                   "    (void)plan;\n"
+                   "    return sgemmGetVersion(&v) == SGEMM_STATUS_SUCCESS ? 0 : 1;\n"
+                   "}\n")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, "-c", str(src), "-o", str(tmp_path / "use_header.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     for st in _binding.Status:
         assert sg.status_string(st) == "SGEMM_STATUS_" + st.name
