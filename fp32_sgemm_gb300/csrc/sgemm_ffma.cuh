@@ -15,9 +15,12 @@
 //     (fma.rn.f32x2: each lane issues one instruction per two products).
 //   * epilogue straight from registers: alpha*acc (+ beta*C, and C is not
 //     read when beta == 0), 16-byte stores when C's alignment allows; or, in
-//     the configurations for short K, each warp writes its alpha*acc block
-//     to its own shared-memory staging area and one lane hands it to TMA
-//     tile stores, so that C drains to memory while the next tile computes.
+//     the STORE_TMA configurations (the automatic choice wherever C is not
+//     read, and wherever C is not 16-byte aligned), each warp writes its
+//     alpha*acc block to its own shared-memory staging area, and then either
+//     one lane hands it to TMA tile stores, so that C drains to memory while
+//     the next tile computes, or (C not 16-byte aligned) the warp writes it
+//     back in 64-byte row runs.
 //
 // What the pages contribute, and what changed for this chip:
 //   * the per-thread outer-product register tile and the K loop over staged
@@ -31,7 +34,10 @@
 //   * the thread tile's A values read as 16-byte vectors (the pages transpose
 //     A in shared memory for this; TMA cannot transpose 4-byte elements, so
 //     A stays k-contiguous and each 16-byte read carries 4 consecutive k of
-//     one row, used over 4 k steps); bank conflicts between the rows a warp
+//     one row, used over 4 k steps; the next group is read one k step ahead,
+//     while each k's B values are read just before its FMAs, which is what
+//     fits 255 registers -- some configurations keep 8-byte A reads with
+//     both fragments double buffered); bank conflicts between the rows a warp
 //     reads together are removed by the TMA 32/64/128-byte swizzle instead
 //     of padding, which keeps every vector read 16-byte aligned ("The Final
 //     Kernel", "The Padding Has To Go");
