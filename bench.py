@@ -66,7 +66,7 @@ def parse_args():
                     help="0 FP32 FFMA (CUDA cores), 1 error-compensated 3xTF32 (tensor cores)")
     ap.add_argument("--schedule", type=int, default=0,
                     help="0 automatic, 1 whole tiles per CTA, 2 stream-K")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--tensor-steps", type=int, default=100,
                     help="steps of the 3xTF32 path reported beside the FFMA line (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
