@@ -132,9 +132,17 @@ def _torch():
     return torch
 
 
-def _stream_ptr(stream) -> int | None:
+def _stream_ptr(stream, device_index: int | None = None) -> int | None:
+    """cudaStream_t of `stream` (None: torch's current stream on the given
+    device, else on the current device)."""
     torch = _torch()
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            # The raw-handle query skips building a torch.cuda.Stream object
+            # (a few microseconds per call, as much as a small product takes).
+            idx = torch.cuda.current_device() if device_index is None else device_index
+            return raw(idx) or None
         stream = torch.cuda.current_stream()
     if isinstance(stream, int):
         return stream or None
@@ -146,18 +154,20 @@ def _matrix(t, name: str, rows: int | None = None, cols: int | None = None):
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.float32:
+    if t.dtype is not torch.float32:
         raise TypeError(f"{name} must be float32, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dim() != 2:
+    shape = t.shape
+    if len(shape) != 2:
         raise ValueError(f"{name} must be 2-D")
-    r, c = t.shape
-    if r > 1 and c > 0 and t.stride(1) != 1:
+    r, c = shape
+    stride = t.stride()
+    if r > 1 and c > 0 and stride[1] != 1:
         raise ValueError(f"{name} must be row major (stride(1) == 1)")
-    ld = t.stride(0) if r > 1 else max(c, 1)
+    ld = stride[0] if r > 1 else max(c, 1)
     if rows is not None and r != rows or cols is not None and c != cols:
-        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected ({rows}, {cols})")
+        raise ValueError(f"{name} has shape {tuple(shape)}, expected ({rows}, {cols})")
     return t.data_ptr(), max(ld, c, 1)
 
 
@@ -175,6 +185,10 @@ class Handle:
         with torch.cuda.device(self.device):
             _check(self._lib.sgemmCreate(ctypes.byref(self._h)), "sgemmCreate")
         self._ws = None
+        # Workspace sizes already asked for, by shape, pitches and operand
+        # alignment; the handle's settings enter the size, so their setters
+        # clear it.
+        self._ws_sizes = {}
 
     @property
     def ptr(self):
@@ -194,6 +208,7 @@ class Handle:
 
     def set_algo(self, algo: int):
         _check(self._lib.sgemmSetAlgo(self._h, int(algo)), "sgemmSetAlgo")
+        self._ws_sizes.clear()
 
     def set_kernel_events(self, start, stop):
         """Record torch.cuda.Event objects around the main kernel of later
@@ -206,10 +221,12 @@ class Handle:
     def set_math_mode(self, mode: int):
         """0 FP32 FFMA (default), 1 error-compensated 3xTF32 on the tensor cores."""
         _check(self._lib.sgemmSetMathMode(self._h, int(mode)), "sgemmSetMathMode")
+        self._ws_sizes.clear()
 
     def set_schedule(self, schedule: int):
         """0 automatic, 1 whole tiles per CTA, 2 stream-K when it applies."""
         _check(self._lib.sgemmSetSchedule(self._h, int(schedule)), "sgemmSetSchedule")
+        self._ws_sizes.clear()
 
     def set_wait_timeout(self, ns: int):
         _check(self._lib.sgemmSetWaitTimeout(self._h, int(ns)), "sgemmSetWaitTimeout")
@@ -304,9 +321,15 @@ class Handle:
         b, ldb = _matrix(B, "B")
         c, ldc = _matrix(C, "C", M, N)
         if M and N and K and alpha != 0.0:
-            self._ensure_workspace(self.workspace_size(M, N, K, a, lda, b, ldb))
+            key = (M, N, K, lda, ldb, a & 15, b & 15)
+            need = self._ws_sizes.get(key)
+            if need is None:
+                if len(self._ws_sizes) > 256:
+                    self._ws_sizes.clear()
+                need = self._ws_sizes[key] = self.workspace_size(M, N, K, a, lda, b, ldb)
+            self._ensure_workspace(need)
         _check(self._lib.sgemmEx(self._h, M, N, K, float(alpha), a, lda, b, ldb, float(beta),
-                                 c, ldc, _stream_ptr(stream)), "sgemmEx")
+                                 c, ldc, _stream_ptr(stream, self.device.index)), "sgemmEx")
         return C
 
 
