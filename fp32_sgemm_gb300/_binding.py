@@ -301,14 +301,20 @@ class Handle:
             raise ValueError("batch sizes do not match")
         oa, ob = int(bool(trans_a)), int(bool(trans_b))
         if M and N and K and batch and alpha != 0.0:
-            n = ctypes.c_size_t()
-            _check(self._lib.sgemmStridedBatchedWorkspaceSize(
-                self._h, oa, ob, M, N, K, a, lda, sa, b, ldb, sb, batch, ctypes.byref(n)),
-                "sgemmStridedBatchedWorkspaceSize")
-            self._ensure_workspace(n.value)
+            key = ("batched", oa, ob, M, N, K, lda, sa, ldb, sb, batch, a & 15, b & 15)
+            need = self._ws_sizes.get(key)
+            if need is None:
+                n = ctypes.c_size_t()
+                _check(self._lib.sgemmStridedBatchedWorkspaceSize(
+                    self._h, oa, ob, M, N, K, a, lda, sa, b, ldb, sb, batch, ctypes.byref(n)),
+                    "sgemmStridedBatchedWorkspaceSize")
+                if len(self._ws_sizes) > 256:
+                    self._ws_sizes.clear()
+                need = self._ws_sizes[key] = n.value
+            self._ensure_workspace(need)
         _check(self._lib.sgemmStridedBatched(self._h, oa, ob, M, N, K, float(alpha), a, lda, sa, b,
                                              ldb, sb, float(beta), c, ldc, sc, batch,
-                                             _stream_ptr(stream)), "sgemmStridedBatched")
+                                             _stream_ptr(stream, self.device.index)), "sgemmStridedBatched")
         return C
 
     def gemm(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
