@@ -7,8 +7,13 @@ of the chip's FP32 FFMA peak.
 
 One step is one call of the library (C = alpha*A@B + beta*C) on one batch of
 synthetic inputs (uniform[-1, 1), seed of the workload) already resident in
-HBM.  Three input sets are rotated so that consecutive steps never find their
-operands in L2.  Prints ONE JSON line on rank 0.
+HBM.  Input sets are rotated (at least three, and together more than 1.2x
+the L2) so that consecutive steps never find their operands in L2.  Prints
+ONE JSON line on rank 0: the headline workload (4096^3 by default) with its
+roofline, end-to-end value, oracle baseline and run-to-run spread, and under
+"workloads" the other four workloads of the benchmark set (128^3, 1024^3,
+4095 x 4097 x 1023 with alpha 0.5 / beta 0.25, 8192^3), each measured the
+same way.
 
 Under torchrun (N > 1) every rank multiplies its own copy of the workload on
 its own GPU (independent replicas, no data exchange); the host-side barrier
@@ -70,6 +75,10 @@ def parse_args():
     ap.add_argument("--tensor-steps", type=int, default=100,
                     help="steps of the 3xTF32 path reported beside the FFMA line (0 = skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only the headline workload (not the other four of the set)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="repeats of the timed K-step loop for the run-to-run spread")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -304,53 +313,86 @@ def job_tflops(flops_per_rank_step: float, world: int, ms_per_step: float) -> fl
     return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
 
 
-def run_ours(args, w, rank: int, world: int, local_rank: int):
-    import torch
-    import fp32_sgemm_gb300 as sg
+class GpuContext:
+    """What every measurement on this rank shares: device, stream, handle."""
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    sg.load_library(build_if_missing=True)
-    handle = sg.Handle(dev)
-    handle.set_algo(args.algo)
-    handle.set_schedule(args.schedule)
-    handle.set_math_mode(args.math)
-    props = torch.cuda.get_device_properties(dev)
-    sms = props.multi_processor_count
-    l2_bytes = getattr(props, "L2_cache_size", 0) or 0
+    def __init__(self, args, rank: int, world: int, local_rank: int):
+        import torch
+        import fp32_sgemm_gb300 as sg
+        self.torch, self.sg = torch, sg
+        self.args, self.rank, self.world, self.local_rank = args, rank, world, local_rank
+        torch.cuda.set_device(local_rank)
+        self.dev = torch.device("cuda", local_rank)
+        sg.load_library(build_if_missing=True)
+        self.handle = sg.Handle(self.dev)
+        self.handle.set_algo(args.algo)
+        self.handle.set_schedule(args.schedule)
+        self.handle.set_math_mode(args.math)
+        props = torch.cuda.get_device_properties(self.dev)
+        self.sms = props.multi_processor_count
+        self.l2_bytes = getattr(props, "L2_cache_size", 0) or 0
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            self.dist = dist
 
-    p = inputs.workload_problem(w, "uniform")
-    set_bytes = 4 * (p.A.size + p.B.size + w.M * w.N)
-    nsets = 3
-    A0 = torch.from_numpy(p.A).to(dev)
-    B0 = torch.from_numpy(p.B).to(dev)
-    C0 = torch.from_numpy(p.C0).to(dev) if p.C0 is not None else torch.zeros((w.M, w.N), device=dev)
-    sets = [(A0, B0, C0)] + [(A0.clone(), B0.clone(), C0.clone()) for _ in range(nsets - 1)]
-    handle._ensure_workspace(handle.workspace_size(w.M, w.N, w.K, A0.data_ptr(), A0.stride(0),
-                                                   B0.data_ptr(), B0.stride(0)))
-    plan = handle.plan(A0, B0, C0, w.alpha, w.beta)
-    stream = torch.cuda.current_stream(dev)
 
-    def timed_loop(steps: int, warmup: int, sample_clocks: bool, kernel_events: bool):
+class WorkloadRun:
+    """Device-resident inputs of one workload, rotated over enough sets that
+    consecutive steps never find their operands in L2, and the timed loops
+    over them."""
+
+    def __init__(self, ctx: GpuContext, w):
+        torch = ctx.torch
+        self.ctx, self.w = ctx, w
+        self.p = inputs.workload_problem(w, "uniform")
+        p = self.p
+        self.set_bytes = 4 * (p.A.size + p.B.size + w.M * w.N)
+        # At least three sets, and together more than 1.2x the L2 (small
+        # workloads would otherwise run from L2 between steps).
+        want = int(np.ceil(1.2 * max(ctx.l2_bytes, 1) / self.set_bytes)) + 1
+        self.nsets = max(3, min(want, 1024))
+        A0 = torch.from_numpy(p.A).to(ctx.dev)
+        B0 = torch.from_numpy(p.B).to(ctx.dev)
+        C0 = (torch.from_numpy(p.C0).to(ctx.dev) if p.C0 is not None
+              else torch.zeros((w.M, w.N), device=ctx.dev))
+        self.sets = [(A0, B0, C0)] + [(A0.clone(), B0.clone(), C0.clone()) for _ in range(self.nsets - 1)]
+        self.ensure_workspace()
+        self.plan = ctx.handle.plan(A0, B0, C0, w.alpha, w.beta)
+
+    def ensure_workspace(self):
+        A0, B0, _ = self.sets[0]
+        h = self.ctx.handle
+        h._ensure_workspace(h.workspace_size(self.w.M, self.w.N, self.w.K, A0.data_ptr(), A0.stride(0),
+                                             B0.data_ptr(), B0.stride(0)))
+
+    def l2_note(self) -> str:
+        return (f"{self.nsets} rotating input sets of {self.set_bytes / 1e6:.1f} MB "
+                f"({self.nsets * self.set_bytes / 1e6:.0f} MB > {self.ctx.l2_bytes / 1e6:.0f} MB L2)")
+
+    def timed_loop(self, steps: int, warmup: int, sample_clocks: bool, kernel_events: bool):
         """Warm up, then time `steps` calls on the device (events on the
         launching stream); with kernel_events, also each call's main kernel
         alone (events the library records right around that launch; their
         host cost would count in the step time of small products, so the
         step time comes from a loop without them)."""
+        ctx, w = self.ctx, self.w
+        torch, h, stream = ctx.torch, ctx.handle, ctx.stream
         for i in range(max(warmup, 3)):
-            A, B, C = sets[i % nsets]
-            handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
-        torch.cuda.synchronize(dev)
-        assert handle.device_error() == 0
-        kstart = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        kstop = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            A, B, C = self.sets[i % self.nsets]
+            h.gemm(A, B, C, w.alpha, w.beta, stream=stream)
+        torch.cuda.synchronize(ctx.dev)
+        assert h.device_error() == 0
+        kstart = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if kernel_events else []
+        kstop = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if kernel_events else []
         for e in kstart + kstop:
             e.record(stream)          # torch creates the event on first record
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        sampler = ClockSampler(local_rank) if sample_clocks else None
+        torch.cuda.synchronize(ctx.dev)
+        if ctx.dist is not None:
+            ctx.dist.barrier()
+        torch.cuda.synchronize(ctx.dev)
+        sampler = ClockSampler(ctx.local_rank) if sample_clocks else None
         if sampler:
             sampler.start()
             time.sleep(0.3)
@@ -358,86 +400,185 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         t_end = torch.cuda.Event(enable_timing=True)
         t_begin.record(stream)
         for i in range(steps):
-            A, B, C = sets[i % nsets]
+            A, B, C = self.sets[i % self.nsets]
             if kernel_events:
-                handle.set_kernel_events(kstart[i], kstop[i])
-            handle.gemm(A, B, C, w.alpha, w.beta, stream=stream)
+                h.set_kernel_events(kstart[i], kstop[i])
+            h.gemm(A, B, C, w.alpha, w.beta, stream=stream)
         t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        handle.set_kernel_events(None, None)
+        torch.cuda.synchronize(ctx.dev)
+        h.set_kernel_events(None, None)
         clocks = sampler.stop() if sampler else None
-        if world > 1:
-            dist.barrier()
+        if ctx.dist is not None:
+            ctx.dist.barrier()
         elapsed = t_begin.elapsed_time(t_end)
-        kms = [a.elapsed_time(b) for a, b in zip(kstart, kstop)] if kernel_events else []
-        assert handle.device_error() == 0
-        elapsed = max_over_ranks(elapsed, dev)
+        kms = [a.elapsed_time(b) for a, b in zip(kstart, kstop)]
+        assert h.device_error() == 0
+        elapsed = max_over_ranks(elapsed, ctx.dev)
         return elapsed, kms, clocks
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
+    def roofline(self, launch_ms: list, clocks: dict | None) -> dict:
+        ctx, w = self.ctx, self.w
+        flops = 2.0 * w.M * w.N * w.K
+        mean_launch_ms = statistics.mean(launch_ms)
+        achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+        max_mhz = (clocks or {}).get("sm_max_mhz") or sm_max_mhz_query(ctx.local_rank) or 2070.0
+        sus_mhz = (clocks or {}).get("sm_mhz")
+        algo_bytes = 4.0 * (w.M * w.K + w.K * w.N + w.M * w.N * (2 if w.beta != 0.0 else 1))
+        hbm_peak, hbm_basis = measured_hbm()
+        ffma_peak_est = ctx.sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6
+        if flops / algo_bytes < ffma_peak_est / (hbm_peak * 1e9):
+            # Skinny shapes: below the ridge, HBM bounds the kernel.
+            gbs = algo_bytes / (mean_launch_ms * 1e-3) / 1e9
+            r = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                 "frac": gbs / hbm_peak, "traffic": None, "peak_basis": hbm_basis,
+                 "achieved_basis": "compulsory bytes 4(MK+KN+MN) per call over the timed kernels "
+                                   "(streaming kernel + split reduction)",
+                 "tflops": achieved}
+        elif ctx.args.math == 0:
+            # Roofline of the dominant (main) kernel: bound by the FP32 FMA pipes.
+            peak = ctx.sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
+            peak_sus = ctx.sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
+            r = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                 "frac": achieved / peak,
+                 "traffic": profiled_traffic(self.plan) if w.name == "sgemm_4096" else None,
+                 "peak_basis": f"{ctx.sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x "
+                               f"{max_mhz:.0f} MHz (max SM clock)",
+                 "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
+                 "sustained_sm_mhz": sus_mhz}
+        else:
+            r = tensor_roofline(flops, mean_launch_ms)
+        r.update({"kernel_ms_mean": mean_launch_ms, "kernel_ms_min": min(launch_ms),
+                  "kernel_ms_median": statistics.median(launch_ms)})
+        return r
+
+    def e2e(self, steps: int) -> dict:
+        """The same metric through the host-buffer C entry point: pinned host
+        A, B (C), copies up, product, copy of C down, all timed."""
+        ctx, w, p = self.ctx, self.w, self.p
+        torch, sg = ctx.torch, ctx.sg
+        Ah = torch.from_numpy(p.A).pin_memory()
+        Bh = torch.from_numpy(p.B).pin_memory()
+        Ch = (torch.from_numpy(p.C0.copy()) if p.C0 is not None
+              else torch.zeros((w.M, w.N))).pin_memory()
+        ws = torch.empty(sg.host_workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device=ctx.dev)
+        for _ in range(3):
+            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=ctx.handle, stream=ctx.stream)
+        torch.cuda.synchronize(ctx.dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(ctx.stream)
+        for _ in range(steps):
+            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=ctx.handle, stream=ctx.stream)
+        e1.record(ctx.stream)
+        torch.cuda.synchronize(ctx.dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, ctx.dev)
+        del ws
+        h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0.0 else 0))
+        return {"value": job_tflops(2.0 * w.M * w.N * w.K, ctx.world, e_ms), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N,
+                "ms_per_step": e_ms, "steps": steps,
+                "path": "sgemmHostEx: pinned host A,B -> device, SGEMM, C -> pinned host"}
+
+    def cpu_baseline(self, seconds: float) -> dict:
+        w, p = self.w, self.p
+        c_flops, c_times, rows, threads = oracle_rows_sample(w, p, seconds, 1)
+        cpu = {"value": c_flops / c_times[0] / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{rows} of {w.M} output rows (all {w.N} columns, K={w.K}) "
+                         f"in {c_times[0]:.2f} s, fp64 C oracle"}
+        cpu.update(oracle_extra_timings(w, p, min(seconds, 10.0)))
+        return cpu
+
+    def release(self):
+        self.sets = None
+        self.ctx.torch.cuda.empty_cache()
+
+
+def steps_for(run: WorkloadRun, asked: int, min_ms: float = 40.0, cap: int = 4000) -> int:
+    """At least the steps asked for, and enough for about min_ms of timed
+    work (a 128^3 step takes microseconds)."""
+    w = run.w
+    est_ms = max(2.0 * w.M * w.N * w.K / 60e12 * 1e3, 0.004)
+    return int(min(cap, max(asked, np.ceil(min_ms / est_ms))))
+
+
+def measure_workload(ctx: GpuContext, w, steps: int, warmup: int, e2e_steps: int, cpu_seconds: float):
+    """One entry of the `workloads` map: device throughput, kernel-event
+    times and roofline, end-to-end value and the oracle on the host cores."""
+    run = WorkloadRun(ctx, w)
+    steps = steps_for(run, steps)
+    el, _, clocks = run.timed_loop(steps, warmup, True, False)
+    _, kms, _ = run.timed_loop(steps, warmup, False, True)
+    ms = el / steps
+    entry = {
+        "value": job_tflops(2.0 * w.M * w.N * w.K, ctx.world, ms), "unit": "TFLOP/s", "ms_per_step": ms,
+        "steps": steps, "warmup": max(warmup, 3),
+        "config": dict(workload_config(w, run.l2_note()),
+                       schedule="stream-K" if run.plan["stream_k"] else "whole tiles",
+                       kind=run.plan["kind"],
+                       tile=f"{run.plan['tile_m']}x{run.plan['tile_n']}x{run.plan['tile_k']}",
+                       ctas=run.plan["ctas"], launches_per_step=run.plan["launches"]),
+        "roofline": run.roofline(kms, clocks),
+        "gpu_launches": steps * run.plan["launches"],
+        "clocks": clocks,
+    }
+    if w.name == "sgemm_128":
+        entry["us_per_step"] = ms * 1e3
+    run.release()
+    if e2e_steps > 0:
+        entry["e2e"] = run.e2e(e2e_steps)
+    if ctx.rank == 0 and cpu_seconds > 0:
+        entry["cpu_baseline"] = run.cpu_baseline(cpu_seconds)
+    return entry
+
+
+def run_ours(args, w, rank: int, world: int, local_rank: int):
+    ctx = GpuContext(args, rank, world, local_rank)
+    handle = ctx.handle
+    run = WorkloadRun(ctx, w)
+    plan = run.plan
+
     # The step time (value) from a loop with nothing but the calls, clocks
     # sampled meanwhile; the main kernel's own time (roofline) from a second
     # loop with the library's kernel events.
-    elapsed_ms, _, clocks = timed_loop(args.steps, args.warmup, True, False)
-    _, launch_ms, _ = timed_loop(args.steps, args.warmup, False, True)
+    elapsed_ms, _, clocks = run.timed_loop(args.steps, args.warmup, True, False)
+    _, launch_ms, _ = run.timed_loop(args.steps, args.warmup, False, True)
 
     flops = 2.0 * w.M * w.N * w.K
     ms_per_step = elapsed_ms / args.steps
     value = job_tflops(flops, world, ms_per_step)
+    roofline = run.roofline(launch_ms, clocks)
 
-    mean_launch_ms = statistics.mean(launch_ms)
-    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
-    max_mhz = clocks.get("sm_max_mhz") or sm_max_mhz_query(local_rank) or 2070.0
-    sus_mhz = clocks.get("sm_mhz")
-    algo_bytes = 4.0 * (w.M * w.K + w.K * w.N + w.M * w.N * (2 if w.beta != 0.0 else 1))
-    hbm_peak, hbm_basis = measured_hbm()
-    ffma_peak_est = sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6
-    if flops / algo_bytes < ffma_peak_est / (hbm_peak * 1e9):
-        # Skinny shapes: below the ridge, HBM bounds the kernel.
-        gbs = algo_bytes / (mean_launch_ms * 1e-3) / 1e9
-        roofline = {
-            "bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-            "frac": gbs / hbm_peak, "traffic": None, "peak_basis": hbm_basis,
-            "achieved_basis": "compulsory bytes 4(MK+KN+MN) per call over the timed kernels "
-                              "(streaming kernel + split reduction)",
-            "tflops": achieved,
-        }
-    elif args.math == 0:
-        # Roofline of the dominant (main) kernel: bound by the FP32 FMA pipes.
-        peak = sms * FFMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
-        peak_sus = sms * FFMA_PER_CLK_PER_SM * 2 * sus_mhz * 1e6 / 1e12 if sus_mhz else None
-        roofline = {
-            "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(plan) if w.name == "sgemm_4096" else None,
-            "peak_basis": f"{sms} SMs x {FFMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 FLOP x "
-                          f"{max_mhz:.0f} MHz (max SM clock)",
-            "frac_at_sustained_clock": (achieved / peak_sus) if peak_sus else None,
-            "sustained_sm_mhz": sus_mhz,
-        }
-    else:
-        roofline = tensor_roofline(flops, mean_launch_ms)
-    roofline.update({"kernel_ms_mean": mean_launch_ms, "kernel_ms_min": min(launch_ms),
-                     "kernel_ms_median": statistics.median(launch_ms)})
+    # Run-to-run spread: the same K-step loop repeated, (max - min) / median
+    # of the per-repeat throughput.
+    spread = None
+    if args.repeats > 1:
+        vals = [value]
+        for _ in range(args.repeats - 1):
+            el, _, _ = run.timed_loop(args.steps, args.warmup, False, False)
+            vals.append(job_tflops(flops, world, el / args.steps))
+        med = statistics.median(vals)
+        spread = {"repeats": len(vals), "steps_each": args.steps, "values": vals,
+                  "min": min(vals), "max": max(vals), "median": med,
+                  "rel_spread": (max(vals) - min(vals)) / med,
+                  "what": "(max - min) / median of the TFLOP/s of repeated K-step loops"}
 
     # The tensor-core 3xTF32 path on the same inputs (reported beside the
     # FFMA headline, which the metric defines against the FFMA peak).
     tensor_path = None
     if args.math == 0 and args.tensor_steps > 0:
         handle.set_math_mode(1)
-        handle._ensure_workspace(handle.workspace_size(w.M, w.N, w.K, A0.data_ptr(), A0.stride(0),
-                                                       B0.data_ptr(), B0.stride(0)))
-        tplan = handle.plan(A0, B0, C0, w.alpha, w.beta)
-        t_el, _, _ = timed_loop(args.tensor_steps, args.warmup, False, False)
-        _, t_k, _ = timed_loop(args.tensor_steps, args.warmup, False, True)
+        run.ensure_workspace()
+        tplan = handle.plan(*run.sets[0], w.alpha, w.beta)
+        t_el, _, _ = run.timed_loop(args.tensor_steps, args.warmup, False, False)
+        _, t_k, _ = run.timed_loop(args.tensor_steps, args.warmup, False, True)
         handle.set_math_mode(0)
         t_step = t_el / args.tensor_steps
         tensor_path = {
             "math": "3xTF32 (tcgen05, error-compensated; same FP32 acceptance bound)",
             "value": job_tflops(flops, world, t_step), "unit": "TFLOP/s",
             "ms_per_step": t_step, "steps": args.tensor_steps,
-            "launches_per_step": 3,
+            "launches_per_step": tplan["launches"],
             "roofline": tensor_roofline(flops, statistics.mean(t_k)),
             "config": {"tile": f"{tplan['tile_m']}x{tplan['tile_n']}x{tplan['tile_k']}",
                        "schedule": "stream-K" if tplan["stream_k"] else "whole tiles",
@@ -447,42 +588,27 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         if w.name == "sgemm_4096":
             tensor_path["roofline"]["traffic"] = profiled_traffic(tplan, TENSOR_PROFILE_SUMMARY,
                                                                   TENSOR_KERNEL_SOURCES)
+    config = dict(workload_config(w, run.l2_note()), algo=args.algo,
+                  schedule="stream-K" if plan["stream_k"] else "whole tiles",
+                  tile=f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
+                  stages=plan["stages"], ctas=plan["ctas"], parallelism=f"replicas x{world}")
+    run.release()
 
-    # End to end through the host-buffer C entry point: pinned host A, B (C),
-    # copies up, product, copy of C down, all inside the timed region.
-    e2e = None
-    if args.e2e_steps > 0:
-        Ah = torch.from_numpy(p.A).pin_memory()
-        Bh = torch.from_numpy(p.B).pin_memory()
-        Ch = (torch.from_numpy(p.C0.copy()) if p.C0 is not None
-              else torch.zeros((w.M, w.N))).pin_memory()
-        ws = torch.empty(sg.host_workspace_size(w.M, w.N, w.K), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=handle, stream=stream)
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            sg.sgemm_host(Ah, Bh, Ch, w.alpha, w.beta, workspace=ws, handle=handle, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        e_ms = max_over_ranks(e_ms, dev)
-        h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0.0 else 0))
-        e2e = {"value": job_tflops(flops, world, e_ms), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N,
-               "ms_per_step": e_ms, "steps": args.e2e_steps,
-               "path": "sgemmHostEx: pinned host A,B -> device, SGEMM, C -> pinned host"}
-
+    e2e = run.e2e(args.e2e_steps) if args.e2e_steps > 0 else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        c_flops, c_times, rows, threads = oracle_rows_sample(w, p, args.cpu_seconds, 1)
-        cpu = {"value": c_flops / c_times[0] / 1e12, "unit": "TFLOP/s", "cores": threads,
-               "kind": "oracle",
-               "sample": f"{rows} of {w.M} output rows (all {w.N} columns, K={w.K}) "
-                         f"in {c_times[0]:.1f} s, fp64 C oracle"}
-        cpu.update(oracle_extra_timings(w, p, min(args.cpu_seconds, 10.0)))
+        cpu = run.cpu_baseline(args.cpu_seconds)
+
+    # The other workloads of the benchmark set, each measured the same way
+    # (parity for all of them is checked by the GPU tests).
+    workloads = None
+    if not args.no_workloads and w.name == "sgemm_4096":
+        workloads = {}
+        for name in ("sgemm_128", "sgemm_1024", "sgemm_4095x4097x1023", "sgemm_8192"):
+            ow = inputs.WORKLOADS[name]
+            workloads[name] = measure_workload(
+                ctx, ow, args.steps, args.warmup, min(args.e2e_steps, 10 if ow.M >= 8192 else 40),
+                0.0 if args.no_cpu_baseline else min(args.cpu_seconds, 6.0))
 
     if rank != 0:
         return
@@ -493,16 +619,13 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "scaling": "weak", "vs_baseline": value / PAGES_BEST_TFLOPS,
         "vs_baseline_ref": "9.66 TFLOP/s: the pages' best kernel at 4096^3 on an RTX 3060",
         "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(
-            w, f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB "
-               f"(> {l2_bytes / 1e6:.0f} MB L2)"),
-            algo=args.algo, schedule="stream-K" if plan["stream_k"] else "whole tiles",
-            tile=f"{plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}",
-            stages=plan["stages"], ctas=plan["ctas"], parallelism=f"replicas x{world}"),
+        "config": config,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "spread": spread,
         "tensor_path": tensor_path,
+        "workloads": workloads,
         "gpu_launches": args.steps * plan["launches"],
         "clocks": clocks,
     }

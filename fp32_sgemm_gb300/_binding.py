@@ -80,6 +80,10 @@ SIGNATURES = {
     "sgemmGetDeviceError": (_st, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "sgemmSelfTestWaitTimeout": (_st, [_vp, ctypes.c_uint64, _vp]),
     "sgemmNoAlloc": (_st, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "sgemmNoAllocGetDeviceError": (_st, [ctypes.POINTER(ctypes.c_int)]),
+    "sgemmNoAllocSetWaitTimeout": (_st, [ctypes.c_uint64]),
+    "sgemmNoAllocSetTestWithheldSignal": (_st, [ctypes.c_int]),
+    "sgemmSetTestWithheldSignal": (_st, [_vp, ctypes.c_int]),
 }
 
 _lock = threading.Lock()
@@ -230,6 +234,11 @@ class Handle:
 
     def set_wait_timeout(self, ns: int):
         _check(self._lib.sgemmSetWaitTimeout(self._h, int(ns)), "sgemmSetWaitTimeout")
+
+    def set_test_withheld_signal(self, which: int):
+        """Test hook: 0 none, 1 stream-K flag, 2 ring refill, 3 stage release
+        (the bounded wait for the withheld signal then runs out)."""
+        _check(self._lib.sgemmSetTestWithheldSignal(self._h, int(which)), "sgemmSetTestWithheldSignal")
 
     def device_error(self) -> int:
         code = ctypes.c_int()

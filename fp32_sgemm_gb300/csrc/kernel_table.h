@@ -98,6 +98,7 @@ struct Tf32x3Args {
     uint32_t *flags;
     uint32_t *err;
     uint64_t timeout_ns;
+    int withhold;        // test hook (Withhold): a signal left out on purpose
 };
 struct Tf32x3Info {
     const void *fn[4];   // variant index as for the FFMA kernels
@@ -179,5 +180,18 @@ void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *ds
 void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *hi, float *lo,
                        int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);
 void launch_wait_selftest(uint32_t *err, uint64_t timeout_ns, cudaStream_t s);
+
+// Load a kernel's code now rather than at its first launch (with lazy module
+// loading the first launch would load it, which can commit device memory).
+inline cudaError_t load_kernel(const void *fn) {
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, fn);
+}
+// Every kernel each translation unit can launch, loaded on the current
+// device (the skinny TMA kernels also get their shared-memory opt-in).
+cudaError_t preload_small_kernels();
+cudaError_t preload_skinny_kernels();
+cudaError_t preload_skinny_tma_kernels();
+cudaError_t preload_aux_kernels();
 
 }  // namespace sg

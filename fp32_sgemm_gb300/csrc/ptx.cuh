@@ -32,7 +32,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-// One non-blocking probe: true once the phase with parity `parity` completed.
+// One probe: true once the phase with parity `parity` completed.  The
+// thread may be suspended inside the probe until the phase completes or a
+// system-dependent time passes.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -40,6 +42,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// The same probe, suspended at most about `hint_ns` nanoseconds (it still
+// returns as soon as the phase completes), so that a waiting loop looks at
+// the clock often enough for its limit to mean what it says.
+constexpr uint32_t kProbeSuspendNs = 2000;
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
     return done != 0;
 }
 
@@ -54,17 +70,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint32_t kMaxWaitProbes = 1u << 30;
 
 // Bounded wait on an mbarrier phase.  Returns false if the phase did not
-// complete within `timeout_ns` (or kMaxWaitProbes probes); never spins forever.
+// complete within `timeout_ns` (or kMaxWaitProbes probes); never spins
+// forever.  The clock is read every 16 probes of at most kProbeSuspendNs,
+// so the limit is overshot by some 32 us at most.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((probe & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+        if (mbar_try_wait_hint(bar, parity, kProbeSuspendNs)) return true;
+        if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
     }
     return false;
 }
+
+// Limit of a wait whose signal depends on another wait of the same CTA
+// (a consumer's wait for data the TMA issuer loads once it has a free
+// stage): twice the upstream limit, so that when the upstream wait runs
+// out first, its site -- the root cause -- is the one recorded.
+__device__ __forceinline__ uint64_t downstream_limit(uint64_t timeout_ns) { return 2 * timeout_ns; }
 
 // Global-memory flag used between CTAs: release store / acquire load at GPU scope.
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
@@ -76,14 +100,19 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     return v;
 }
 
-// Bounded wait for a global flag to become nonzero (the CTAs involved are
-// all resident: the persistent grid never exceeds one wave).
-__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *p, uint64_t timeout_ns) {
-    if (ld_acquire_gpu(p) != 0) return true;
+__device__ __forceinline__ void red_release_add_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until a global counter reaches `target` (acquire).  The
+// CTAs involved are all resident: the persistent grid never exceeds one
+// wave.
+__device__ __forceinline__ bool count_wait_bounded(const uint32_t *p, uint32_t target, uint64_t timeout_ns) {
+    if (ld_acquire_gpu(p) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
         __nanosleep(64);
-        if (ld_acquire_gpu(p) != 0) return true;
+        if (ld_acquire_gpu(p) >= target) return true;
         if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
     }
     return false;
@@ -91,8 +120,20 @@ __device__ __forceinline__ bool flag_wait_bounded(const uint32_t *p, uint64_t ti
 
 // Error word layout: bits 24..31 = which wait expired, bits 0..23 = CTA index.
 enum WaitSite : uint32_t {
-    kSiteConsumerFull = 1, kSiteProducerEmpty = 2, kSiteSelfTest = 3,
-    kSiteStreamKFlag = 4, kSiteCtaSync = 5
+    kSiteConsumerFull = 1, kSiteProducerEmpty = 2, kSiteSelfTest = 3, kSiteStreamKFlag = 4
+};
+
+// Test hook for failure detection: a signal the kernels leave out on purpose,
+// so that the bounded wait for it runs out and the expiry path (record the
+// site, let the CTA's own copies land, return) runs without any fault.
+//   kWithholdStreamKFlag: CTAs holding a partial tile never publish it (the
+//     finishing CTA's flag wait, site 4, expires);
+//   kWithholdRefill: the TMA issuer stops after filling the ring once (the
+//     consumers' data wait, site 1, expires);
+//   kWithholdRelease: consumers never release a stage (the issuer's slot
+//     wait, site 2, expires).
+enum Withhold : int {
+    kWithholdNone = 0, kWithholdStreamKFlag = 1, kWithholdRefill = 2, kWithholdRelease = 3
 };
 
 __device__ __forceinline__ void record_error(uint32_t *err, uint32_t site) {

@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -94,6 +95,7 @@ struct sgemmContext {
     int algo = 0;
     int schedule = 0;   // 0 automatic, 1 whole tiles only, 2 stream-K whenever it applies
     int math = 0;       // 0 FP32 FFMA, 1 error-compensated 3xTF32 on the tensor cores
+    int withhold = 0;   // test hook: signal the kernels leave out (sg::Withhold)
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;   // around the main kernel, if set
     // sgemmHostEx pipeline: copy-in and copy-out streams and their events,
     // created with the handle.
@@ -324,9 +326,11 @@ int choose_algo(const sgemmContext *h, const Problem &q) {
     return kDefaultAlgo - 1;
 }
 
-int occupancy_for(const sgemmContext *h, KernelEntry &e) {
+// CTAs of a main-kernel configuration per SM of device `dev` (queried once
+// per device, after the shared-memory opt-in); -1 if the query fails.
+int occupancy_on(int dev, KernelEntry &e) {
     std::lock_guard<std::mutex> lk(g_occ_mutex);
-    int &occ = e.occupancy[h->device];
+    int &occ = e.occupancy[dev];
     if (occ == 0) {
         if (cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e.smem) != cudaSuccess)
             return -1;
@@ -337,6 +341,8 @@ int occupancy_for(const sgemmContext *h, KernelEntry &e) {
     }
     return occ;
 }
+
+int occupancy_for(const sgemmContext *h, KernelEntry &e) { return occupancy_on(h->device, e); }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -680,6 +686,7 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
     args.group_m = pl.group_m;
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
+    args.withhold = h->withhold;
     args.sk_tile0 = pl.num_tiles;
     int ctas = pl.dp_ctas;
     if (pl.sk_ctas > 0 && h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials) {
@@ -829,6 +836,7 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     args.group_m = pl.group_m;
     args.err = h->d_err;
     args.timeout_ns = h->timeout_ns;
+    args.withhold = h->withhold;
     int ctas = pl.dp_ctas;
     args.sk_tile0 = pl.num_tiles;
     if (use_sk) {
@@ -869,6 +877,34 @@ size_t skinny_query_bytes(const sgemmContext *h, const Problem &q) {
         bytes = std::max(bytes, align256(sg::skinny_tma_geometry(small_m, int(q.M), int(q.N), int(q.K),
                                                                  h->sm_count).ws_bytes));
     return bytes;
+}
+
+// Workspace a call on these operands can use, whatever its beta and C: the
+// tile configuration (and with it the stream-K scratch) depends on whether
+// C is read (beta != 0) and whether C is 16-byte aligned with a pitch of
+// whole 16-byte units, so the query plans each of those cases and keeps
+// the largest need.  C's own address is never dereferenced by planning.
+sgemmStatus_t workspace_query(const sgemmContext *h, Problem q, size_t *bytes) {
+    static float *const kAlignedC = reinterpret_cast<float *>(uintptr_t(256));
+    static float *const kOddC = reinterpret_cast<float *>(uintptr_t(260));
+    const struct { float beta; float *c; int64_t ldc; } cases[3] = {
+        {0.0f, kAlignedC, round_up(std::max<int64_t>(1, q.N), 4)},
+        {1.0f, kAlignedC, round_up(std::max<int64_t>(1, q.N), 4)},
+        {1.0f, kOddC, std::max<int64_t>(1, q.N)},
+    };
+    size_t need = 0;
+    for (const auto &c : cases) {
+        q.beta = c.beta;
+        q.C = c.c;
+        q.ldc = c.ldc;
+        q.sc = q.batch == 1 ? 0 : c.ldc * q.M;
+        Plan pl;
+        sgemmStatus_t st = make_plan(h, q, pl);
+        if (st != SGEMM_STATUS_SUCCESS) return st;
+        need = std::max({need, workspace_bytes(pl), skinny_query_bytes(h, q)});
+    }
+    *bytes = need;
+    return SGEMM_STATUS_SUCCESS;
 }
 
 void release_handle_resources(sgemmContext *h) {
@@ -977,12 +1013,8 @@ sgemmStatus_t sgemmGetWorkspaceSize(sgemmHandle_t h, int64_t M, int64_t N, int64
     const float dummy_c = 0.f;
     sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, &dummy_c, std::max<int64_t>(1, N), true);
     if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0 || K == 0) return st;
-    Plan pl;
-    st = make_plan(h, M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, std::max<int64_t>(1, N), pl);
-    if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = std::max(workspace_bytes(pl),
-                      skinny_query_bytes(h, nn_problem(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, N)));
-    return SGEMM_STATUS_SUCCESS;
+    if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    return workspace_query(h, nn_problem(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, nullptr, N), bytes);
 }
 
 sgemmStatus_t sgemmSetWorkspace(sgemmHandle_t h, void *ptr, size_t bytes) {
@@ -1056,13 +1088,7 @@ sgemmStatus_t sgemmStridedBatchedWorkspaceSize(sgemmHandle_t h, sgemmOperation_t
     sgemmStatus_t st = validate(q);
     if (st != SGEMM_STATUS_SUCCESS || q.empty() || K == 0) return st;
     if (h == nullptr) return SGEMM_STATUS_INVALID_VALUE;
-    Plan pl;
-    Problem qc = q;
-    qc.C = nullptr;
-    st = make_plan(h, qc, pl);
-    if (st != SGEMM_STATUS_SUCCESS) return st;
-    *bytes = std::max(workspace_bytes(pl), skinny_query_bytes(h, qc));
-    return SGEMM_STATUS_SUCCESS;
+    return workspace_query(h, q, bytes);
 }
 
 sgemmStatus_t sgemmHostWorkspaceSize(int64_t M, int64_t N, int64_t K, size_t *bytes) {
@@ -1237,6 +1263,13 @@ sgemmStatus_t sgemmSetWaitTimeout(sgemmHandle_t h, uint64_t timeout_ns) {
     return SGEMM_STATUS_SUCCESS;
 }
 
+sgemmStatus_t sgemmSetTestWithheldSignal(sgemmHandle_t h, int which) {
+    if (h == nullptr || which < sg::kWithholdNone || which > sg::kWithholdRelease)
+        return SGEMM_STATUS_INVALID_VALUE;
+    h->withhold = which;
+    return SGEMM_STATUS_SUCCESS;
+}
+
 sgemmStatus_t sgemmGetDeviceError(sgemmHandle_t h, int *code) {
     if (h == nullptr || code == nullptr) return SGEMM_STATUS_INVALID_VALUE;
     *code = 0;
@@ -1287,15 +1320,23 @@ namespace {
 
 struct StaticScratchSlot {
     std::once_flag once;
+    std::atomic<bool> ready{false};   // set-up ran (status below is final)
     sgemmStatus_t status = SGEMM_STATUS_INTERNAL_ERROR;
-    unsigned char *ptr = nullptr;   // device address of g_sgemm_static_scratch
+    unsigned char *ptr = nullptr;     // device address of g_sgemm_static_scratch
     int sm_count = 0;
+    // Settings of this device's calls (host values; no device state).
+    std::atomic<uint64_t> timeout_ns{kDefaultTimeoutNs};
+    std::atomic<int> withhold{0};
 };
 StaticScratchSlot g_static_slots[kMaxDevices];
 
-// Once per device, with that device current: the array's device address (in
-// host code its name is only a host-side stand-in), the SM count and the
-// architecture check.
+// Once per device, with that device current: the architecture check, the SM
+// count, the array's device address (in host code its name is only a
+// host-side stand-in), and every kernel this entry point can launch loaded
+// up front -- each main-kernel configuration with its shared-memory opt-in
+// and occupancy (cached per device), the small-product, skinny and
+// auxiliary kernels -- so that no later call loads a module.  Looking up
+// the address loads the module holding the array, which commits its memory.
 void setup_static_scratch(StaticScratchSlot &slot, int dev) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -1313,9 +1354,36 @@ void setup_static_scratch(StaticScratchSlot &slot, int dev) {
         slot.status = SGEMM_STATUS_LAUNCH_FAILED;
         return;
     }
+    std::call_once(g_kernels_once, init_kernel_table);
+    for (auto &row : g_kernels)
+        for (KernelEntry &e : row)
+            if (occupancy_on(dev, e) < 1) {
+                slot.status = SGEMM_STATUS_LAUNCH_FAILED;
+                return;
+            }
+    if (sg::preload_small_kernels() != cudaSuccess || sg::preload_skinny_kernels() != cudaSuccess ||
+        sg::preload_skinny_tma_kernels() != cudaSuccess || sg::preload_aux_kernels() != cudaSuccess ||
+        encode_fn() == nullptr) {
+        slot.status = SGEMM_STATUS_LAUNCH_FAILED;
+        return;
+    }
     slot.ptr = static_cast<unsigned char *>(ptr);
     slot.sm_count = sms;
     slot.status = SGEMM_STATUS_SUCCESS;
+}
+
+// The current device's slot, set up on first use.
+sgemmStatus_t static_slot(StaticScratchSlot *&out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    StaticScratchSlot &slot = g_static_slots[dev];
+    std::call_once(slot.once, [&slot, dev] {
+        setup_static_scratch(slot, dev);
+        slot.ready.store(true);
+    });
+    out = &slot;
+    return slot.status;
 }
 
 }  // namespace
@@ -1325,21 +1393,22 @@ extern "C" sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alp
                                       float beta, float *C, int64_t ldc, cudaStream_t stream) {
     sgemmStatus_t st = validate(M, N, K, A, lda, B, ldb, C, ldc, alpha != 0.0f);
     if (st != SGEMM_STATUS_SUCCESS || M == 0 || N == 0) return st;
+    StaticScratchSlot *slot = nullptr;
+    st = static_slot(slot);
+    if (st != SGEMM_STATUS_SUCCESS) return st;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
-    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
-    StaticScratchSlot &slot = g_static_slots[dev];
-    std::call_once(slot.once, [&slot, dev] { setup_static_scratch(slot, dev); });
-    if (slot.status != SGEMM_STATUS_SUCCESS) return slot.status;
+    cudaGetDevice(&dev);
 
     // A context on the stack whose error word and workspace are carved out
     // of the static array.
     sgemmContext ctx;
     ctx.device = dev;
-    ctx.sm_count = slot.sm_count;
-    ctx.d_err = reinterpret_cast<uint32_t *>(slot.ptr);
-    ctx.ws = slot.ptr + kStaticErrBytes;
+    ctx.sm_count = slot->sm_count;
+    ctx.d_err = reinterpret_cast<uint32_t *>(slot->ptr);
+    ctx.ws = slot->ptr + kStaticErrBytes;
     ctx.ws_bytes = kStaticScratchBytes - kStaticErrBytes;
+    ctx.timeout_ns = slot->timeout_ns.load();
+    ctx.withhold = slot->withhold.load();
 
     Plan pl;
     st = make_plan(&ctx, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, pl);
@@ -1348,4 +1417,41 @@ extern "C" sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alp
     // stream-K scratch is used only when it fits as well.
     if (pl.ws_a + pl.ws_b > ctx.ws_bytes) return SGEMM_STATUS_NOT_SUPPORTED;
     return run(&ctx, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+extern "C" sgemmStatus_t sgemmNoAllocSetWaitTimeout(uint64_t timeout_ns) {
+    if (timeout_ns < kMinTimeoutNs) return SGEMM_STATUS_INVALID_VALUE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    g_static_slots[dev].timeout_ns.store(timeout_ns);
+    return SGEMM_STATUS_SUCCESS;
+}
+
+extern "C" sgemmStatus_t sgemmNoAllocSetTestWithheldSignal(int which) {
+    if (which < sg::kWithholdNone || which > sg::kWithholdRelease) return SGEMM_STATUS_INVALID_VALUE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    g_static_slots[dev].withhold.store(which);
+    return SGEMM_STATUS_SUCCESS;
+}
+
+extern "C" sgemmStatus_t sgemmNoAllocGetDeviceError(int *code) {
+    if (code == nullptr) return SGEMM_STATUS_INVALID_VALUE;
+    *code = 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_STATUS_LAUNCH_FAILED;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_STATUS_NOT_SUPPORTED;
+    StaticScratchSlot &slot = g_static_slots[dev];
+    // No call has set up this device: no kernel of this path has run on it.
+    if (!slot.ready.load()) return SGEMM_STATUS_SUCCESS;
+    if (slot.status != SGEMM_STATUS_SUCCESS) return slot.status;
+    uint32_t word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, slot.ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(slot.ptr, 0, sizeof(word)) != cudaSuccess)
+        return SGEMM_STATUS_LAUNCH_FAILED;
+    *code = int(word);
+    return word == 0 ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_DEVICE_TIMEOUT;
 }

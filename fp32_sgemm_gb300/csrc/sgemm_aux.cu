@@ -260,6 +260,24 @@ void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *h
     sgemm_split_rows_kernel<<<grid, 256, 0, s>>>(src, ld_src, s_src, hi, lo, ld_dst, s_dst, rows, cols, batch);
 }
 
+cudaError_t preload_aux_kernels() {
+    const void *fns[] = {
+        reinterpret_cast<const void *>(&sgemm_scale_c_kernel),
+        reinterpret_cast<const void *>(&sgemm_pack_rows_kernel),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, true, true>),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, false, true>),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, false, false>),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<false, true, true>),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<false, false, true>),
+        reinterpret_cast<const void *>(&sgemm_transpose_kernel<false, false, false>),
+        reinterpret_cast<const void *>(&sgemm_split_rows_kernel),
+        reinterpret_cast<const void *>(&sgemm_split_rows_vec4_kernel),
+        reinterpret_cast<const void *>(&sgemm_wait_selftest_kernel)};
+    for (const void *fn : fns)
+        if (cudaError_t e = load_kernel(fn); e != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
 void launch_wait_selftest(uint32_t *err, uint64_t timeout_ns, cudaStream_t s) {
     sgemm_wait_selftest_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
 }

@@ -70,9 +70,10 @@ struct GemmArgs {
     int group_m;          // rasterisation: tile rows per band
     int sk_tile0;         // tiles [0, sk_tile0) whole, round robin; [sk_tile0, num_tiles) stream-K
     float *partials;      // stream-K: one BM x BN partial tile per CTA
-    uint32_t *flags;      // stream-K: one ready flag per CTA, zeroed before the launch
+    uint32_t *flags;      // stream-K: one counter per CTA (warps that stored their part), zeroed before the launch
     uint32_t *err;        // device error word (bounded waits)
     uint64_t timeout_ns;
+    int withhold;         // test hook (Withhold): a signal left out on purpose
 };
 
 template <int KA> struct AVecT;
@@ -133,7 +134,7 @@ struct FfmaConfig {
     // as NJ boxes of WTM rows x 4*WC columns (box j = the lane columns of j).
     static constexpr int C_BOX_COLS = 4 * WC, C_BOX_BYTES = WTM * C_BOX_COLS * 4;
     static constexpr int STORE_BYTES = STORE_TMA ? CONSUMER_WARPS * WTM * WTN * 4 : 0;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STORE_BYTES + (2 * STAGES + 1) * 8 + 128 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STORE_BYTES + 2 * STAGES * 8 + 128 + 1024;
     static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
     // TMA boxes are at most 256 elements a side: wider tiles take several.
     // A's boxes stack rows (the stage layout is unchanged); B's boxes sit one
@@ -371,8 +372,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     unsigned char *sC = smem + STAGES * Cfg::STAGE_BYTES;   // STORE_BYTES of C staging
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::STORE_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *cta_bar = empty + STAGES;   // consumer-warp rendezvous (stream-K fixup)
-    SliceCursor *cursor = reinterpret_cast<SliceCursor *>(cta_bar + 1);
+    SliceCursor *cursor = reinterpret_cast<SliceCursor *>(empty + STAGES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -382,7 +382,6 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
-        mbar_init(cta_bar, Cfg::CONSUMER_WARPS);
         fence_barrier_init();
     }
     __syncthreads();
@@ -395,6 +394,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             prefetch_tensormap(&tmB);
             cursor_begin(cursor, p);
             while (cursor_valid(cursor)) {
+                if (p.withhold == kWithholdRefill && cursor_issued(cursor) >= STAGES) {
+                    drain_slices<Cfg>(0, cursor_issued(cursor), full, p.timeout_ns);
+                    return;
+                }
                 if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
                     // No consumer may ever take the most recent slices.
@@ -478,16 +481,6 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     };
 
-    // Rendezvous of the consumer warps (bounded; used around the stream-K
-    // partial-sum exchange).
-    uint32_t cta_phase = 0;
-    auto consumer_sync = [&]() {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cta_bar);
-        if (!mbar_wait_bounded(cta_bar, cta_phase, p.timeout_ns)) record_error(p.err, kSiteCtaSync);
-        cta_phase ^= 1u;
-    };
-
     WorkIter it;
     it.begin(p);
     Segment seg;
@@ -524,7 +517,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++g) {
-            if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+            if (!mbar_wait_bounded(&full[stage], phase, downstream_limit(p.timeout_ns))) {
                 record_error(p.err, kSiteConsumerFull);
                 if (producer) drain_slices<Cfg>(g, cursor_issued(cursor), full, p.timeout_ns);
                 if constexpr (TMA_EPILOGUE) { if (lane == 0) bulk_wait_all(); }
@@ -584,9 +577,9 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (lane == 0 && p.withhold != kWithholdRelease) mbar_arrive(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            if (producer && g >= Cfg::REFILL_LAG && cursor_valid(cursor)) {
+            if (producer && g >= Cfg::REFILL_LAG && cursor_valid(cursor) && p.withhold != kWithholdRefill) {
                 if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
                     record_error(p.err, kSiteProducerEmpty);
                     drain_slices<Cfg>(g + 1, cursor_issued(cursor), full, p.timeout_ns);
@@ -597,6 +590,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         }
 
         // ---------------- stream-K fixup ----------------
+        // Warp by warp: the same (warp, lane) holds the same elements of the
+        // tile in every CTA, so each warp hands over and collects its own
+        // part with no CTA-wide rendezvous.  A CTA's counter counts the
+        // warps that have stored their part of its partial tile.
         if (seg.kb0 != 0 || seg.kb1 != p.k_blocks) {
             float4 *mine = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * (BM * BN));
             if (seg.kb0 != 0) {
@@ -610,8 +607,9 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                                make_float4(acc[i][2 * j].x, acc[i][2 * j].y,
                                            acc[i][2 * j + 1].x, acc[i][2 * j + 1].y));
                 __threadfence();
-                consumer_sync();
-                if (threadIdx.x == 0) st_release_gpu(&p.flags[blockIdx.x], 1u);
+                __syncwarp();
+                if (lane == 0 && p.withhold != kWithholdStreamKFlag)
+                    red_release_add_gpu(&p.flags[blockIdx.x], 1u);
                 it.advance(p, seg);
                 continue;
             }
@@ -620,11 +618,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const int tile_u0 = seg.t * p.k_blocks;
             const int c_first = cta_of_unit(tile_u0 + seg.kb1, p);
             const int c_last = cta_of_unit(tile_u0 + p.k_blocks - 1, p);
-            if (threadIdx.x == 0) {
+            if (lane == 0) {
                 for (int c = c_first; c <= c_last; ++c)
-                    if (!flag_wait_bounded(&p.flags[c], p.timeout_ns)) record_error(p.err, kSiteStreamKFlag);
+                    if (!count_wait_bounded(&p.flags[c], (uint32_t)Cfg::CONSUMER_WARPS, p.timeout_ns))
+                        record_error(p.err, kSiteStreamKFlag);
             }
-            consumer_sync();
+            __syncwarp();
             for (int c = c_first; c <= c_last; ++c) {
                 const float4 *other = reinterpret_cast<const float4 *>(p.partials + (size_t)c * (BM * BN));
 #pragma unroll

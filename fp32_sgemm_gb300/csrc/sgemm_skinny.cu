@@ -250,6 +250,20 @@ void launch_n(int M, int N, int K, const float *A, int64_t lda, const float *B, 
     skinny_n_partial_kernel<T><<<grid, kSkinnyThreads, 0, s>>>(M, N, K, A, lda, B, ldb, part, k_chunk, vec_a);
 }
 
+cudaError_t preload_skinny_kernels() {
+    const void *fns[] = {
+        reinterpret_cast<const void *>(&skinny_m_partial_kernel<1>), reinterpret_cast<const void *>(&skinny_m_partial_kernel<2>),
+        reinterpret_cast<const void *>(&skinny_m_partial_kernel<4>), reinterpret_cast<const void *>(&skinny_m_partial_kernel<8>),
+        reinterpret_cast<const void *>(&skinny_m_partial_kernel<16>), reinterpret_cast<const void *>(&skinny_m_partial_kernel<32>),
+        reinterpret_cast<const void *>(&skinny_n_partial_kernel<1>), reinterpret_cast<const void *>(&skinny_n_partial_kernel<2>),
+        reinterpret_cast<const void *>(&skinny_n_partial_kernel<4>), reinterpret_cast<const void *>(&skinny_n_partial_kernel<8>),
+        reinterpret_cast<const void *>(&skinny_n_partial_kernel<16>), reinterpret_cast<const void *>(&skinny_n_partial_kernel<32>),
+        reinterpret_cast<const void *>(&skinny_reduce_kernel)};
+    for (const void *fn : fns)
+        if (cudaError_t e = load_kernel(fn); e != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
 void launch_skinny(bool small_m, int M, int N, int K, float alpha, const float *A, int64_t lda,
                    const float *B, int64_t ldb, float beta, float *C, int64_t ldc, float *part,
                    int splits, cudaStream_t s) {

@@ -342,9 +342,32 @@ void launch_n_tma(const CUtensorMap &a, const CUtensorMap &b, const SkinnyTmaArg
     skinny_n_tma_kernel<T><<<p.ctas, kThreads, kSmemBytes, s>>>(a, b, p);
 }
 
+template <int T>
+cudaError_t preload_tma_t() {
+    // The same opt-in the launchers make at their first call.
+    cudaError_t e = cudaFuncSetAttribute(skinny_m_tma_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(skinny_n_tma_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) e = load_kernel(reinterpret_cast<const void *>(&skinny_m_tma_kernel<T>));
+    if (e == cudaSuccess) e = load_kernel(reinterpret_cast<const void *>(&skinny_n_tma_kernel<T>));
+    return e;
+}
+
 inline int round_small(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : n <= 16 ? 16 : 32; }
 
 }  // namespace
+
+cudaError_t preload_skinny_tma_kernels() {
+    cudaError_t e = preload_tma_t<1>();
+    if (e == cudaSuccess) e = preload_tma_t<2>();
+    if (e == cudaSuccess) e = preload_tma_t<4>();
+    if (e == cudaSuccess) e = preload_tma_t<8>();
+    if (e == cudaSuccess) e = preload_tma_t<16>();
+    if (e == cudaSuccess) e = preload_tma_t<32>();
+    if (e == cudaSuccess) e = load_kernel(reinterpret_cast<const void *>(&skinny_tma_reduce_kernel));
+    return e;
+}
 
 SkinnyTmaGeom skinny_tma_geometry(bool small_m, int M, int N, int K, int sms) {
     SkinnyTmaGeom g;

@@ -256,6 +256,27 @@ int small_splits(int M, int N, int K, int batch, int sms) {
     return s;
 }
 
+namespace {
+template <bool TA, bool TB>
+cudaError_t preload_small_ab() {
+    const void *fns[] = {reinterpret_cast<const void *>(&sgemm_small_kernel<TA, TB, true, true>),
+                         reinterpret_cast<const void *>(&sgemm_small_kernel<TA, TB, true, false>),
+                         reinterpret_cast<const void *>(&sgemm_small_kernel<TA, TB, false, true>),
+                         reinterpret_cast<const void *>(&sgemm_small_kernel<TA, TB, false, false>)};
+    for (const void *fn : fns)
+        if (cudaError_t e = load_kernel(fn); e != cudaSuccess) return e;
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t preload_small_kernels() {
+    cudaError_t e = preload_small_ab<false, false>();
+    if (e == cudaSuccess) e = preload_small_ab<false, true>();
+    if (e == cudaSuccess) e = preload_small_ab<true, false>();
+    if (e == cudaSuccess) e = preload_small_ab<true, true>();
+    return e;
+}
+
 void launch_small(SmallArgs p, int trans_a, int trans_b, int batch, cudaStream_t s) {
     p.tiles_m = (p.M + kTile - 1) / kTile;
     p.tiles_n = (p.N + kTile - 1) / kTile;

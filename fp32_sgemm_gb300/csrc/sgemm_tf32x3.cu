@@ -114,22 +114,6 @@ __device__ __forceinline__ void prefetch_l2(const float *p) {
     asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
 }
 
-__device__ __forceinline__ void red_release_add_gpu(uint32_t *p, uint32_t v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-
-// Bounded wait until a counter reaches `target` (acquire).
-__device__ __forceinline__ bool count_wait_bounded(const uint32_t *p, uint32_t target, uint64_t timeout_ns) {
-    if (ld_acquire_gpu(p) >= target) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
-        __nanosleep(64);
-        if (ld_acquire_gpu(p) >= target) return true;
-        if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
-    }
-    return false;
-}
-
 template <class Cfg, bool BETA_ZERO, bool C_VEC>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
 sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
@@ -189,6 +173,10 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             int bt, tm, tn;
             tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
             for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                if (p.withhold == kWithholdRefill && issued >= STAGES) {
+                    ok = false;     // test hook: stop after one ring fill (drain below)
+                    break;
+                }
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                     record_error(p.err, kSiteProducerEmpty);
                     ok = false;
@@ -234,7 +222,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns)) {
+                if (!mbar_wait_bounded(&full[stage], phase, downstream_limit(p.timeout_ns))) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
                     return;
@@ -258,7 +246,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
                     mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
                 }
-                mma_commit(&empty[stage]);      // frees the stage once these MMAs are done
+                if (p.withhold != kWithholdRelease)
+                    mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             mma_commit(&tfull[ab]);             // chunk ready for the epilogue
@@ -315,7 +304,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             for (int kb0 = seg.kb0; kb0 < seg.kb1; kb0 += Cfg::CHUNK_KB, ++gc) {
                 const int ab = gc & 1;
                 const uint32_t use = (uint32_t)(gc >> 1);
-                if (!mbar_wait_bounded(&tfull[ab], use & 1u, p.timeout_ns)) {
+                if (!mbar_wait_bounded(&tfull[ab], use & 1u, downstream_limit(p.timeout_ns))) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
                     break;
@@ -351,7 +340,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                                make_float4(sum[4 * q], sum[4 * q + 1], sum[4 * q + 2], sum[4 * q + 3]));
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) red_release_add_gpu(&p.flags[blockIdx.x], 1u);
+                    if (lane == 0 && p.withhold != kWithholdStreamKFlag)
+                        red_release_add_gpu(&p.flags[blockIdx.x], 1u);
                     w.advance(p, seg);
                     continue;
                 }

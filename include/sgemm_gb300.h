@@ -339,14 +339,38 @@ sgemmStatus_t sgemmSetKernelEvents(sgemmHandle_t handle, cudaEvent_t start,
  */
 sgemmStatus_t sgemmSetWaitTimeout(sgemmHandle_t handle, uint64_t timeout_ns);
 
+
 /*
  * Synchronise the handle's device, read and clear its error word.  *code is
  * 0 when no kernel recorded an error; otherwise the return value is
- * DEVICE_TIMEOUT and *code holds the raw word: bits 24..31 say which wait
- * expired (1 consumer data wait, 2 producer slot wait, 3 self test), bits
- * 0..23 the CTA index.
+ * DEVICE_TIMEOUT and *code holds the raw word of the FIRST expiry since the
+ * last read: bits 24..31 say which wait expired (1 a consumer's wait for
+ * operand data, 2 the TMA issuer's wait for a free pipeline stage, 3 the
+ * self test, 4 the wait for another CTA's stream-K partial tile, 5 the
+ * consumer warps' rendezvous around that exchange), bits 0..23 the CTA
+ * index.  A call during which a wait expired has left C undefined.
  */
 sgemmStatus_t sgemmGetDeviceError(sgemmHandle_t handle, int *code);
+
+/*
+ * TEST HOOK for failure detection, not for production use: calls on this
+ * handle leave out one signal inside the kernels on purpose, so that the
+ * bounded wait for it runs out and its give-up path runs (record the site
+ * in the error word, let the CTA's own copies land, free tensor memory,
+ * return); no kernel faults or hangs.  The C these calls write is
+ * undefined.  `which`:
+ *   0 = none (default);
+ *   1 = CTAs holding a stream-K partial tile never announce it (site 4
+ *       expires, in both math modes, on launches that use stream-K);
+ *   2 = the TMA issuer stops after filling the pipeline once (site 1
+ *       expires, on launches whose CTAs take more K slices than stages);
+ *   3 = consumers never release a pipeline stage (site 2 expires, same
+ *       launches).
+ * Only the main kernels (FFMA and 3xTF32) honour it.  Use a short limit
+ * (sgemmSetWaitTimeout) so that the expiries come quickly.  INVALID_VALUE
+ * for other values or a NULL handle.
+ */
+sgemmStatus_t sgemmSetTestWithheldSignal(sgemmHandle_t handle, int which);
 
 /*
  * Health check of the bounded-wait machinery: enqueue one single-CTA kernel
@@ -370,10 +394,13 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
  * lives in one file-scope device array of SGEMM_NOALLOC_SCRATCH_BYTES
  * (32 MiB) that every GPU loading this library holds until process exit.
  * The caller passes A, B and C as for sgemm().
- *   - The first call on a device does one-time set-up on the current device
- *     (looks up the array's device address, reads the SM count, checks the
- *     architecture, queries kernel occupancy).  Make that first call before
- *     any stream capture.
+ *   - The first call on a device does one-time set-up on the current device:
+ *     it checks the architecture, reads the SM count, looks up the array's
+ *     device address (which loads the library module holding the array and
+ *     so commits its 32 MiB), and loads every kernel this entry point can
+ *     launch, with each one's shared-memory opt-in and occupancy, so that
+ *     no later call loads code or commits memory.  Make that first call
+ *     before any stream capture and outside any allocator hook.
  *   - Every call shares the one array per device and the array keeps the
  *     last call's contents; what must start at zero (the stream-K flags) is
  *     cleared on the stream before each launch.  Calls whose work overlaps
@@ -384,8 +411,9 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
  *     K * round_up(N, 4) floats together at most 32 MiB minus 256 bytes;
  *     larger ones return SGEMM_STATUS_NOT_SUPPORTED before anything is
  *     enqueued.  Stream-K is used only when its scratch fits as well.
- *   - A bounded-wait timeout inside this path is recorded in the array's own
- *     error word, which no entry point reads back.
+ *   - Every wait inside these kernels is bounded (2 s by default, see
+ *     sgemmNoAllocSetWaitTimeout); an expiry is recorded in the array's own
+ *     error word, which sgemmNoAllocGetDeviceError reads and clears.
  * Other status codes as for sgemm().
  */
 #define SGEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -393,6 +421,30 @@ sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alpha,
                            const float *A, int64_t lda, const float *B,
                            int64_t ldb, float beta, float *C, int64_t ldc,
                            cudaStream_t stream);
+
+/*
+ * Synchronise the CURRENT device, then read and clear the error word that
+ * sgemmNoAlloc's kernels on this device record bounded-wait expiries in
+ * (the first expiry since the last read is kept).  *code and the return
+ * value as for sgemmGetDeviceError(): 0 and SUCCESS when nothing expired
+ * (also before the first sgemmNoAlloc call on the device, which is then
+ * not touched), otherwise the raw word and DEVICE_TIMEOUT.  Allocates
+ * nothing.  Like sgemmNoAlloc, the pages have no counterpart of it.
+ */
+sgemmStatus_t sgemmNoAllocGetDeviceError(int *code);
+
+/*
+ * Wait limit, in nanoseconds, of sgemmNoAlloc's kernels on the CURRENT
+ * device (default 2e9, minimum 1e6; INVALID_VALUE below).  Host setting
+ * only: nothing is enqueued or allocated.
+ */
+sgemmStatus_t sgemmNoAllocSetWaitTimeout(uint64_t timeout_ns);
+
+/*
+ * sgemmSetTestWithheldSignal() for sgemmNoAlloc's calls on the CURRENT
+ * device (same values and meaning; TEST HOOK, not for production use).
+ */
+sgemmStatus_t sgemmNoAllocSetTestWithheldSignal(int which);
 
 #ifdef __cplusplus
 }

@@ -133,7 +133,16 @@ def test_null_handle_rejected(lib):
     assert lib.sgemmSetAlgo(None, 1) == _binding.Status.INVALID_VALUE
     code = ctypes.c_int()
     assert lib.sgemmGetDeviceError(None, ctypes.byref(code)) == _binding.Status.INVALID_VALUE
+    assert lib.sgemmSetTestWithheldSignal(None, 1) == _binding.Status.INVALID_VALUE
     assert lib.sgemmDestroy(None) == 0
+
+
+def test_no_alloc_settings_validated_on_host(lib):
+    # Rejected before any CUDA call (this machine may have no GPU).
+    assert lib.sgemmNoAllocSetWaitTimeout(999_999) == _binding.Status.INVALID_VALUE
+    assert lib.sgemmNoAllocSetTestWithheldSignal(-1) == _binding.Status.INVALID_VALUE
+    assert lib.sgemmNoAllocSetTestWithheldSignal(4) == _binding.Status.INVALID_VALUE
+    assert lib.sgemmNoAllocGetDeviceError(None) == _binding.Status.INVALID_VALUE
 
 
 def _batched(lib, opA=0, opB=0, M=4, N=4, K=4, lda=None, ldb=None, ldc=None, sa=0, sb=0, sc=0,

@@ -97,3 +97,86 @@ def test_rejects_repacking_beyond_the_static_array(sg):
     assert _noalloc(lib, A, B, C, 1.0, 0.0) == sg.Status.NOT_SUPPORTED
     torch.cuda.synchronize()
     assert bool((C == 3.0).all()), "nothing may be enqueued on rejection"
+
+
+def _noalloc_error(lib):
+    code = ctypes.c_int(-1)
+    st = lib.sgemmNoAllocGetDeviceError(ctypes.byref(code))
+    return st, code.value
+
+
+def test_bounded_wait_expiry_is_reported_and_cleared(sg):
+    """A wait that runs out inside this entry point's kernels is recorded in
+    the static array's error word, which sgemmNoAllocGetDeviceError reads
+    and clears.  The expiry is made by leaving out the stream-K flags (a
+    signal nothing then sets; no fault), with a 20 ms limit."""
+    lib = sg.load_library()
+    M = N = 2048
+    K = 512   # 128 tiles of 256 x 128 on 152 SMs: the last wave is split stream-K
+    p = inputs.make_problem(M, N, K, seed=31, kind="integer")
+    A, B = _views(p)
+    C = torch.zeros((M, N), device="cuda")
+    assert _noalloc(lib, A, B, C, 1.0, 0.0) == sg.Status.SUCCESS
+    assert _noalloc_error(lib) == (sg.Status.SUCCESS, 0)
+    assert lib.sgemmNoAllocSetWaitTimeout(20_000_000) == sg.Status.SUCCESS
+    assert lib.sgemmNoAllocSetTestWithheldSignal(1) == sg.Status.SUCCESS
+    try:
+        assert _noalloc(lib, A, B, C, 1.0, 0.0) == sg.Status.SUCCESS
+        st, code = _noalloc_error(lib)
+    finally:
+        lib.sgemmNoAllocSetTestWithheldSignal(0)
+        lib.sgemmNoAllocSetWaitTimeout(2_000_000_000)
+    assert st == sg.Status.DEVICE_TIMEOUT, (st, code)
+    assert code >> 24 == 4, f"expired at site {code >> 24}, expected the stream-K flag wait"
+    assert _noalloc_error(lib) == (sg.Status.SUCCESS, 0), "reading the word clears it"
+    # The next call is correct again.
+    C.fill_(float("nan"))
+    assert _noalloc(lib, A, B, C, 1.0, 0.0) == sg.Status.SUCCESS
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64),
+                                  oracle.sgemm_ref(M, N, K, 1.0, p.A, p.B))
+    assert _noalloc_error(lib) == (sg.Status.SUCCESS, 0)
+
+
+def test_settings_checked(sg):
+    lib = sg.load_library()
+    assert lib.sgemmNoAllocSetWaitTimeout(10) == sg.Status.INVALID_VALUE
+    assert lib.sgemmNoAllocSetTestWithheldSignal(7) == sg.Status.INVALID_VALUE
+    assert lib.sgemmNoAllocGetDeviceError(None) == sg.Status.INVALID_VALUE
+
+
+def test_no_device_memory_is_committed_by_later_calls(sg):
+    """After the first call on a device, later calls commit no device
+    memory, even on shapes that take kernels not launched before (small
+    products, skinny products, repacked operands, the scale-only path)."""
+    lib = sg.load_library()
+    torch.cuda.synchronize()
+    cases = []
+    for (M, N, K, lda, ldb, alpha, beta) in [
+            (96, 80, 72, None, None, 1.0, 0.0),        # small-product kernel
+            (8, 4096, 2048, None, None, 1.0, 0.5),     # skinny, TMA-fed
+            (5, 777, 301, 301, 777, 1.0, 0.0),         # skinny, plain loads
+            (600, 700, 333, 333, 701, 0.5, 0.25),      # both operands repacked
+            (300, 200, 100, None, None, 0.0, 2.0),     # scale only
+            (1536, 1280, 640, None, None, 1.0, 0.0)]:  # main kernel, stream-K
+        p = inputs.make_problem(M, N, K, seed=M + N, kind="integer", alpha=alpha, beta=beta,
+                                lda=lda, ldb=ldb)
+        A, B = _views(p)
+        C = (torch.from_numpy(p.C0).cuda() if p.C0 is not None
+             else torch.zeros((M, N), device="cuda"))
+        ref = oracle.sgemm_ref(M, N, K, alpha, p.A, p.B, beta, p.C0)
+        cases.append((A, B, C, alpha, beta, ref))
+    # First call on the device (set-up), if no earlier test made it.
+    warm = torch.zeros((64, 64), device="cuda")
+    assert _noalloc(lib, warm, warm, warm.clone(), 1.0, 0.0) == sg.Status.SUCCESS
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    reserved_before = torch.cuda.memory_reserved()
+    for A, B, C, alpha, beta, _ in cases:
+        assert _noalloc(lib, A, B, C, alpha, beta) == sg.Status.SUCCESS
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert torch.cuda.memory_reserved() == reserved_before
+    assert free_after >= free_before, f"device memory dropped by {free_before - free_after} bytes"
+    for A, B, C, alpha, beta, ref in cases:
+        np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), ref)
