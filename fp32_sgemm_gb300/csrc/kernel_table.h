@@ -47,33 +47,25 @@ void fill_variants(KernelEntry *v) {
     v[3] = make_entry<Cfg, false, false>();
 }
 
+// Tile configurations are numbered 1..kNumAlgos (sgemmSetAlgo); the
+// numbers of configurations measured slower and no longer built stay
+// unused, so the shipped ones keep their numbers.
 constexpr int kNumAlgos = 30;
-void fill_algo1(KernelEntry *v);
-void fill_algo2(KernelEntry *v);
-void fill_algo3(KernelEntry *v);
-void fill_algo4(KernelEntry *v);
-void fill_algo5(KernelEntry *v);
-void fill_algo6(KernelEntry *v);
-void fill_algo7(KernelEntry *v);
-void fill_algo8(KernelEntry *v);
-void fill_algo9(KernelEntry *v);
+constexpr int kShippedAlgos[] = {10, 16, 17, 18, 19, 20, 21, 23, 24, 27, 28, 29, 30};
+constexpr bool algo_shipped(int algo) {
+    for (int a : kShippedAlgos)
+        if (a == algo) return true;
+    return false;
+}
 void fill_algo10(KernelEntry *v);
-void fill_algo11(KernelEntry *v);
-void fill_algo12(KernelEntry *v);
-void fill_algo13(KernelEntry *v);
-void fill_algo14(KernelEntry *v);
-void fill_algo15(KernelEntry *v);
 void fill_algo16(KernelEntry *v);
 void fill_algo17(KernelEntry *v);
 void fill_algo18(KernelEntry *v);
 void fill_algo19(KernelEntry *v);
 void fill_algo20(KernelEntry *v);
 void fill_algo21(KernelEntry *v);
-void fill_algo22(KernelEntry *v);
 void fill_algo23(KernelEntry *v);
 void fill_algo24(KernelEntry *v);
-void fill_algo25(KernelEntry *v);
-void fill_algo26(KernelEntry *v);
 void fill_algo27(KernelEntry *v);
 void fill_algo28(KernelEntry *v);
 void fill_algo29(KernelEntry *v);
@@ -91,11 +83,13 @@ struct Tf32x3Args {
     int group_m;
     // Stream-K (as for the FFMA kernel): tiles >= sk_tile0 are cut into
     // (tile, K slice) units shared evenly by the CTAs; partial tiles go to
-    // `partials` (one BM x BN slot per CTA) and are announced in `flags`
-    // (one counter per CTA, zero at launch).  sk_tile0 == num_tiles: none.
+    // `partials` (one BM x BN slot per CTA) and each epilogue warp announces
+    // its part by writing the launch tag to its word of `flags` (one per
+    // CTA and epilogue warp).  sk_tile0 == num_tiles: none.
     int sk_tile0;
     float *partials;
     uint32_t *flags;
+    uint32_t *sk_seq;    // {tag of the last completed launch, CTAs finished in this one}
     uint32_t *err;
     uint64_t timeout_ns;
     int withhold;        // test hook (Withhold): a signal left out on purpose

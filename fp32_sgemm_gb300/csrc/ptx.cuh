@@ -104,6 +104,51 @@ __device__ __forceinline__ void red_release_add_gpu(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Bounded wait until a global word equals `tag` (acquire).  The CTAs
+// involved are all resident: the persistent grid never exceeds one wave.
+__device__ __forceinline__ bool tag_wait_bounded(const uint32_t *p, uint32_t tag, uint64_t timeout_ns) {
+    if (ld_acquire_gpu(p) == tag) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t probe = 1; probe < kMaxWaitProbes; ++probe) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) == tag) return true;
+        if ((probe & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return false;
+}
+
+// Stream-K launch tags.  The partial-tile flags of a launch carry a tag no
+// earlier launch used, so a flag left from an earlier launch (or from one
+// whose waits gave up) never reads as ready.  seq[0] holds the tag of the
+// last launch that completed, seq[1] counts the CTAs of the running launch
+// that finished; the last of them publishes the new tag.  Both live in
+// device memory, so a replayed CUDA graph gets a fresh tag every time.
+__device__ __forceinline__ uint32_t sk_launch_tag(const uint32_t *seq) {
+    const uint32_t t = ld_relaxed_gpu(seq) + 1u;
+    return t == 0u ? 1u : t;    // 0 is what a fresh flag holds
+}
+// Called once per CTA (one thread), after the CTA has read the tag.
+__device__ __forceinline__ void sk_launch_done(uint32_t *seq, uint32_t tag) {
+    if (atom_add_acq_rel_gpu(seq + 1, 1u) == gridDim.x - 1u) {
+        st_relaxed_gpu(seq + 1, 0u);
+        st_relaxed_gpu(seq, tag);
+    }
+}
+
 // Bounded wait until a global counter reaches `target` (acquire).  The
 // CTAs involved are all resident: the persistent grid never exceeds one
 // wave.
@@ -139,6 +184,17 @@ enum Withhold : int {
 __device__ __forceinline__ void record_error(uint32_t *err, uint32_t site) {
     if (err != nullptr)
         atomicCAS(err, 0u, (site << 24) | (blockIdx.x & 0xFFFFFFu));
+}
+
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialisation may start while the kernel before it in the stream is
+// still running: it must wait for that kernel (its completion and memory
+// flush) before it reads or writes any global memory.  Signalling early
+// lets the next kernel's CTAs be placed on SMs as this one's finish.
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

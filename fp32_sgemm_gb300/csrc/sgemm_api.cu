@@ -26,6 +26,12 @@ namespace {
 constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr uint64_t kMinTimeoutNs = 1000000ull;
+// Device control block: error word and stream-K sequence in the first 256
+// bytes, then one flag word per CTA and warp of a stream-K launch (up to
+// 1016 CTAs of 8 warps: more than two CTAs on every SM of the part).
+constexpr size_t kCtlBytes = 32768;
+constexpr int kCtlFlagsOffset = 64;                         // words
+constexpr int kCtlFlagWords = int(kCtlBytes / 4) - kCtlFlagsOffset;
 
 using sg::KernelEntry;
 using sg::kMaxDevices;
@@ -36,32 +42,15 @@ std::once_flag g_kernels_once;
 std::mutex g_occ_mutex;
 
 void init_kernel_table() {
-    sg::fill_algo1(g_kernels[0]);
-    sg::fill_algo2(g_kernels[1]);
-    sg::fill_algo3(g_kernels[2]);
-    sg::fill_algo4(g_kernels[3]);
-    sg::fill_algo5(g_kernels[4]);
-    sg::fill_algo6(g_kernels[5]);
-    sg::fill_algo7(g_kernels[6]);
-    sg::fill_algo8(g_kernels[7]);
-    sg::fill_algo9(g_kernels[8]);
     sg::fill_algo10(g_kernels[9]);
-    sg::fill_algo11(g_kernels[10]);
-    sg::fill_algo12(g_kernels[11]);
-    sg::fill_algo13(g_kernels[12]);
-    sg::fill_algo14(g_kernels[13]);
-    sg::fill_algo15(g_kernels[14]);
     sg::fill_algo16(g_kernels[15]);
     sg::fill_algo17(g_kernels[16]);
     sg::fill_algo18(g_kernels[17]);
     sg::fill_algo19(g_kernels[18]);
     sg::fill_algo20(g_kernels[19]);
     sg::fill_algo21(g_kernels[20]);
-    sg::fill_algo22(g_kernels[21]);
     sg::fill_algo23(g_kernels[22]);
     sg::fill_algo24(g_kernels[23]);
-    sg::fill_algo25(g_kernels[24]);
-    sg::fill_algo26(g_kernels[25]);
     sg::fill_algo27(g_kernels[26]);
     sg::fill_algo28(g_kernels[27]);
     sg::fill_algo29(g_kernels[28]);
@@ -88,7 +77,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct sgemmContext {
     int device = -1;
     int sm_count = 0;
+    // Device control block (allocated with the handle): word 0 the error
+    // word, words 1-2 the stream-K launch sequence {tag, CTAs finished},
+    // from word kCtlFlagsOffset the stream-K flags (kCtlFlagWords words: one
+    // per CTA and warp of a launch).
     uint32_t *d_err = nullptr;
+    uint32_t *d_flags = nullptr;
+    uint32_t *d_sk_seq = nullptr;
+    int flag_words = 0;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     uint64_t timeout_ns = kDefaultTimeoutNs;
@@ -204,7 +200,7 @@ struct Plan {
     int prep_a = 0, prep_b = 0;
     int64_t lda_p = 0, ldb_p = 0, sa_p = 0, sb_p = 0;
     size_t ws_a = 0, ws_b = 0;      // repacked A / B
-    size_t ws_flags = 0, ws_partials = 0;   // stream-K scratch (0 when not used)
+    size_t ws_partials = 0;         // stream-K partial tiles (0 when not used)
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, group_m = 16;
     int k_blocks = 0;
     int dp_ctas = 0, sk_ctas = 0;   // persistent grid for whole tiles / stream-K
@@ -228,10 +224,10 @@ struct Plan {
 // FMAs) measured fastest from 1024^3 to 8192^3 where C is 16-byte aligned
 // and read (beta != 0); otherwise configuration 28 (the same tile and loop,
 // a 2-stage ring, C through a shared-memory staging area: TMA stores when
-// beta == 0 and C is aligned, else row runs).  Their loop beats the earlier
-// one (8-byte A and 16-byte B reads both double buffered: configurations
-// 15 and 22) by 1-2% (4096^3: 2160 -> 2134 us; 8192^3: 17293 -> 17023 us;
-// beta = 0.5: 2197 -> 2148 us).
+// beta == 0 and C is aligned, else row runs).  Their loop beat the earlier
+// one (8-byte A and 16-byte B reads both double buffered, since removed) by
+// 1-2% (4096^3: 2160 -> 2134 us; 8192^3: 17293 -> 17023 us; beta = 0.5:
+// 2197 -> 2148 us).
 constexpr int kDefaultAlgo = 29;     // beta != 0, C 16-byte aligned
 constexpr int kStoreTmaAlgo = 28;    // beta == 0 or C not 16-byte aligned
 constexpr int kWideStoreTmaAlgo = 27;   // the same, 128 x 256, for wide products
@@ -303,7 +299,7 @@ bool c_vector_ok(const Problem &q) {
 }
 
 int choose_algo(const sgemmContext *h, const Problem &q) {
-    if (h->algo >= 1 && h->algo <= kNumAlgos) return h->algo - 1;
+    if (h->algo != 0) return sg::algo_shipped(h->algo) ? h->algo - 1 : -1;
     if (q.M <= 128 && q.N <= 128) return 10 - 1;
     if (q.M <= 32 && q.M <= q.N) return 18 - 1;
     if (q.N <= 32) return 19 - 1;
@@ -449,7 +445,6 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
         if (rem_units < 8 * slots) first = waves >= 1 ? (waves - 1) * slots : 0;
         pl.sk_tile0 = int(first);
         pl.sk_ctas = int(sk_ctas);
-        pl.ws_flags = align256(size_t(sk_ctas) * 4);
         pl.ws_partials = size_t(sk_ctas) * size_t(info.bm) * size_t(info.bn) * 4;
     }
     pl.pub.tile_m = info.bm;
@@ -550,6 +545,7 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     pl.pub.packs_b = pl.prep_b != 0;
     pl.pub.vector_epilogue = c_vector_ok(q) ? 1 : 0;
     pl.algo_index = choose_algo(h, q);
+    if (pl.algo_index < 0) return SGEMM_STATUS_INVALID_VALUE;   // a configuration that is not built
     pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
     pl.tiles_m = int(ceil_div(q.M, e.bm));
@@ -569,7 +565,10 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     const double dp_eff = per_sm / std::ceil(per_sm);
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
     const bool want_sk = h->schedule == 2 || (h->schedule == 0 && dp_eff < 0.985);
-    const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots, true);
+    // Schedule 2 spreads the units evenly over every CTA slot; the automatic
+    // schedule may use fewer CTAs for few tiles (each tile cut into pieces).
+    const int64_t sk_ctas = h->schedule == 2 ? std::min(units, slots)
+                                             : stream_k_ctas(pl.num_tiles, pl.k_blocks, slots, true);
     if (want_sk && pl.k_blocks >= 2 && units < kMaxDim && sk_ctas > 0) {
         // All but the last full wave of tiles run whole (their concurrent
         // tiles form a compact band, friendly to L2); the last wave plus the
@@ -577,7 +576,6 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
         const int64_t waves = pl.num_tiles / slots;
         pl.sk_tile0 = waves >= 2 ? int((waves - 1) * slots) : 0;
         pl.sk_ctas = int(sk_ctas);
-        pl.ws_flags = align256(size_t(sk_ctas) * 4);
         pl.ws_partials = size_t(sk_ctas) * size_t(e.bm) * size_t(e.bn) * 4;
     }
     pl.pub.tile_m = e.bm;
@@ -634,13 +632,34 @@ inline sgemmStatus_t last_launch() {
     return cudaGetLastError() == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
 }
 
+// Main kernels are launched with programmatic stream serialisation: their
+// CTAs may be placed (and set up their barriers) while the previous kernel
+// in the stream finishes; they wait for it (griddepcontrol.wait) before
+// touching global memory.
 sgemmStatus_t launch_main(sgemmContext *h, const void *fn, int ctas, int threads, int smem,
                           void **kargs, cudaStream_t stream) {
     if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
         return SGEMM_STATUS_LAUNCH_FAILED;
-    cudaError_t err = cudaLaunchKernel(fn, dim3(ctas), dim3(threads), kargs, size_t(smem), stream);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelExC(&cfg, fn, kargs);
     if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
     return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
+}
+
+// Stream-K needs its partial tiles in the workspace (after `used` bytes)
+// and one flag word per CTA and warp in the handle's control block.
+bool sk_usable(const sgemmContext *h, const Plan &pl, size_t used, int warps) {
+    return pl.sk_ctas > 0 && h->ws != nullptr && h->ws_bytes >= used + pl.ws_partials &&
+           int64_t(pl.sk_ctas) * warps <= h->flag_words;
 }
 
 sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cudaStream_t stream) {
@@ -689,15 +708,12 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
     args.withhold = h->withhold;
     args.sk_tile0 = pl.num_tiles;
     int ctas = pl.dp_ctas;
-    if (pl.sk_ctas > 0 && h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials) {
-        char *sk = ws + pl.ws_split;
+    if (sk_usable(h, pl, pl.ws_split, info.threads / 32 - 2)) {
         args.sk_tile0 = pl.sk_tile0;
-        args.flags = reinterpret_cast<uint32_t *>(sk);
-        args.partials = reinterpret_cast<float *>(sk + pl.ws_flags);
+        args.flags = h->d_flags;
+        args.sk_seq = h->d_sk_seq;
+        args.partials = reinterpret_cast<float *>(ws + pl.ws_split);
         ctas = pl.sk_ctas;
-        // Counters start at zero for every launch.
-        if (cudaMemsetAsync(args.flags, 0, size_t(ctas) * 4, stream) != cudaSuccess)
-            return SGEMM_STATUS_LAUNCH_FAILED;
     }
     void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
     return launch_main(h, info.fn[pl.variant], ctas, info.threads, info.smem, kargs, stream);
@@ -779,8 +795,7 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
 
     const float *Ause = q.A, *Buse = q.B;
     // Stream-K scratch is optional: without room for it, whole tiles are used.
-    const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
-                        h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
+    const bool use_sk = sk_usable(h, pl, pl.ws_a + pl.ws_b, g_kernels[pl.algo_index][pl.variant].threads / 32);
     const int M = int(q.M), N = int(q.N), K = int(q.K), batch = int(q.batch);
     if (pl.prep_a || pl.prep_b) {
         if (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b) return SGEMM_STATUS_WORKSPACE_REQUIRED;
@@ -840,15 +855,13 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     int ctas = pl.dp_ctas;
     args.sk_tile0 = pl.num_tiles;
     if (use_sk) {
-        char *ws = static_cast<char *>(h->ws) + pl.ws_a + pl.ws_b;
+        // Partial tiles in the workspace; flags and launch tags in the
+        // handle's control block (no reset needed between launches).
         args.sk_tile0 = pl.sk_tile0;
-        args.flags = reinterpret_cast<uint32_t *>(ws);
-        args.partials = reinterpret_cast<float *>(ws + pl.ws_flags);
+        args.flags = h->d_flags;
+        args.sk_seq = h->d_sk_seq;
+        args.partials = reinterpret_cast<float *>(static_cast<char *>(h->ws) + pl.ws_a + pl.ws_b);
         ctas = pl.sk_ctas;
-        // Flags start at zero for every launch (set by the CTA that stores a
-        // partial tile, read by the CTA that finishes that tile).
-        if (cudaMemsetAsync(args.flags, 0, size_t(ctas) * 4, stream) != cudaSuccess)
-            return SGEMM_STATUS_LAUNCH_FAILED;
     }
     void *kargs[] = {&tmA, &tmB, &tmC, &args};
     return launch_main(h, e.fn, ctas, e.threads, e.smem, kargs, stream);
@@ -861,7 +874,7 @@ sgemmStatus_t run(sgemmContext *h, int64_t M, int64_t N, int64_t K, float alpha,
 }
 
 size_t workspace_bytes(const Plan &pl) {
-    return pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials + pl.ws_split;
+    return pl.ws_a + pl.ws_b + pl.ws_partials + pl.ws_split;
 }
 
 // Skinny products use the workspace only when it is big enough; the size
@@ -961,8 +974,9 @@ sgemmStatus_t sgemmCreate(sgemmHandle_t *handle) {
     if (h == nullptr) return SGEMM_STATUS_INTERNAL_ERROR;
     h->device = dev;
     h->sm_count = sms;
-    bool ok = cudaMalloc(&h->d_err, sizeof(uint32_t)) == cudaSuccess &&
-              cudaMemset(h->d_err, 0, sizeof(uint32_t)) == cudaSuccess &&
+    h->flag_words = kCtlFlagWords;
+    bool ok = cudaMalloc(&h->d_err, kCtlBytes) == cudaSuccess &&
+              cudaMemset(h->d_err, 0, kCtlBytes) == cudaSuccess &&
               cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&h->ev_begin, cudaEventDisableTiming) == cudaSuccess &&
@@ -975,6 +989,8 @@ sgemmStatus_t sgemmCreate(sgemmHandle_t *handle) {
         delete h;
         return SGEMM_STATUS_LAUNCH_FAILED;
     }
+    h->d_sk_seq = h->d_err + 1;
+    h->d_flags = h->d_err + kCtlFlagsOffset;
     *handle = h;
     return SGEMM_STATUS_SUCCESS;
 }
@@ -1218,13 +1234,13 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
     if (pl.pub.kind == 1 || pl.pub.kind == 3) pl.pub.raster_group = pl.group_m;
     if (pl.pub.kind == 3) {
         const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
-                            h->ws_bytes >= pl.ws_split + pl.ws_flags + pl.ws_partials;
+                            h->ws_bytes >= pl.ws_split + pl.ws_partials;
         pl.pub.ctas = use_sk ? pl.sk_ctas : pl.dp_ctas;
         pl.pub.stream_k = use_sk ? 1 : 0;
     }
     if (pl.pub.kind == 1) {
         const bool use_sk = pl.sk_ctas > 0 && h->ws != nullptr &&
-                            h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_flags + pl.ws_partials;
+                            h->ws_bytes >= pl.ws_a + pl.ws_b + pl.ws_partials;
         pl.pub.ctas = use_sk ? pl.sk_ctas : pl.dp_ctas;
         pl.pub.stream_k = use_sk ? 1 : 0;
     }
@@ -1233,7 +1249,10 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
 }
 
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
-    if (h == nullptr || algo < 0 || algo > kNumAlgos) return SGEMM_STATUS_INVALID_VALUE;
+    // 1..3 also name the tensor-core tiles of math mode 1.
+    if (h == nullptr || algo < 0 || algo > kNumAlgos ||
+        (algo > sg::kNumTf32x3Configs && !sg::algo_shipped(algo)))
+        return SGEMM_STATUS_INVALID_VALUE;
     h->algo = algo;
     return SGEMM_STATUS_SUCCESS;
 }
@@ -1310,7 +1329,7 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t h, uint64_t timeout_ns, cud
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
-constexpr size_t kStaticErrBytes = 256;                     // error word, padded
+constexpr size_t kStaticCtlBytes = kCtlBytes;               // control block (as a handle's)
 
 }  // namespace
 
@@ -1357,7 +1376,7 @@ void setup_static_scratch(StaticScratchSlot &slot, int dev) {
     std::call_once(g_kernels_once, init_kernel_table);
     for (auto &row : g_kernels)
         for (KernelEntry &e : row)
-            if (occupancy_on(dev, e) < 1) {
+            if (e.fn != nullptr && occupancy_on(dev, e) < 1) {
                 slot.status = SGEMM_STATUS_LAUNCH_FAILED;
                 return;
             }
@@ -1405,8 +1424,11 @@ extern "C" sgemmStatus_t sgemmNoAlloc(int64_t M, int64_t N, int64_t K, float alp
     ctx.device = dev;
     ctx.sm_count = slot->sm_count;
     ctx.d_err = reinterpret_cast<uint32_t *>(slot->ptr);
-    ctx.ws = slot->ptr + kStaticErrBytes;
-    ctx.ws_bytes = kStaticScratchBytes - kStaticErrBytes;
+    ctx.d_sk_seq = ctx.d_err + 1;
+    ctx.d_flags = ctx.d_err + kCtlFlagsOffset;
+    ctx.flag_words = kCtlFlagWords;
+    ctx.ws = slot->ptr + kStaticCtlBytes;
+    ctx.ws_bytes = kStaticScratchBytes - kStaticCtlBytes;
     ctx.timeout_ns = slot->timeout_ns.load();
     ctx.withhold = slot->withhold.load();
 

@@ -2,9 +2,9 @@
 //
 // Structure (persistent CTAs, one per SM slot; tiles taken round robin,
 // then stream-K units):
-//   * a producer: thread 0 of the first consumer warp (or, in some
-//     configurations, a dedicated warp) streams the K slices of A and B into
-//     an S-stage shared-memory ring with TMA tile loads; each stage has a
+//   * a producer: thread 0 (one of the consumers) streams the K slices of A
+//     and B into an S-stage shared-memory ring with TMA tile loads; each
+//     stage has a
 //     "full" mbarrier (TMA transaction bytes) and an "empty" mbarrier (one
 //     arrival per consumer warp).  Out-of-range rows/columns of partial tiles
 //     arrive as zeros (TMA out-of-bounds fill), so M, N, K need not be tile
@@ -70,7 +70,8 @@ struct GemmArgs {
     int group_m;          // rasterisation: tile rows per band
     int sk_tile0;         // tiles [0, sk_tile0) whole, round robin; [sk_tile0, num_tiles) stream-K
     float *partials;      // stream-K: one BM x BN partial tile per CTA
-    uint32_t *flags;      // stream-K: one counter per CTA (warps that stored their part), zeroed before the launch
+    uint32_t *flags;      // stream-K: per CTA and consumer warp, the launch tag of the part it stored
+    uint32_t *sk_seq;     // stream-K: {tag of the last completed launch, CTAs finished in this one}
     uint32_t *err;        // device error word (bounded waits)
     uint64_t timeout_ns;
     int withhold;         // test hook (Withhold): a signal left out on purpose
@@ -88,16 +89,14 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 // Tile configuration.
 //   BM x BN output tile, BK-wide K slices, STAGES-deep shared-memory ring;
 //   WARPS_M x WARPS_N consumer warps, each lane an 8 x 16 register tile
-//   (lane grid WR x (32/WR) inside a warp);
+//   (lane grid WR x (32/WR) inside a warp); thread 0 also issues the TMA
+//   loads;
 //   KA: k values per vector read of A (4 -> 16 B, 2 -> 8 B);
-//   PRODUCER_WARP: 1 = a dedicated TMA warp, 0 = thread 0 of the first
-//   consumer warp issues the loads (no extra warp);
-//   PIPE: 1 = fragments of the next k are read while this k's FMAs run
-//   (explicit register double buffering), 2 = only the A fragments are
-//   double buffered (the next A group read one k ahead; each k's B values
-//   read just before its FMAs, which frees 16 registers for 16-byte A
-//   reads), 0 = left to the compiler;
-//   KQ_UNROLL: A-vector groups per loop iteration (PIPE = 1 needs >= 2);
+//   PIPE_B: the next A group is always read one k step ahead of need
+//   (register double buffering); 1 = the B values of the next k are read
+//   while this k's FMAs run as well, 0 = each k's B values are read just
+//   before its FMAs (which frees 16 registers for 16-byte A reads);
+//   KQ_UNROLL: A-vector groups per loop iteration (even);
 //   STORE_TMA: 1 = beta == 0 tiles leave through a per-warp shared-memory
 //   staging area and TMA tile stores (64 x 16 boxes) instead of st.global;
 //   REFILL_LAG (inline producer): after consuming slice g, thread 0 refills
@@ -105,8 +104,8 @@ __device__ __forceinline__ float vec_get(const float2 &v, int k) { return k == 0
 //   waits for all warps to release slice g but keeps STAGES - 1 slices in
 //   flight instead of STAGES - 2 (what a 2-stage ring needs).
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_,
-          int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_ = 4, int PRODUCER_WARP_ = 1,
-          int PIPE_ = 0, int SCALAR_FMA_ = 0, int STORE_TMA_ = 0, int REFILL_LAG_ = 1>
+          int WR_, int KQ_UNROLL_, int MIN_CTAS_, int KA_, int PIPE_B_, int STORE_TMA_ = 0,
+          int REFILL_LAG_ = 1>
 struct FfmaConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -116,14 +115,11 @@ struct FfmaConfig {
     static constexpr int KQ_UNROLL = KQ_UNROLL_;
     static constexpr int MIN_CTAS = MIN_CTAS_;
     static constexpr int KA = KA_;
-    static constexpr bool PRODUCER_WARP = PRODUCER_WARP_ != 0;
-    static constexpr bool PIPE = PIPE_ != 0;
-    static constexpr bool PIPE_B = PIPE_ == 1;   // B fragments double buffered too
-    static constexpr bool SCALAR_FMA = SCALAR_FMA_ != 0;   // fmaf instead of packed fma.rn.f32x2
+    static constexpr bool PIPE_B = PIPE_B_ != 0;   // B fragments double buffered too
     static constexpr bool STORE_TMA = STORE_TMA_ != 0;
     static constexpr int REFILL_LAG = REFILL_LAG_;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMER_WARPS + (PRODUCER_WARP ? 1 : 0)) * 32;
+    static constexpr int THREADS = CONSUMER_WARPS * 32;
     static constexpr int ROW_BYTES_A = BK * 4;                 // one row of the A slice
     static constexpr int A_STAGE_BYTES = BM * BK * 4;
     static constexpr int B_STAGE_BYTES = BK * BN * 4;
@@ -134,6 +130,8 @@ struct FfmaConfig {
     // as NJ boxes of WTM rows x 4*WC columns (box j = the lane columns of j).
     static constexpr int C_BOX_COLS = 4 * WC, C_BOX_BYTES = WTM * C_BOX_COLS * 4;
     static constexpr int STORE_BYTES = STORE_TMA ? CONSUMER_WARPS * WTM * WTN * 4 : 0;
+    // Barriers, then 128 bytes for the TMA issuer's slice cursor and the
+    // stream-K launch tag, then 1024 for aligning the stages.
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STORE_BYTES + 2 * STAGES * 8 + 128 + 1024;
     static constexpr int NKQ = BK / KA;                        // A-vector groups per slice
     // TMA boxes are at most 256 elements a side: wider tiles take several.
@@ -151,7 +149,7 @@ struct FfmaConfig {
     static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "stage alignment");
     static_assert(KA == 2 || KA == 4, "A vector width");
     static_assert(NKQ % KQ_UNROLL == 0, "unroll must divide the slice");
-    static_assert(!PIPE || KQ_UNROLL % 2 == 0, "pipelined fragments alternate two buffers");
+    static_assert(KQ_UNROLL % 2 == 0, "pipelined fragments alternate two buffers");
     static_assert(STAGES >= 2, "ring depth");
     static_assert(REFILL_LAG == 0 || REFILL_LAG == 1, "refill lag");
     // Staging writes are conflict-free when the 8 lanes of a quarter warp
@@ -373,9 +371,12 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES + Cfg::STORE_BYTES);
     uint64_t *empty = full + STAGES;
     SliceCursor *cursor = reinterpret_cast<SliceCursor *>(empty + STAGES);
+    volatile uint32_t *sk_tag_s = reinterpret_cast<volatile uint32_t *>(cursor + 1);
+    static_assert(sizeof(SliceCursor) + 4 <= 128, "cursor and tag fit their 128 bytes");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const bool stream_k = p.sk_tile0 < p.num_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -383,41 +384,31 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
         fence_barrier_init();
-    }
-    __syncthreads();
-
-    if constexpr (Cfg::PRODUCER_WARP) {
-        if (warp == Cfg::CONSUMER_WARPS) {
-            // ---------------- dedicated producer warp ----------------
-            if (lane != 0) return;
-            prefetch_tensormap(&tmA);
-            prefetch_tensormap(&tmB);
-            cursor_begin(cursor, p);
-            while (cursor_valid(cursor)) {
-                if (p.withhold == kWithholdRefill && cursor_issued(cursor) >= STAGES) {
-                    drain_slices<Cfg>(0, cursor_issued(cursor), full, p.timeout_ns);
-                    return;
-                }
-                if (!issue_slice<Cfg>(cursor, p, &tmA, &tmB, sA, sB, full, empty)) {
-                    record_error(p.err, kSiteProducerEmpty);
-                    // No consumer may ever take the most recent slices.
-                    drain_slices<Cfg>(0, cursor_issued(cursor), full, p.timeout_ns);
-                    return;
-                }
-            }
-            return;
-        }
-    }
-
-    // ---------------- consumers ----------------
-    // Inline producer: thread 0 issues the first STAGES slices up front, then
-    // after consuming slice g (g >= 1) refills the stage of slice g - 1, which
-    // every warp has released by the time thread 0 is done with slice g (with
-    // REFILL_LAG 0: the stage of slice g itself, once every warp released it).
-    const bool producer = !Cfg::PRODUCER_WARP && threadIdx.x == 0;
-    if (producer) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+    }
+    // Only shared memory and kernel parameters so far; from here on global
+    // memory is read and written.
+    griddep_launch_dependents();
+    griddep_wait();
+    if (threadIdx.x == 0 && stream_k) *sk_tag_s = sk_launch_tag(p.sk_seq);
+    __syncthreads();
+    // (The tag is read back from shared memory where it is used: a value
+    // kept live across the FMA loop would compete for its registers.)
+
+    // Thread 0 reports the end of its CTA's part of a stream-K launch at
+    // whichever of its exits it takes (the normal end, or a wait that gave
+    // up), so that the next launch gets a fresh tag in every case.
+    auto cta_done = [&]() {
+        if (threadIdx.x == 0 && p.sk_tile0 < p.num_tiles) sk_launch_done(p.sk_seq, *sk_tag_s);
+    };
+    // ---------------- consumers ----------------
+    // Producer: thread 0 issues the first STAGES slices up front, then after
+    // consuming slice g (g >= 1) refills the stage of slice g - 1, which
+    // every warp has released by the time thread 0 is done with slice g (with
+    // REFILL_LAG 0: the stage of slice g itself, once every warp released it).
+    const bool producer = threadIdx.x == 0;
+    if (producer) {
         if constexpr (TMA_EPILOGUE) prefetch_tensormap(&tmC);
         cursor_begin(cursor, p);
         while (cursor_valid(cursor) && cursor_issued(cursor) < STAGES)
@@ -468,15 +459,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const float2 a2 = make_float2(av, av);
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
-                if constexpr (Cfg::SCALAR_FMA) {
-                    acc[i][2 * j].x = fmaf(av, b[j].x, acc[i][2 * j].x);
-                    acc[i][2 * j].y = fmaf(av, b[j].y, acc[i][2 * j].y);
-                    acc[i][2 * j + 1].x = fmaf(av, b[j].z, acc[i][2 * j + 1].x);
-                    acc[i][2 * j + 1].y = fmaf(av, b[j].w, acc[i][2 * j + 1].y);
-                } else {
-                    acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
-                    acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
-                }
+                acc[i][2 * j] = __ffma2_rn(a2, make_float2(b[j].x, b[j].y), acc[i][2 * j]);
+                acc[i][2 * j + 1] = __ffma2_rn(a2, make_float2(b[j].z, b[j].w), acc[i][2 * j + 1]);
             }
         }
     };
@@ -521,58 +505,45 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 record_error(p.err, kSiteConsumerFull);
                 if (producer) drain_slices<Cfg>(g, cursor_issued(cursor), full, p.timeout_ns);
                 if constexpr (TMA_EPILOGUE) { if (lane == 0) bulk_wait_all(); }
+                cta_done();
                 return;
             }
             const unsigned char *As = sA + stage * Cfg::A_STAGE_BYTES + a_row0_off;
             const float *Bs = reinterpret_cast<const float *>(sB + stage * Cfg::B_STAGE_BYTES) + b_off;
 
-            if constexpr (Cfg::PIPE) {
-                // Register double buffering: while the FMAs of k run, the B
-                // values of k+1 (and, one k ahead of need, the next A group)
-                // are read into the other buffer.  Loop iterations cover
-                // KQ_UNROLL groups so the buffer roles are compile-time.
-                AVec a0[TM], a1[TM];
-                float4 b0[NJ], b1[NJ];
-                load_a(As, 0, a0);
-                if constexpr (Cfg::PIPE_B) load_b(Bs, 0, b0);
-                constexpr int KSTEPS = Cfg::KQ_UNROLL * KA;
+            // Register double buffering: while the FMAs of k run, the B
+            // values of k+1 (and, one k ahead of need, the next A group)
+            // are read into the other buffer.  Loop iterations cover
+            // KQ_UNROLL groups so the buffer roles are compile-time.
+            AVec a0[TM], a1[TM];
+            float4 b0[NJ], b1[NJ];
+            load_a(As, 0, a0);
+            if constexpr (Cfg::PIPE_B) load_b(Bs, 0, b0);
+            constexpr int KSTEPS = Cfg::KQ_UNROLL * KA;
 #pragma unroll 1
-                for (int kq0 = 0; kq0 < NKQ; kq0 += Cfg::KQ_UNROLL) {
-                    const bool more = kq0 + Cfg::KQ_UNROLL < NKQ;
+            for (int kq0 = 0; kq0 < NKQ; kq0 += Cfg::KQ_UNROLL) {
+                const bool more = kq0 + Cfg::KQ_UNROLL < NKQ;
 #pragma unroll
-                    for (int u = 0; u < Cfg::KQ_UNROLL; ++u) {
-                        AVec (&ac)[TM] = (u & 1) ? a1 : a0;
-                        AVec (&an)[TM] = (u & 1) ? a0 : a1;
-#pragma unroll
-                        for (int kr = 0; kr < KA; ++kr) {
-                            const int ks = u * KA + kr;                 // k step inside the iteration
-                            float4 (&bc)[NJ] = (Cfg::PIPE_B && (ks & 1)) ? b1 : b0;
-                            float4 (&bn)[NJ] = (ks & 1) ? b0 : b1;
-                            const bool last = ks == KSTEPS - 1;
-                            if constexpr (Cfg::PIPE_B) {
-                                if (!last || more) load_b(Bs, kq0 * KA + ks + 1, bn);
-                            } else {
-                                // Keep each k's B reads in place: hoisted
-                                // reads of later k would need registers.
-                                asm volatile("" ::: "memory");
-                                load_b(Bs, kq0 * KA + ks, bc);
-                            }
-                            if (kr == KA - 2 && (u + 1 < Cfg::KQ_UNROLL || more))
-                                load_a(As, kq0 + u + 1, an);
-                            fma_k(ac, kr, bc);
-                        }
-                    }
-                }
-            } else {
-#pragma unroll Cfg::KQ_UNROLL
-                for (int kq = 0; kq < NKQ; ++kq) {
-                    AVec a[TM];
-                    load_a(As, kq, a);
+                for (int u = 0; u < Cfg::KQ_UNROLL; ++u) {
+                    AVec (&ac)[TM] = (u & 1) ? a1 : a0;
+                    AVec (&an)[TM] = (u & 1) ? a0 : a1;
 #pragma unroll
                     for (int kr = 0; kr < KA; ++kr) {
-                        float4 b[NJ];
-                        load_b(Bs, kq * KA + kr, b);
-                        fma_k(a, kr, b);
+                        const int ks = u * KA + kr;                 // k step inside the iteration
+                        float4 (&bc)[NJ] = (Cfg::PIPE_B && (ks & 1)) ? b1 : b0;
+                        float4 (&bn)[NJ] = (ks & 1) ? b0 : b1;
+                        const bool last = ks == KSTEPS - 1;
+                        if constexpr (Cfg::PIPE_B) {
+                            if (!last || more) load_b(Bs, kq0 * KA + ks + 1, bn);
+                        } else {
+                            // Keep each k's B reads in place: hoisted
+                            // reads of later k would need registers.
+                            asm volatile("" ::: "memory");
+                            load_b(Bs, kq0 * KA + ks, bc);
+                        }
+                        if (kr == KA - 2 && (u + 1 < Cfg::KQ_UNROLL || more))
+                            load_a(As, kq0 + u + 1, an);
+                        fma_k(ac, kr, bc);
                     }
                 }
             }
@@ -584,6 +555,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                     record_error(p.err, kSiteProducerEmpty);
                     drain_slices<Cfg>(g + 1, cursor_issued(cursor), full, p.timeout_ns);
                     if constexpr (TMA_EPILOGUE) bulk_wait_all();
+                    cta_done();
                     return;
                 }
             }
@@ -592,8 +564,8 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         // ---------------- stream-K fixup ----------------
         // Warp by warp: the same (warp, lane) holds the same elements of the
         // tile in every CTA, so each warp hands over and collects its own
-        // part with no CTA-wide rendezvous.  A CTA's counter counts the
-        // warps that have stored their part of its partial tile.
+        // part with no CTA-wide rendezvous; the flag of (CTA, warp) holds
+        // this launch's tag once that warp's part is stored.
         if (seg.kb0 != 0 || seg.kb1 != p.k_blocks) {
             float4 *mine = reinterpret_cast<float4 *>(p.partials + (size_t)blockIdx.x * (BM * BN));
             if (seg.kb0 != 0) {
@@ -609,7 +581,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                 __threadfence();
                 __syncwarp();
                 if (lane == 0 && p.withhold != kWithholdStreamKFlag)
-                    red_release_add_gpu(&p.flags[blockIdx.x], 1u);
+                    st_release_gpu(&p.flags[blockIdx.x * Cfg::CONSUMER_WARPS + warp], *sk_tag_s);
                 it.advance(p, seg);
                 continue;
             }
@@ -620,7 +592,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const int c_last = cta_of_unit(tile_u0 + p.k_blocks - 1, p);
             if (lane == 0) {
                 for (int c = c_first; c <= c_last; ++c)
-                    if (!count_wait_bounded(&p.flags[c], (uint32_t)Cfg::CONSUMER_WARPS, p.timeout_ns))
+                    if (!tag_wait_bounded(&p.flags[c * Cfg::CONSUMER_WARPS + warp], *sk_tag_s, p.timeout_ns))
                         record_error(p.err, kSiteStreamKFlag);
             }
             __syncwarp();
@@ -785,6 +757,7 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         it.advance(p, seg);
     }
+    cta_done();
     if constexpr (TMA_EPILOGUE) {
         if (lane == 0) bulk_wait_all();
     }

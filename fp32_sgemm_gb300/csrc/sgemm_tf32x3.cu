@@ -132,7 +132,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     uint64_t *tfull = bars + 2 * STAGES;        // MMA -> epilogue, per accumulator
     uint64_t *tempty = tfull + 2;               // epilogue -> MMA, per accumulator
     uint64_t *drain = tempty + 2;               // MMA completion before teardown
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);   // [1]: stream-K launch tag
     float *xpose = reinterpret_cast<float *>(tmem_slot + 4);     // 16 bytes after the barriers
 
     const int warp = threadIdx.x >> 5;
@@ -150,18 +150,26 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         }
         mbar_init(drain, 1);
         fence_barrier_init();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
-
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer ----------------
         prefetch_tensormap(&tmAhi);
         prefetch_tensormap(&tmAlo);
         prefetch_tensormap(&tmBhi);
         prefetch_tensormap(&tmBlo);
+    }
+    // Shared memory, tensor memory and parameters only so far: wait for the
+    // kernel before this one (the operand split) before touching global
+    // memory.
+    griddep_launch_dependents();
+    griddep_wait();
+    const bool stream_k = p.sk_tile0 < p.num_tiles;
+    if (threadIdx.x == 32 && stream_k) tmem_slot[1] = sk_launch_tag(p.sk_seq);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    const uint32_t sk_tag = stream_k ? reinterpret_cast<volatile uint32_t *>(tmem_slot)[1] : 0u;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -341,7 +349,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     __threadfence();
                     __syncwarp();
                     if (lane == 0 && p.withhold != kWithholdStreamKFlag)
-                        red_release_add_gpu(&p.flags[blockIdx.x], 1u);
+                        st_release_gpu(&p.flags[blockIdx.x * Cfg::EPI_WARPS + ew], sk_tag);
                     w.advance(p, seg);
                     continue;
                 }
@@ -352,7 +360,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 const int c_last = tc_cta_of_unit(tile_u0 + p.k_blocks - 1, p);
                 if (lane == 0) {
                     for (int c = c_first; c <= c_last; ++c)
-                        if (!count_wait_bounded(&p.flags[c], (uint32_t)Cfg::EPI_WARPS, p.timeout_ns))
+                        if (!tag_wait_bounded(&p.flags[c * Cfg::EPI_WARPS + ew], sk_tag, p.timeout_ns))
                             record_error(p.err, kSiteStreamKFlag);
                 }
                 __syncwarp();
@@ -466,6 +474,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (threadIdx.x == 32 && stream_k) sk_launch_done(p.sk_seq, sk_tag);
 }
 
 // ---------------------------------------------------------------- launches

@@ -30,10 +30,18 @@
  *     k is fixed for a given shape, so repeated calls give identical bits.
  *   - Errors are returned, never printed or raised; see sgemmStatus_t.
  *   - Thread safety: a handle may be used from one host thread at a time.
+ *     Calls on one handle share its workspace and its device control block
+ *     (stream-K flags), so calls on one handle must not run concurrently on
+ *     the GPU: order them on one stream, or use one handle per stream.
+ *   - Main kernels are launched with programmatic stream serialisation:
+ *     they may be placed on SMs while the previous kernel in the stream
+ *     finishes, and wait for it before touching any memory.
  *   - CUDA graphs: sgemmEx(), sgemm() and sgemmStridedBatched() enqueue only
- *     kernels and memsets on `stream`, so they can be captured, provided the
- *     workspace they need is attached and the same shape was run once before
- *     the capture (the first call of a kernel variant sets its attributes).
+ *     kernels on `stream`, so they can be captured, provided the workspace
+ *     they need is attached and the same shape was run once before the
+ *     capture (the first call of a kernel variant sets its attributes).
+ *     Replays stay correct: the stream-K flags carry a launch tag kept in
+ *     device memory, fresh for every launch.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -81,8 +89,10 @@ sgemmStatus_t sgemmGetVersion(int *version);
  * Create a handle bound to the CURRENT device.  Checks that the device is
  * compute capability 10.3 (ARCH_MISMATCH otherwise), reads its SM count,
  * creates the two copy streams and the events of sgemmHostEx, and allocates
- * the handle's 4-byte device error word: the only device allocation the
- * library makes, done here and never on the compute path.
+ * the handle's 32 KiB device control block (the error word, and the flags
+ * and launch sequence through which stream-K CTAs hand over partial tiles):
+ * the only device allocation the library makes, done here and never on the
+ * compute path.
  */
 sgemmStatus_t sgemmCreate(sgemmHandle_t *handle);
 
@@ -103,9 +113,9 @@ sgemmStatus_t sgemmGetDefaultHandle(sgemmHandle_t *handle);
  *     not 16-byte aligned or row pitch not a multiple of 16 bytes) into rows
  *     padded to a multiple of 4 floats: REQUIRED for such operands;
  *   - math mode 1 (3xTF32): the TF32 hi / lo parts of A and B: REQUIRED;
- *   - stream-K scratch (one ready counter and one BM x BN FP32 partial tile
- *     per CTA of the launch) when the output tiles do not divide evenly over
- *     the SMs or are too few to fill them (their K ranges are then split):
+ *   - stream-K scratch (one BM x BN FP32 partial tile per CTA of the
+ *     launch) when the output tiles do not divide evenly over the SMs or are
+ *     too few to fill them (their K ranges are then split):
  *     OPTIONAL; with less workspace the call runs whole tiles per CTA instead
  *     (same result up to summation order, less even load);
  *   - skinny products (M or N <= 32): the partial sums of their K splits:
@@ -266,22 +276,22 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * twice as wide as tall, 23 / 24 for K of at most 64 that is a multiple of
  * 16 / not a multiple of 16 (multiples of 32 excepted), else 28; otherwise
  * 30 under 256 rows or for wide products, 20 / 21 for K of at most 64 that
- * is not a multiple of 32, else 29); 1..11 = a fixed
- * configuration of the 128 x 128 output tile (K slice 16 or 32, 3 or 4
- * pipeline stages, a dedicated TMA warp or TMA issued by a compute thread,
- * one or two CTAs per SM, packed or scalar FMAs); 12 = 64 x 256,
- * 13 = 256 x 64 (four warps, two CTAs per SM); 14 = 128 x 256,
- * 15 = 256 x 128, 16 = 64 x 512, 17 = 512 x 64, 18 = 32 x 1024,
- * 19 = 1024 x 32, 20 / 21 = 256 x 128 with K slices of 16 / 8 and
- * 6 / 8 stages (eight warps, one CTA per SM); 22 = 256 x 128 and
- * 26 = 128 x 256 with 2 stages, 23 / 25 = 256 x 128 with K slices of 16
- * and 4 stages, 24 = 256 x 128 with K slices of 8 and 8 stages, all five
- * storing C through shared memory: by TMA when beta == 0 and C is 16-byte
- * aligned, in row runs of plain stores when C is not 16-byte aligned;
- * 27 / 28 / 29 / 30 = 26 / 22 / 15 / 14 with 16-byte A reads and only the
- * A fragments double buffered, the inner loop that 16, 17, 23 and 24 use
- * as well (see fp32_sgemm_gb300/csrc/sgemm_algo*.cu).
- * In math mode 1
+ * is not a multiple of 32, else 29).  Fixed configurations (every one
+ * but 10 is eight warps in one CTA per SM; fp32_sgemm_gb300/csrc/
+ * sgemm_algo*.cu):
+ *   10 = 128 x 128, four warps, two CTAs per SM;
+ *   16 = 64 x 512, 17 = 512 x 64, 18 = 32 x 1024, 19 = 1024 x 32;
+ *   20 / 21 = 256 x 128 with K slices of 16 / 8 (6 / 8 stages);
+ *   23 / 24 = 256 x 128 with K slices of 16 / 8 (4 / 8 stages) and C
+ *   through shared memory;
+ *   27 / 28 = 128 x 256 / 256 x 128, K slices of 32, 2 stages, C through
+ *   shared memory (by TMA when beta == 0 and C is 16-byte aligned, in row
+ *   runs of plain stores when C is not 16-byte aligned);
+ *   29 / 30 = 256 x 128 / 128 x 256, K slices of 32, 4 stages, C from
+ *   registers.
+ * Other numbers up to 30 (configurations measured slower and no longer
+ * built) return INVALID_VALUE, here or, for 1..3 set in math mode 0, from
+ * the product call.  In math mode 1
  * (3xTF32) the values 1..3 pick the tensor-core tile instead: 128 x 128,
  * 128 x 192 or 128 x 256.  Every configuration computes the same result up
  * to summation order.
@@ -408,7 +418,8 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
  *     ordering) race on the array: order them on one stream.
  *   - Operands that need repacking (base not 16-byte aligned or row pitch not
  *     a multiple of 4 floats) must fit in the array: M * round_up(K, 4) and
- *     K * round_up(N, 4) floats together at most 32 MiB minus 256 bytes;
+ *     K * round_up(N, 4) floats together at most 32 MiB minus 32 KiB (the
+ *     array's first 32 KiB are the control block a handle has of its own);
  *     larger ones return SGEMM_STATUS_NOT_SUPPORTED before anything is
  *     enqueued.  Stream-K is used only when its scratch fits as well.
  *   - Every wait inside these kernels is bounded (2 s by default, see

@@ -137,6 +137,13 @@ def test_null_handle_rejected(lib):
     assert lib.sgemmDestroy(None) == 0
 
 
+def test_configurations_not_built_are_rejected(lib):
+    # Numbers of tile configurations that are not built (measured slower)
+    # are refused before the handle is touched (a fake pointer here).
+    for algo in (4, 9, 11, 15, 22, 25, 26, 31, -1):
+        assert lib.sgemmSetAlgo(F, algo) == _binding.Status.INVALID_VALUE
+
+
 def test_no_alloc_settings_validated_on_host(lib):
     # Rejected before any CUDA call (this machine may have no GPU).
     assert lib.sgemmNoAllocSetWaitTimeout(999_999) == _binding.Status.INVALID_VALUE

@@ -85,12 +85,13 @@ def test_ffma_pipeline_waits_expire(sg, which, site):
 
 
 def test_ffma_stream_k_flag_wait_expires(sg):
-    # One tile whose K range is split over 16 CTAs; CTA 0 finishes it and
-    # waits for the other 15 partial tiles' flags, which never come.
+    # Four tiles of 16 K slices, one slice per CTA: the CTA holding a tile's
+    # first slice waits for the other 15 partial tiles' flags, which never
+    # come.
     h = sg.Handle()
     h.set_algo(28)
     h.set_schedule(2)
-    _expire_then_recover(sg, h, 256, 128, 4096, FLAG, SITE_FLAG,
+    _expire_then_recover(sg, h, 512, 256, 512, FLAG, SITE_FLAG, expect_ctas=64,
                          plan_check=lambda pl: pl["stream_k"] == 1 or pytest.fail(str(pl)))
     h.close()
 
