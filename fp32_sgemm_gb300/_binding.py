@@ -44,7 +44,8 @@ class Plan(ctypes.Structure):
                 ("tile_k", ctypes.c_int), ("stages", ctypes.c_int), ("ctas", ctypes.c_int),
                 ("packs_a", ctypes.c_int), ("packs_b", ctypes.c_int),
                 ("vector_epilogue", ctypes.c_int), ("kind", ctypes.c_int),
-                ("stream_k", ctypes.c_int), ("raster_group", ctypes.c_int)]
+                ("stream_k", ctypes.c_int), ("raster_group", ctypes.c_int),
+                ("edge_cols", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -166,8 +166,36 @@ void launch_skinny_tma(bool small_m, const CUtensorMap &tmA, const CUtensorMap &
 // Auxiliary kernels (sgemm_aux.cu); all take a batch (matrix z at base + z * stride).
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t stride_c, int batch,
                     cudaStream_t s);
-void launch_pack_rows(const float *src, int64_t ld_src, int64_t s_src, float *dst, int64_t ld_dst,
-                      int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);
+// One launch of operand preparation before the main kernel: up to two
+// repacks (rows x cols matrices, batch of them, into pitch ld_dst) and the
+// edge job (C's last r columns, r <= kEdgeMaxCols, that the main kernel
+// leaves out).  Unused parts: npack = 0 / 1, edge.r = 0.
+constexpr int kEdgeMaxCols = 8;
+struct PackJob {
+    const float *src;
+    int64_t ld_src, s_src;
+    float *dst;
+    int64_t ld_dst, s_dst;
+    int rows, cols, batch;
+    int64_t groups, units;   // set by launch_prep
+};
+struct EdgeJob {
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+    int M, K, n0, r;        // columns [n0, n0 + r) of C
+    float alpha, beta;
+};
+struct PrepArgs {
+    PackJob pack[2];
+    int npack;
+    EdgeJob edge;
+    int edge_blocks;         // set by launch_prep
+};
+cudaError_t launch_prep(PrepArgs p, cudaStream_t s);
 // src[r][c] -> dst[c][r]; with dst2 != NULL the TF32 split: dst = hi, dst2 = lo.
 void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
                       int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);

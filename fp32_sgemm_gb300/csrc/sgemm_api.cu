@@ -216,6 +216,10 @@ struct Plan {
     bool skinny_tma = false;        // TMA-fed skinny kernels (operands read in place)
     sg::SkinnyTmaGeom skinny_geom;
     int small_splits = 1;           // small-product kernel (kind 5): CTAs per block of C
+    // FFMA path: columns [n_main, N) of C are computed by the edge job of
+    // the preparation launch instead of a last tile column that thin.
+    int64_t n_main = 0;
+    int edge_cols = 0;
 };
 
 // Configuration 29 (256 x 128 tile, eight consumer warps, one CTA per SM,
@@ -257,6 +261,10 @@ bool thin_ffma_preferred(const sgemmContext *h, const Problem &q) {
 // 128 x 128^3 (2^28) 22.7 vs 27.4 us, the tile kernel wins.  Only in the
 // automatic FFMA setting (a pinned tile configuration or schedule, or math
 // mode 1, keeps the kernel asked for).
+// Edge columns are split off only when M x K is at least this (below, the
+// saved padding is worth less than the work of the edge job).
+constexpr double kEdgeMinMK = double(1 << 21);
+
 constexpr int64_t kSmallMaxDim = 1024;
 constexpr int64_t kSmallMaxK = 8192;
 constexpr int64_t kSmallMaxWork = int64_t(1) << 27;   // batch x M x N x K multiply-adds
@@ -548,8 +556,20 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     if (pl.algo_index < 0) return SGEMM_STATUS_INVALID_VALUE;   // a configuration that is not built
     pl.variant = (q.beta == 0.0f ? 0 : 2) + (pl.pub.vector_epilogue ? 0 : 1);
     KernelEntry &e = g_kernels[pl.algo_index][pl.variant];
+    // A last tile column of at most kEdgeMaxCols columns would multiply
+    // mostly zero padding (4095 x 4097 x 1023: 16 tiles of 256 x 128 for one
+    // column, 3% of the launch); in the automatic setting, when there is
+    // enough work for that to matter, those columns go to the edge job of
+    // the preparation launch, and the main kernel covers whole tiles only.
+    pl.n_main = q.N;
+    const int64_t edge = q.N % e.bn;
+    if (h->algo == 0 && q.opA == 0 && q.opB == 0 && q.batch == 1 && edge >= 1 && edge <= sg::kEdgeMaxCols &&
+        q.N > e.bn && double(q.M) * double(q.K) >= kEdgeMinMK) {
+        pl.edge_cols = int(edge);
+        pl.n_main = q.N - edge;
+    }
     pl.tiles_m = int(ceil_div(q.M, e.bm));
-    pl.tiles_n = int(ceil_div(q.N, e.bn));
+    pl.tiles_n = int(ceil_div(pl.n_main, e.bn));
     const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * q.batch;
     if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.num_tiles = int(tiles);
@@ -582,7 +602,11 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     pl.pub.tile_n = e.bn;
     pl.pub.tile_k = e.bk;
     pl.pub.stages = e.stages;
-    pl.pub.launches = 1 + pl.pub.packs_a + pl.pub.packs_b;
+    pl.pub.edge_cols = pl.edge_cols;
+    // Transposes are launches of their own; repacks and the edge job share
+    // one preparation launch.
+    pl.pub.launches = 1 + (pl.prep_a == 2) + (pl.prep_b == 2) +
+                      ((pl.prep_a == 1 || pl.prep_b == 1 || pl.edge_cols > 0) ? 1 : 0);
     return SGEMM_STATUS_SUCCESS;
 }
 
@@ -796,23 +820,34 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     const float *Ause = q.A, *Buse = q.B;
     // Stream-K scratch is optional: without room for it, whole tiles are used.
     const bool use_sk = sk_usable(h, pl, pl.ws_a + pl.ws_b, g_kernels[pl.algo_index][pl.variant].threads / 32);
-    const int M = int(q.M), N = int(q.N), K = int(q.K), batch = int(q.batch);
-    if (pl.prep_a || pl.prep_b) {
-        if (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b) return SGEMM_STATUS_WORKSPACE_REQUIRED;
+    // The main kernel covers columns [0, n_main) of C.
+    const int M = int(q.M), N = int(pl.n_main), K = int(q.K), batch = int(q.batch);
+    if (pl.prep_a || pl.prep_b || pl.edge_cols) {
+        if ((pl.prep_a || pl.prep_b) && (h->ws == nullptr || h->ws_bytes < pl.ws_a + pl.ws_b))
+            return SGEMM_STATUS_WORKSPACE_REQUIRED;
         char *ws = static_cast<char *>(h->ws);
+        sg::PrepArgs prep{};
         if (pl.prep_a) {
             float *Ap = reinterpret_cast<float *>(ws);
-            if (pl.prep_a == 1) sg::launch_pack_rows(q.A, q.lda, q.sa, Ap, pl.lda_p, pl.sa_p, M, K, batch, stream);
-            else sg::launch_transpose(q.A, q.lda, q.sa, Ap, nullptr, pl.lda_p, pl.sa_p, K, M, batch, stream);
+            if (pl.prep_a == 1)
+                prep.pack[prep.npack++] = sg::PackJob{q.A, q.lda, q.sa, Ap, pl.lda_p, pl.sa_p, M, K, batch, 0, 0};
+            else
+                sg::launch_transpose(q.A, q.lda, q.sa, Ap, nullptr, pl.lda_p, pl.sa_p, K, M, batch, stream);
             Ause = Ap;
         }
         if (pl.prep_b) {
             float *Bp = reinterpret_cast<float *>(ws + pl.ws_a);
-            if (pl.prep_b == 1) sg::launch_pack_rows(q.B, q.ldb, q.sb, Bp, pl.ldb_p, pl.sb_p, K, N, batch, stream);
-            else sg::launch_transpose(q.B, q.ldb, q.sb, Bp, nullptr, pl.ldb_p, pl.sb_p, N, K, batch, stream);
+            if (pl.prep_b == 1)
+                prep.pack[prep.npack++] = sg::PackJob{q.B, q.ldb, q.sb, Bp, pl.ldb_p, pl.sb_p, K, N, batch, 0, 0};
+            else
+                sg::launch_transpose(q.B, q.ldb, q.sb, Bp, nullptr, pl.ldb_p, pl.sb_p, int(q.N), K, batch, stream);
             Buse = Bp;
         }
+        if (pl.edge_cols)
+            prep.edge = sg::EdgeJob{q.A, q.lda, q.B, q.ldb, q.C, q.ldc, M, K, N, pl.edge_cols, q.alpha, q.beta};
         if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
+        if ((prep.npack > 0 || pl.edge_cols) && sg::launch_prep(prep, stream) != cudaSuccess)
+            return SGEMM_STATUS_LAUNCH_FAILED;
     }
 
     int variant = pl.variant;
@@ -823,7 +858,7 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
         // encoder rejects takes the st.global epilogue of the same tile.
         const KernelEntry &ec = g_kernels[pl.algo_index][variant];
         const int64_t sc = q.batch == 1 ? q.ldc * q.M : q.sc;
-        if (encode_3d(&tmC, q.C, q.N, q.M, q.batch, q.ldc, sc, ec.c_box_cols, ec.c_box_rows,
+        if (encode_3d(&tmC, q.C, pl.n_main, q.M, q.batch, q.ldc, sc, ec.c_box_cols, ec.c_box_rows,
                       CU_TENSOR_MAP_SWIZZLE_NONE) != SGEMM_STATUS_SUCCESS)
             variant = 1;
     }
@@ -832,7 +867,8 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
     // Boxes of at most 256 rows / columns; wider tiles load several.
     st = encode_3d(&tmA, Ause, q.K, q.M, q.batch, pl.lda_p, pl.sa_p, e.bk, std::min(e.bm, 256), swizzle_for_bk(e.bk));
     if (st != SGEMM_STATUS_SUCCESS) return st;
-    st = encode_3d(&tmB, Buse, q.N, q.K, q.batch, pl.ldb_p, pl.sb_p, std::min(e.bn, 256), e.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = encode_3d(&tmB, Buse, pl.n_main, q.K, q.batch, pl.ldb_p, pl.sb_p, std::min(e.bn, 256), e.bk,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != SGEMM_STATUS_SUCCESS) return st;
 
     sg::GemmArgs args{};

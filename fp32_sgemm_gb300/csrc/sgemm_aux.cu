@@ -23,31 +23,103 @@ __global__ void sgemm_scale_c_kernel(int M, int N, float beta, float *C, int64_t
         }
 }
 
-// Copy rows x cols row-major matrices into buffers with row pitch ld_dst (a
-// multiple of 4 floats, 16-byte aligned rows), so that TMA can address them.
-// A thread moves 4 consecutive elements of a row per step: four 4-byte
-// loads (the source pitch may be odd) and one 16-byte store; the padding
-// columns up to the next multiple of 4 are written as zeros.  One flat
-// grid-stride loop over (matrix, row, 4-column group) keeps every CTA busy
-// whatever the shape (a CTA per row left most of a short row's CTA idle).
-__global__ void __launch_bounds__(256)
-sgemm_pack_rows_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
-                       float *__restrict__ dst, int64_t ld_dst, int64_t s_dst, int rows, int cols,
-                       int batch) {
-    const int64_t groups = (cols + 3) / 4;
-    const int64_t units = (int64_t)batch * rows * groups;
-    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-         u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t zr = u / groups;
-        const int c = (int)(u - zr * groups) * 4;
-        const int64_t z = zr / rows, r = zr - z * rows;
-        const float *sr = src + z * s_src + r * ld_src + c;
-        float4 v;
-        v.x = sr[0];
-        v.y = c + 1 < cols ? sr[1] : 0.f;
-        v.z = c + 2 < cols ? sr[2] : 0.f;
-        v.w = c + 3 < cols ? sr[3] : 0.f;
-        *reinterpret_cast<float4 *>(dst + z * s_dst + r * ld_dst + c) = v;
+// Operand preparation in one launch (launched with programmatic stream
+// serialisation: it waits for the kernel before it, and lets the main kernel
+// after it be placed as its CTAs finish):
+//   * up to two repack jobs: rows x cols row-major matrices copied into
+//     buffers whose row pitch is a multiple of 4 floats (16-byte aligned
+//     rows), so that TMA can address them; a thread moves 4 consecutive
+//     elements of a row per step (four 4-byte loads, as the source pitch
+//     may be odd, and one 16-byte store; the padding up to the next
+//     multiple of 4 is written as zeros), in one flat grid-stride loop over
+//     (job, matrix, row, 4-column group) that keeps every CTA busy whatever
+//     the shapes;
+//   * the edge job: the last r <= kEdgeMaxCols columns of C when the main
+//     kernel leaves them out (a last tile column that thin would multiply
+//     mostly padding): one warp per row of C, lanes striding over k with
+//     FP32 FMAs, then a fixed butterfly sum across the warp, so the result
+//     is the same every run.  C = alpha * sum (+ beta * C, C not read when
+//     beta == 0).  Blocks [0, edge_blocks) take the edge job, the rest the
+//     repacks.
+// At most 64 registers (4 CTAs per SM): the repack role is bound by the
+// latency of its 4-byte loads and needs many of them in flight, so each of
+// its threads moves four units at a time, and the edge role keeps four k
+// steps' loads in flight.
+__device__ __forceinline__ void prep_pack_load(const PackJob &j, int64_t v, float4 &w, float *&dst) {
+    const int64_t zr = v / j.groups;
+    const int c = (int)(v - zr * j.groups) * 4;
+    const int64_t z = zr / j.rows, r = zr - z * j.rows;
+    const float *sr = j.src + z * j.s_src + r * j.ld_src + c;
+    w.x = sr[0];
+    w.y = c + 1 < j.cols ? sr[1] : 0.f;
+    w.z = c + 2 < j.cols ? sr[2] : 0.f;
+    w.w = c + 3 < j.cols ? sr[3] : 0.f;
+    dst = j.dst + z * j.s_dst + r * j.ld_dst + c;
+}
+
+__global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constant__ PrepArgs p) {
+    griddep_wait();
+    griddep_launch_dependents();
+    if ((int)blockIdx.x < p.edge_blocks) {
+        const EdgeJob &e = p.edge;
+        const int lane = threadIdx.x & 31;
+        const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+        if (row >= e.M) return;
+        float s[kEdgeMaxCols];
+#pragma unroll
+        for (int j = 0; j < kEdgeMaxCols; ++j) s[j] = 0.f;
+        const float *a = e.A + (int64_t)row * e.lda;
+        // The sums take k in ascending order either way.
+        int k = lane;
+        for (; k + 3 * 32 < e.K; k += 4 * 32) {
+            float av[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) av[u] = a[k + 32 * u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float *b = e.B + (int64_t)(k + 32 * u) * e.ldb + e.n0;
+#pragma unroll
+                for (int j = 0; j < kEdgeMaxCols; ++j)
+                    if (j < e.r) s[j] = fmaf(av[u], b[j], s[j]);
+            }
+        }
+        for (; k < e.K; k += 32) {
+            const float av = a[k];
+            const float *b = e.B + (int64_t)k * e.ldb + e.n0;
+#pragma unroll
+            for (int j = 0; j < kEdgeMaxCols; ++j)
+                if (j < e.r) s[j] = fmaf(av, b[j], s[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kEdgeMaxCols; ++j)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+        if (lane == 0) {
+            float *c = e.C + (int64_t)row * e.ldc + e.n0;
+#pragma unroll
+            for (int j = 0; j < kEdgeMaxCols; ++j)
+                if (j < e.r) c[j] = e.beta == 0.0f ? e.alpha * s[j] : fmaf(e.beta, c[j], e.alpha * s[j]);
+        }
+        return;
+    }
+    const int64_t total = p.pack[0].units + p.pack[1].units;
+    const int64_t stride = (int64_t)(gridDim.x - p.edge_blocks) * blockDim.x;
+    for (int64_t u0 = (int64_t)(blockIdx.x - p.edge_blocks) * blockDim.x + threadIdx.x; u0 < total;
+         u0 += 4 * stride) {
+        float4 w[4];
+        float *dst[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t u = u0 + q * stride;
+            dst[q] = nullptr;
+            if (u < total) {
+                const bool second = u >= p.pack[0].units;
+                prep_pack_load(second ? p.pack[1] : p.pack[0], second ? u - p.pack[0].units : u, w[q], dst[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (dst[q] != nullptr) *reinterpret_cast<float4 *>(dst[q]) = w[q];
     }
 }
 
@@ -215,11 +287,30 @@ void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t str
     sgemm_scale_c_kernel<<<grid, 256, 0, s>>>(M, N, beta, C, ldc, stride_c, batch);
 }
 
-void launch_pack_rows(const float *src, int64_t ld_src, int64_t s_src, float *dst, int64_t ld_dst,
-                      int64_t s_dst, int rows, int cols, int batch, cudaStream_t s) {
-    const int64_t units = int64_t(batch) * rows * cdiv(cols, 4);
-    const unsigned blocks = unsigned(std::max<int64_t>(1, std::min<int64_t>(cdiv(units, 256), 4096)));
-    sgemm_pack_rows_kernel<<<blocks, 256, 0, s>>>(src, ld_src, s_src, dst, ld_dst, s_dst, rows, cols, batch);
+cudaError_t launch_prep(PrepArgs p, cudaStream_t s) {
+    int64_t units = 0;
+    for (int i = 0; i < 2; ++i) {
+        PackJob &j = p.pack[i];
+        if (i >= p.npack) j = PackJob{};
+        j.groups = (j.cols + 3) / 4;
+        j.units = (int64_t)j.batch * j.rows * j.groups;
+        units += j.units;
+    }
+    p.edge_blocks = p.edge.r > 0 ? (int)cdiv(p.edge.M, 8) : 0;
+    // Four units per thread per step; at most four CTAs per SM stay resident.
+    const int pack_blocks = (int)std::max<int64_t>(units > 0 ? 1 : 0, std::min<int64_t>(cdiv(units, 4 * 256), 4096));
+    const int blocks = p.edge_blocks + pack_blocks;
+    if (blocks == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sgemm_prep_kernel, p);
 }
 
 void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
@@ -263,7 +354,7 @@ void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *h
 cudaError_t preload_aux_kernels() {
     const void *fns[] = {
         reinterpret_cast<const void *>(&sgemm_scale_c_kernel),
-        reinterpret_cast<const void *>(&sgemm_pack_rows_kernel),
+        reinterpret_cast<const void *>(&sgemm_prep_kernel),
         reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, true, true>),
         reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, false, true>),
         reinterpret_cast<const void *>(&sgemm_transpose_kernel<true, false, false>),

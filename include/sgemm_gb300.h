@@ -238,7 +238,8 @@ sgemmStatus_t sgemmHostEx(sgemmHandle_t handle, int64_t M, int64_t N, int64_t K,
  * the number of CTAs of the main kernel and whether operands are repacked.
  */
 typedef struct sgemmPlan {
-    int launches;       /* kernels one call enqueues (0 for M == 0 or N == 0) */
+    int launches;       /* kernels one call enqueues (0 for M == 0 or N == 0); repacks of A and
+                           B and the edge columns share one preparation launch */
     int tile_m, tile_n; /* output tile of the main kernel (0 if none) */
     int tile_k;         /* K slice staged per pipeline step */
     int stages;         /* shared-memory pipeline depth (kind 4: 6 when the TMA-fed
@@ -258,6 +259,10 @@ typedef struct sgemmPlan {
     int stream_k;       /* 1 if K slices of some tiles are split between CTAs (stream-K) */
     int raster_group;   /* tile rows per band of the tile order (tiles running together
                            share rows of A and columns of B in L2); 0 if no tiles */
+    int edge_cols;      /* kind 1: the last edge_cols (<= 8) columns of C are computed in the
+                           preparation launch (a warp per row) instead of by a last tile column
+                           that thin; the main kernel covers whole tiles.  Only in the automatic
+                           setting, for NN products of one matrix with M * K >= 2^21 */
 } sgemmPlan_t;
 
 sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,

@@ -628,3 +628,43 @@ def test_tma_store_epilogue_batched(sg, handle):
     pad = torch.as_strided(flat, (batch, M, ldc - N), (sc, ldc, 1), N)
     assert torch.isnan(pad).all()
 
+
+
+# Thin last tile columns (N mod 128 in 1..8, M x K >= 2^21) go to the edge
+# job of the preparation launch; the main kernel covers whole tiles.
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,alpha,beta", [
+    (2048, 4096 + 1, 1024, None, None, None, 1.0, 0.0),       # operands read in place
+    (2048, 2048 + 3, 1100, 1101, 2051, 2053, 0.5, 0.25),      # both repacked, C read
+    (1500, 1024 + 8, 2048, None, 1040, 1036, 1.0, -1.0),      # C 16-byte aligned, read
+    (3000, 512 + 5, 800, 801, None, None, 2.0, 0.0),
+])
+def test_edge_columns_split_off(sg, handle, M, N, K, lda, ldb, ldc, alpha, beta):
+    handle.set_algo(0)
+    for kind in ("integer", "uniform"):
+        p = inputs.make_problem(M, N, K, seed=M + N + K, kind=kind, alpha=alpha, beta=beta,
+                                lda=lda, ldb=ldb, ldc=ldc)
+        A = _to_dev(p.A)[:, :K]
+        B = _to_dev(p.B)[:, :N]
+        Cbuf = _to_dev(p.C0 if p.C0 is not None else np.full((M, N), np.nan, np.float32))
+        plan = handle.plan(A, B, Cbuf[:, :N], alpha, beta)
+        assert plan["kind"] == 1 and plan["edge_cols"] == N % plan["tile_n"], plan
+        got = _gpu(sg, handle, p)
+        if kind == "integer":
+            np.testing.assert_array_equal(got[:, :N].astype(np.float64), _ref(p))
+        else:
+            _assert_close(got[:, :N], _ref(p))
+        if p.C0 is not None and p.C0.shape[1] > N:
+            np.testing.assert_array_equal(got[:, N:], p.C0[:, N:])   # ldc padding untouched
+
+
+def test_edge_columns_only_in_the_automatic_setting(sg, handle):
+    p = inputs.make_problem(2048, 4097, 1024, seed=9, kind="integer")
+    A, B = _to_dev(p.A), _to_dev(p.B)
+    C = torch.zeros((2048, 4097), device="cuda")
+    handle.set_algo(0)
+    assert handle.plan(A, B, C)["edge_cols"] == 1
+    handle.set_algo(28)
+    plan = handle.plan(A, B, C)
+    handle.set_algo(0)
+    assert plan["edge_cols"] == 0
+    np.testing.assert_array_equal(_gpu(sg, handle, p, algo=28).astype(np.float64), _ref(p))
