@@ -171,6 +171,8 @@ void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t str
 // edge job (C's last r columns, r <= kEdgeMaxCols, that the main kernel
 // leaves out).  Unused parts: npack = 0 / 1, edge.r = 0.
 constexpr int kEdgeMaxCols = 8;
+// The edge job's B columns (K x r floats) are staged whole in shared memory.
+constexpr int kEdgeMaxStrip = 12288;   // floats (48 KB)
 struct PackJob {
     const float *src;
     int64_t ld_src, s_src;
@@ -193,9 +195,8 @@ struct PrepArgs {
     PackJob pack[2];
     int npack;
     EdgeJob edge;
-    int edge_blocks;         // set by launch_prep
 };
-cudaError_t launch_prep(PrepArgs p, cudaStream_t s);
+cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t s);
 // src[r][c] -> dst[c][r]; with dst2 != NULL the TF32 split: dst = hi, dst2 = lo.
 void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *dst, float *dst2,
                       int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s);

@@ -564,7 +564,7 @@ sgemmStatus_t make_plan(const sgemmContext *h, const Problem &q, Plan &pl) {
     pl.n_main = q.N;
     const int64_t edge = q.N % e.bn;
     if (h->algo == 0 && q.opA == 0 && q.opB == 0 && q.batch == 1 && edge >= 1 && edge <= sg::kEdgeMaxCols &&
-        q.N > e.bn && double(q.M) * double(q.K) >= kEdgeMinMK) {
+        q.N > e.bn && double(q.M) * double(q.K) >= kEdgeMinMK && q.K * edge <= sg::kEdgeMaxStrip) {
         pl.edge_cols = int(edge);
         pl.n_main = q.N - edge;
     }
@@ -846,7 +846,7 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
         if (pl.edge_cols)
             prep.edge = sg::EdgeJob{q.A, q.lda, q.B, q.ldb, q.C, q.ldc, M, K, N, pl.edge_cols, q.alpha, q.beta};
         if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
-        if ((prep.npack > 0 || pl.edge_cols) && sg::launch_prep(prep, stream) != cudaSuccess)
+        if ((prep.npack > 0 || pl.edge_cols) && sg::launch_prep(prep, h->sm_count, stream) != cudaSuccess)
             return SGEMM_STATUS_LAUNCH_FAILED;
     }
 

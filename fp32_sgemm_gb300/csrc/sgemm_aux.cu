@@ -25,101 +25,132 @@ __global__ void sgemm_scale_c_kernel(int M, int N, float beta, float *C, int64_t
 
 // Operand preparation in one launch (launched with programmatic stream
 // serialisation: it waits for the kernel before it, and lets the main kernel
-// after it be placed as its CTAs finish):
-//   * up to two repack jobs: rows x cols row-major matrices copied into
-//     buffers whose row pitch is a multiple of 4 floats (16-byte aligned
-//     rows), so that TMA can address them; a thread moves 4 consecutive
-//     elements of a row per step (four 4-byte loads, as the source pitch
-//     may be odd, and one 16-byte store; the padding up to the next
-//     multiple of 4 is written as zeros), in one flat grid-stride loop over
-//     (job, matrix, row, 4-column group) that keeps every CTA busy whatever
-//     the shapes;
+// after it be placed as its CTAs finish), one persistent wave of CTAs:
 //   * the edge job: the last r <= kEdgeMaxCols columns of C when the main
 //     kernel leaves them out (a last tile column that thin would multiply
 //     mostly padding): one warp per row of C, lanes striding over k with
 //     FP32 FMAs, then a fixed butterfly sum across the warp, so the result
 //     is the same every run.  C = alpha * sum (+ beta * C, C not read when
-//     beta == 0).  Blocks [0, edge_blocks) take the edge job, the rest the
-//     repacks.
-// At most 64 registers (4 CTAs per SM): the repack role is bound by the
-// latency of its 4-byte loads and needs many of them in flight, so each of
-// its threads moves four units at a time, and the edge role keeps four k
-// steps' loads in flight.
-__device__ __forceinline__ void prep_pack_load(const PackJob &j, int64_t v, float4 &w, float *&dst) {
-    const int64_t zr = v / j.groups;
-    const int c = (int)(v - zr * j.groups) * 4;
-    const int64_t z = zr / j.rows, r = zr - z * j.rows;
-    const float *sr = j.src + z * j.s_src + r * j.ld_src + c;
-    w.x = sr[0];
-    w.y = c + 1 < j.cols ? sr[1] : 0.f;
-    w.z = c + 2 < j.cols ? sr[2] : 0.f;
-    w.w = c + 3 < j.cols ? sr[3] : 0.f;
-    dst = j.dst + z * j.s_dst + r * j.ld_dst + c;
-}
-
+//     beta == 0);
+//   * then up to two repack jobs: rows x cols row-major matrices copied
+//     into buffers whose row pitch is a multiple of 4 floats (16-byte
+//     aligned rows), so that TMA can address them; the padding up to the
+//     next multiple of 4 is written as zeros.
+// At most 64 registers (4 CTAs per SM): both roles are bound by the latency
+// of their loads, so each keeps many loads in flight with short chains.
 __global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constant__ PrepArgs p) {
     griddep_wait();
     griddep_launch_dependents();
-    if ((int)blockIdx.x < p.edge_blocks) {
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;                  // warp in block
+    const int wpb = blockDim.x >> 5;
+    if (p.edge.r > 0) {
+        // B's columns [n0, n0 + r) are a strided gather (one cache line per
+        // k): every block stages all of them in shared memory once, column
+        // by column so that lanes reading consecutive k hit consecutive
+        // banks; then its warps take rows of C round robin.
+        extern __shared__ float bstrip[];   // [r][K]
         const EdgeJob &e = p.edge;
-        const int lane = threadIdx.x & 31;
-        const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-        if (row >= e.M) return;
-        float s[kEdgeMaxCols];
+        for (int t = threadIdx.x; t < e.K * e.r; t += blockDim.x) {
+            const int kk = t / e.r, jj = t - kk * e.r;
+            bstrip[jj * e.K + kk] = e.B[(int64_t)kk * e.ldb + e.n0 + jj];
+        }
+        __syncthreads();
+        for (int row = blockIdx.x * wpb + wib; row < e.M; row += gridDim.x * wpb) {
+            float s[kEdgeMaxCols];
 #pragma unroll
-        for (int j = 0; j < kEdgeMaxCols; ++j) s[j] = 0.f;
-        const float *a = e.A + (int64_t)row * e.lda;
-        // The sums take k in ascending order either way.
-        int k = lane;
-        for (; k + 3 * 32 < e.K; k += 4 * 32) {
-            float av[4];
+            for (int j = 0; j < kEdgeMaxCols; ++j) s[j] = 0.f;
+            const float *a = e.A + (int64_t)row * e.lda;
+            // Sixteen k steps' loads of A in flight per lane; every sum takes
+            // k in ascending order.
+            int k = lane;
+            for (; k + 15 * 32 < e.K; k += 16 * 32) {
+                float av[16];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) av[u] = a[k + 32 * u];
+                for (int u = 0; u < 16; ++u) av[u] = a[k + 32 * u];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float *b = e.B + (int64_t)(k + 32 * u) * e.ldb + e.n0;
+                for (int u = 0; u < 16; ++u)
+#pragma unroll
+                    for (int j = 0; j < kEdgeMaxCols; ++j)
+                        if (j < e.r) s[j] = fmaf(av[u], bstrip[j * e.K + k + 32 * u], s[j]);
+            }
+            for (; k < e.K; k += 32) {
+                const float av = a[k];
 #pragma unroll
                 for (int j = 0; j < kEdgeMaxCols; ++j)
-                    if (j < e.r) s[j] = fmaf(av[u], b[j], s[j]);
+                    if (j < e.r) s[j] = fmaf(av, bstrip[j * e.K + k], s[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kEdgeMaxCols; ++j)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+            if (lane == 0) {
+                float *c = e.C + (int64_t)row * e.ldc + e.n0;
+#pragma unroll
+                for (int j = 0; j < kEdgeMaxCols; ++j)
+                    if (j < e.r) c[j] = e.beta == 0.0f ? e.alpha * s[j] : fmaf(e.beta, c[j], e.alpha * s[j]);
             }
         }
-        for (; k < e.K; k += 32) {
-            const float av = a[k];
-            const float *b = e.B + (int64_t)k * e.ldb + e.n0;
-#pragma unroll
-            for (int j = 0; j < kEdgeMaxCols; ++j)
-                if (j < e.r) s[j] = fmaf(av, b[j], s[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < kEdgeMaxCols; ++j)
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
-        if (lane == 0) {
-            float *c = e.C + (int64_t)row * e.ldc + e.n0;
-#pragma unroll
-            for (int j = 0; j < kEdgeMaxCols; ++j)
-                if (j < e.r) c[j] = e.beta == 0.0f ? e.alpha * s[j] : fmaf(e.beta, c[j], e.alpha * s[j]);
-        }
-        return;
     }
-    const int64_t total = p.pack[0].units + p.pack[1].units;
-    const int64_t stride = (int64_t)(gridDim.x - p.edge_blocks) * blockDim.x;
-    for (int64_t u0 = (int64_t)(blockIdx.x - p.edge_blocks) * blockDim.x + threadIdx.x; u0 < total;
-         u0 += 4 * stride) {
-        float4 w[4];
-        float *dst[4];
+
+    // Repacks: a warp per unit of 512 columns of one row (of either job,
+    // rows of all batch entries in turn).  The source row may start at any
+    // 4-byte offset (odd pitch): lane l reads the 16-byte aligned quad that
+    // holds the start of its 4-column group and takes the rest from lane
+    // l + 1's quad by a shuffle, so the row is read with 16-byte loads; a
+    // quad that reaches outside the row (its first or last) is read element
+    // by element, so nothing outside the row is touched.
+    const int64_t total = p.pack[0].units + p.pack[1].units;   // (row, chunk) units
+    const int64_t warps = (int64_t)gridDim.x * wpb;
+    for (int64_t w = (int64_t)blockIdx.x * wpb + wib; w < total; w += warps) {
+        const bool second = w >= p.pack[0].units;
+        const PackJob &j = second ? p.pack[1] : p.pack[0];
+        const int64_t v = second ? w - p.pack[0].units : w;
+        const int64_t chunks = (j.groups + 127) / 128;
+        const int64_t zr = v / chunks;
+        const int gbase = (int)(v - zr * chunks) * 128;
+        const int64_t z = zr / j.rows, r = zr - z * j.rows;
+        const float *src = j.src + z * j.s_src + r * j.ld_src;
+        float *dst = j.dst + z * j.s_dst + r * j.ld_dst;
+        const int ph = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3u);   // floats past a 16-byte boundary
+        const float *ab = src - ph;                                              // 16-byte aligned
+        const int cols = j.cols;
+        // Quad m of the aligned row holds row elements 4m - ph .. 4m - ph + 3.
+        auto quad = [&](int m) {
+            const int e0 = 4 * m - ph;
+            if (e0 >= 0 && e0 + 3 < cols) return *reinterpret_cast<const float4 *>(ab + 4 * m);
+            float4 q;
+            q.x = (e0 >= 0 && e0 < cols) ? ab[4 * m] : 0.f;
+            q.y = (e0 + 1 >= 0 && e0 + 1 < cols) ? ab[4 * m + 1] : 0.f;
+            q.z = (e0 + 2 >= 0 && e0 + 2 < cols) ? ab[4 * m + 2] : 0.f;
+            q.w = (e0 + 3 >= 0 && e0 + 3 < cols) ? ab[4 * m + 3] : 0.f;
+            return q;
+        };
+        float4 q4[4], n4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int64_t u = u0 + q * stride;
-            dst[q] = nullptr;
-            if (u < total) {
-                const bool second = u >= p.pack[0].units;
-                prep_pack_load(second ? p.pack[1] : p.pack[0], second ? u - p.pack[0].units : u, w[q], dst[q]);
-            }
+            const int g = gbase + 32 * q + lane;     // this lane's group: row elements 4g .. 4g + 3
+            // (With ph != 0 the quad after the last group may still hold the
+            // last elements of the row.)
+            q4[q] = (g < j.groups || (ph != 0 && g == j.groups)) ? quad(g) : make_float4(0.f, 0.f, 0.f, 0.f);
+            n4[q] = (lane == 31 && ph != 0 && g < j.groups) ? quad(g + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (dst[q] != nullptr) *reinterpret_cast<float4 *>(dst[q]) = w[q];
+        for (int q = 0; q < 4; ++q) {
+            const int g = gbase + 32 * q + lane;
+            // The next quad: lane + 1's, or (lane 31) loaded above.
+            float4 nx;
+            nx.x = __shfl_down_sync(0xffffffffu, q4[q].x, 1);
+            nx.y = __shfl_down_sync(0xffffffffu, q4[q].y, 1);
+            nx.z = __shfl_down_sync(0xffffffffu, q4[q].z, 1);
+            if (lane == 31) nx = n4[q];
+            float4 o;
+            if (ph == 0) o = q4[q];
+            else if (ph == 1) o = make_float4(q4[q].y, q4[q].z, q4[q].w, nx.x);
+            else if (ph == 2) o = make_float4(q4[q].z, q4[q].w, nx.x, nx.y);
+            else o = make_float4(q4[q].w, nx.x, nx.y, nx.z);
+            if (g < j.groups) *reinterpret_cast<float4 *>(dst + 4 * g) = o;
+        }
     }
 }
 
@@ -287,23 +318,24 @@ void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t str
     sgemm_scale_c_kernel<<<grid, 256, 0, s>>>(M, N, beta, C, ldc, stride_c, batch);
 }
 
-cudaError_t launch_prep(PrepArgs p, cudaStream_t s) {
+cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t s) {
     int64_t units = 0;
     for (int i = 0; i < 2; ++i) {
         PackJob &j = p.pack[i];
         if (i >= p.npack) j = PackJob{};
         j.groups = (j.cols + 3) / 4;
-        j.units = (int64_t)j.batch * j.rows * j.groups;
+        j.units = (int64_t)j.batch * j.rows * cdiv(j.groups, 128);   // (row, 512-column chunk)
         units += j.units;
     }
-    p.edge_blocks = p.edge.r > 0 ? (int)cdiv(p.edge.M, 8) : 0;
-    // Four units per thread per step; at most four CTAs per SM stay resident.
-    const int pack_blocks = (int)std::max<int64_t>(units > 0 ? 1 : 0, std::min<int64_t>(cdiv(units, 4 * 256), 4096));
-    const int blocks = p.edge_blocks + pack_blocks;
+    // One persistent wave: four CTAs of eight warps per SM, every warp takes
+    // edge rows and then repack units in turn.
+    const int64_t warps_needed = std::max<int64_t>(units, p.edge.r > 0 ? p.edge.M : 0);
+    const int blocks = (int)std::min<int64_t>(cdiv(warps_needed, 8), 4 * (int64_t)sms);
     if (blocks == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = p.edge.r > 0 ? size_t(p.edge.r) * size_t(p.edge.K) * 4 : 0;   // <= kEdgeMaxStrip floats
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -666,8 +666,10 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             // two rows x 16 columns (lanes 0-15 a run of one row, 16-31 the
             // next; conflict-free reads of one box), so a warp touches
             // 64-byte runs of C instead of 16-byte pieces of eight rows.
-            // With beta != 0 the C values of eight instructions are loaded
-            // before any is used.
+            // With beta != 0 the C values of a whole box (32 loads per
+            // thread; the accumulators are in the staging area by now, so the
+            // registers are free) are loaded before any is used: reading C
+            // eight loads at a time cost a memory round trip per eight.
             __syncwarp();
             stage_block();
             __syncwarp();
@@ -676,27 +678,33 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
             const int row_w = tm * BM + wm * Cfg::WTM;
             const int col_w = tn * BN + wn * Cfg::WTN;
             float *cb = p.C + (int64_t)bt * p.stride_c;
+            constexpr int PAIRS = Cfg::WTM / 2;                    // row pairs of a box
+            constexpr int NBOX = Cfg::WTN / Cfg::C_BOX_COLS;
+            constexpr int BOXES = 1;                               // boxes per round
 #pragma unroll 1
-            for (int j = 0; j < Cfg::WTN / Cfg::C_BOX_COLS; ++j) {
-                const int col = col_w + Cfg::C_BOX_COLS * j + c16;
-                const bool col_ok = col < p.N;
-#pragma unroll 1
-                for (int rp0 = 0; rp0 < Cfg::WTM / 2; rp0 += 8) {
-                    float cin[8];
-                    if constexpr (!BETA_ZERO) {
+            for (int j0 = 0; j0 < NBOX; j0 += BOXES) {
+                float cin[BOXES][PAIRS];
+                if constexpr (!BETA_ZERO) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int row = row_w + 2 * (rp0 + u) + half;
-                            cin[u] = (col_ok && row < p.M) ? cb[(int64_t)row * p.ldc + col] : 0.f;
+                    for (int jj = 0; jj < BOXES; ++jj) {
+                        const int col = col_w + Cfg::C_BOX_COLS * (j0 + jj) + c16;
+#pragma unroll
+                        for (int u = 0; u < PAIRS; ++u) {
+                            const int row = row_w + 2 * u + half;
+                            cin[jj][u] = (col < p.N && row < p.M) ? cb[(int64_t)row * p.ldc + col] : 0.f;
                         }
                     }
+                }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int r = 2 * (rp0 + u) + half;
+                for (int jj = 0; jj < BOXES; ++jj) {
+                    const int col = col_w + Cfg::C_BOX_COLS * (j0 + jj) + c16;
+#pragma unroll
+                    for (int u = 0; u < PAIRS; ++u) {
+                        const int r = 2 * u + half;
                         const int row = row_w + r;
-                        float v = stf[j * (Cfg::C_BOX_BYTES / 4) + r * Cfg::C_BOX_COLS + c16];
-                        if constexpr (!BETA_ZERO) v = fmaf(beta, cin[u], v);
-                        if (col_ok && row < p.M) cb[(int64_t)row * p.ldc + col] = v;
+                        float v = stf[(j0 + jj) * (Cfg::C_BOX_BYTES / 4) + r * Cfg::C_BOX_COLS + c16];
+                        if constexpr (!BETA_ZERO) v = fmaf(beta, cin[jj][u], v);
+                        if (col < p.N && row < p.M) cb[(int64_t)row * p.ldc + col] = v;
                     }
                 }
             }
