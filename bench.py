@@ -195,23 +195,62 @@ def measured_hbm():
         return 6800.0, "of fallback (6.8 TB/s)"
 
 
-def tensor_roofline(flops: float, kernel_ms: float) -> dict:
-    """Roofline of the 3xTF32 main kernel: three TF32 products per useful
-    multiply-add, against the TF32 dense peak (the measured bf16 tensor peak
-    times the nominal TF32/bf16 ratio 1.1/2.25)."""
-    bf16 = None
+def measure_tf32_peak(dev) -> float | None:
+    """Dense TF32 tensor throughput of this GPU, measured in this run: the
+    best of 10 cuBLAS TF32 products at 8192^3 through torch (a reference
+    figure for the roofline only; nothing of the library runs here)."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
     try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            bf16 = float(json.load(f)["bf16_tflops"])
-        basis = "of measured (bf16 burst x nominal tf32/bf16 1.1/2.25)"
-    except (OSError, KeyError, ValueError):
-        bf16 = 1900.0
-        basis = "of fallback (1.9 PFLOP/s bf16 x nominal tf32/bf16 1.1/2.25)"
-    peak = bf16 * 1.1 / 2.25
+        torch.backends.cuda.matmul.allow_tf32 = True
+        n = 8192
+        a = torch.rand(n, n, device=dev)
+        b = torch.rand(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = None
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def tensor_roofline(flops: float, kernel_ms: float, tf32_peak: float | None = None) -> dict:
+    """Roofline of the 3xTF32 main kernel: three TF32 products per useful
+    multiply-add, against the dense TF32 peak -- measured in this run (cuBLAS
+    TF32 at 8192^3) when given, else the measured bf16 tensor peak times the
+    nominal TF32/bf16 ratio 1.1/2.25.  useful_frac: the useful FP32 FLOPs
+    (2MNK) per second of the kernel over that same peak."""
+    if tf32_peak:
+        peak = tf32_peak
+        basis = "of measured (cuBLAS TF32 8192^3 in this run, best of 10)"
+    else:
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                bf16 = float(json.load(f)["bf16_tflops"])
+            basis = "of measured (bf16 burst x nominal tf32/bf16 1.1/2.25)"
+        except (OSError, KeyError, ValueError):
+            bf16 = 1900.0
+            basis = "of fallback (1.9 PFLOP/s bf16 x nominal tf32/bf16 1.1/2.25)"
+        peak = bf16 * 1.1 / 2.25
     achieved = 3.0 * flops / (kernel_ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": None, "peak_basis": basis,
-            "achieved_basis": "3 TF32 MMAs per useful FMA (hi*hi, hi*lo, lo*hi); split pre-pass excluded"}
+            "achieved_basis": "3 TF32 MMAs per useful FMA (hi*hi, hi*lo, lo*hi); split pre-pass excluded",
+            "useful_frac": achieved / 3.0 / peak}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -567,6 +606,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     # FFMA headline, which the metric defines against the FFMA peak).
     tensor_path = None
     if args.math == 0 and args.tensor_steps > 0:
+        tf32_peak = measure_tf32_peak(ctx.dev)
         handle.set_math_mode(1)
         run.ensure_workspace()
         tplan = handle.plan(*run.sets[0], w.alpha, w.beta)
@@ -579,7 +619,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
             "value": job_tflops(flops, world, t_step), "unit": "TFLOP/s",
             "ms_per_step": t_step, "steps": args.tensor_steps,
             "launches_per_step": tplan["launches"],
-            "roofline": tensor_roofline(flops, statistics.mean(t_k)),
+            "roofline": tensor_roofline(flops, statistics.mean(t_k), tf32_peak),
+            "useful_frac_per_call": (job_tflops(flops, world, t_step) / world) / tf32_peak if tf32_peak else None,
             "config": {"tile": f"{tplan['tile_m']}x{tplan['tile_n']}x{tplan['tile_k']}",
                        "schedule": "stream-K" if tplan["stream_k"] else "whole tiles",
                        "ctas": tplan["ctas"]},

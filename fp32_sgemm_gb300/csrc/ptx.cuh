@@ -221,6 +221,15 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
+// Prefetch a 3-D TMA tile into L2 (no destination, no completion).  A hint
+// only: L2 is where every write of the device lands, so data read later (by
+// a TMA load after griddepcontrol.wait) is current even if the tile was
+// written after the prefetch.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
 // 3-D TMA tile load (c0 innermost, c2 the batch index).
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int32_t c0, int32_t c1, int32_t c2) {

@@ -386,9 +386,26 @@ sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA,
         fence_barrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        // While the kernel before this one finishes: pull this CTA's first
+        // slices into L2 (a hint; nothing is read before the wait below).
+        WorkIter it0;
+        it0.begin(p);
+        Segment s0;
+        if (it0.get(p, s0)) {
+            int bt, tm, tn;
+            tile_coords(s0.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
+            for (int kb = s0.kb0; kb < s0.kb1 && kb < s0.kb0 + STAGES; ++kb) {
+#pragma unroll
+                for (int q = 0; q < Cfg::A_BOXES; ++q)
+                    tma_prefetch_3d(&tmA, kb * BK, tm * BM + q * Cfg::BOX_M, bt);
+#pragma unroll
+                for (int q = 0; q < Cfg::B_BOXES; ++q)
+                    tma_prefetch_3d(&tmB, tn * BN + q * Cfg::BOX_N, kb * BK, bt);
+            }
+        }
     }
-    // Only shared memory and kernel parameters so far; from here on global
-    // memory is read and written.
+    // Only shared memory, kernel parameters and L2 prefetches so far; from
+    // here on global memory is read and written.
     griddep_launch_dependents();
     griddep_wait();
     if (threadIdx.x == 0 && stream_k) *sk_tag_s = sk_launch_tag(p.sk_seq);
