@@ -96,9 +96,11 @@ struct Tf32x3Args {
 };
 struct Tf32x3Info {
     const void *fn[4];   // variant index as for the FFMA kernels
-    int threads, smem, bm, bn, bk, stages, chunk_kb;
+    int threads, smem, bm, bn, bk, stages, chunk_kb;   // bm x bn: the tile
+    int pair;            // 1: a cluster of 2 CTAs (an SM pair) per tile
+    int box_a, box_b;    // rows of A, of B^T one CTA loads per stage
 };
-constexpr int kNumTf32x3Configs = 3;
+constexpr int kNumTf32x3Configs = 4;
 Tf32x3Info tf32x3_info(int config);   // 1-based tile configuration
 // Skinny products, M <= 32 or N <= 32 (sgemm_skinny.cu).
 constexpr int kSkinnyMax = 32;

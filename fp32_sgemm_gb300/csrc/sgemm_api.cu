@@ -377,6 +377,13 @@ int64_t stream_k_ctas(int64_t tiles, int64_t k_blocks, int64_t slots, bool even_
 
 int choose_tf32x3_config(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= sg::kNumTf32x3Configs) return h->algo;
+    // The SM-pair tile (256 x 256, each SM staging and reading half of B)
+    // wins once its tiles occupy at least half of the pairs; measured main
+    // kernel against the 128 x 256 tile: 4096^3 450.8 / 516.5 us, 8192^3
+    // 3467 / 3836 us, 2048^3 (64 tiles) 71.3 / 76.2 us, but 1024^3 (16
+    // tiles) 36.4 / 32.4 us.
+    if (4 * ceil_div(q.M, 256) * ceil_div(q.N, 256) * q.batch >= h->sm_count && ceil_div(q.K, 32) >= 4)
+        return 4;
     // With stream-K evening out the last wave, the widest tile wins as soon
     // as it fills the chip once: it reads the fewest shared-memory bytes per
     // MMA, the resource this kernel is bound by.
@@ -413,35 +420,58 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
     if (tiles > kMaxDim) return SGEMM_STATUS_NOT_SUPPORTED;
     pl.num_tiles = int(tiles);
     pl.k_blocks = int(ceil_div(q.K, info.bk));
+    // Slots: CTAs resident at once, or for the SM-pair tile, clusters of 2.
     static std::mutex occ_mutex;
-    static int occ_cache[kMaxDevices][sg::kNumTf32x3Configs][4] = {};
-    int occ = 0;
+    static int slot_cache[kMaxDevices][sg::kNumTf32x3Configs][4] = {};
+    int64_t slots = 0;
     {
         std::lock_guard<std::mutex> lk(occ_mutex);
-        int &o = occ_cache[h->device][pl.tf32_cfg - 1][pl.variant];
+        int &o = slot_cache[h->device][pl.tf32_cfg - 1][pl.variant];
         if (o == 0) {
             const void *fn = info.fn[pl.variant];
             int n = 0;
-            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, info.threads, info.smem) != cudaSuccess ||
-                n < 1)
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, info.smem) != cudaSuccess)
                 return SGEMM_STATUS_LAUNCH_FAILED;
+            if (info.pair) {
+                cudaLaunchConfig_t cfg{};
+                cfg.gridDim = dim3(2 * h->sm_count);
+                cfg.blockDim = dim3(info.threads);
+                cfg.dynamicSmemBytes = size_t(info.smem);
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+            } else {
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, info.threads, info.smem) != cudaSuccess)
+                    n = 0;
+                n *= h->sm_count;
+            }
+            if (n < 1) return SGEMM_STATUS_LAUNCH_FAILED;
             o = n;
         }
-        occ = o;
+        slots = o;
     }
-    const int64_t slots = int64_t(h->sm_count) * occ;
-    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, slots));
+    const int per_slot = info.pair ? 2 : 1;     // CTAs per slot
+    pl.dp_ctas = int(std::min<int64_t>(pl.num_tiles, slots)) * per_slot;
     // Stream-K for a partial last wave, as for the FFMA kernel, where it
     // pays: cutting tiles costs this kernel about a fifth of a tile's time
     // (measured: partial-tile stores and loads, the counter handshake), so
     // whole tiles stay when the last wave is more than 3/4 full; few tiles
     // (at most half a wave) are split along K when K is deep (>= 1024;
     // below that the split measured slower than one CTA per tile).
+    // For the SM-pair tile the cut pays only up to a half-full last wave
+    // (measured per call, cut against whole: 4096^3, 3.37 waves, 516.6 /
+    // 560.4 us; 8192^3, 13.47 waves, 3624 / 3690 us; 6144^3, 7.58 waves,
+    // 1651 / 1614 us).
     const double per_sm = double(pl.num_tiles) / double(slots);
     const double frac = per_sm - std::floor(per_sm);
     const int64_t units = int64_t(pl.num_tiles) * pl.k_blocks;
-    const bool sk_pays = (per_sm >= 1.0 && frac > 0.0 && frac < 0.75) ||
+    const double frac_max = info.pair ? 0.5 : 0.75;
+    const bool sk_pays = (per_sm >= 1.0 && frac > 0.0 && frac < frac_max) ||
                          (2 * pl.num_tiles <= slots && pl.k_blocks >= 32);
     const bool want_sk = h->schedule == 2 || (h->schedule == 0 && sk_pays);
     const int64_t sk_ctas = stream_k_ctas(pl.num_tiles, pl.k_blocks, slots);
@@ -456,8 +486,9 @@ sgemmStatus_t make_plan_tf32x3(const sgemmContext *h, const Problem &q, Plan &pl
         int64_t first = waves * slots;
         if (rem_units < 8 * slots) first = waves >= 1 ? (waves - 1) * slots : 0;
         pl.sk_tile0 = int(first);
-        pl.sk_ctas = int(sk_ctas);
-        pl.ws_partials = size_t(sk_ctas) * size_t(info.bm) * size_t(info.bn) * 4;
+        pl.sk_ctas = int(sk_ctas) * per_slot;
+        // One partial tile per CTA: its box_a rows of the tile.
+        pl.ws_partials = size_t(pl.sk_ctas) * size_t(info.box_a) * size_t(info.bn) * 4;
     }
     pl.pub.tile_m = info.bm;
     pl.pub.tile_n = info.bn;
@@ -663,9 +694,9 @@ inline sgemmStatus_t last_launch() {
 // Main kernels are launched with programmatic stream serialisation: their
 // CTAs may be placed (and set up their barriers) while the previous kernel
 // in the stream finishes; they wait for it (griddepcontrol.wait) before
-// touching global memory.
+// touching global memory.  cluster = 2: CTAs in pairs (SM-pair tiles).
 sgemmStatus_t launch_main(sgemmContext *h, const void *fn, int ctas, int threads, int smem,
-                          void **kargs, cudaStream_t stream) {
+                          void **kargs, cudaStream_t stream, int cluster = 1) {
     if (h->ev_start != nullptr && cudaEventRecord(h->ev_start, stream) != cudaSuccess)
         return SGEMM_STATUS_LAUNCH_FAILED;
     cudaLaunchConfig_t cfg{};
@@ -673,11 +704,15 @@ sgemmStatus_t launch_main(sgemmContext *h, const void *fn, int ctas, int threads
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
     cudaError_t err = cudaLaunchKernelExC(&cfg, fn, kargs);
     if (err == cudaSuccess && h->ev_stop != nullptr) err = cudaEventRecord(h->ev_stop, stream);
     return err == cudaSuccess ? SGEMM_STATUS_SUCCESS : SGEMM_STATUS_LAUNCH_FAILED;
@@ -713,7 +748,7 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
     for (int i = 0; i < 4; ++i) {
         const bool is_a = i < 2;
         sgemmStatus_t st = encode_3d(&tm[i], ptrs[i], q.K, is_a ? q.M : q.N, q.batch, pl.kp,
-                                     is_a ? sa_d : sb_d, info.bk, is_a ? info.bm : info.bn,
+                                     is_a ? sa_d : sb_d, info.bk, is_a ? info.box_a : info.box_b,
                                      CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != SGEMM_STATUS_SUCCESS) return st;
     }
@@ -744,7 +779,8 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
         ctas = pl.sk_ctas;
     }
     void *kargs[] = {&tm[0], &tm[1], &tm[2], &tm[3], &args};
-    return launch_main(h, info.fn[pl.variant], ctas, info.threads, info.smem, kargs, stream);
+    return launch_main(h, info.fn[pl.variant], ctas, info.threads, info.smem, kargs, stream,
+                       info.pair ? 2 : 1);
 }
 
 sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
@@ -1289,7 +1325,7 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t h, int64_t M, int64_t N, int64_t K, f
 }
 
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t h, int algo) {
-    // 1..3 also name the tensor-core tiles of math mode 1.
+    // 1..4 also name the tensor-core tiles of math mode 1.
     if (h == nullptr || algo < 0 || algo > kNumAlgos ||
         (algo > sg::kNumTf32x3Configs && !sg::algo_shipped(algo)))
         return SGEMM_STATUS_INVALID_VALUE;

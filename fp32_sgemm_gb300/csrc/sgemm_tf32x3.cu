@@ -39,16 +39,25 @@
 
 namespace sg {
 
-template <int BN_, int STAGES_, int CHUNK_KB_, int EPI_WARPS_>
+// PAIR: the tile is computed by an SM pair (a cluster of 2 CTAs,
+// tcgen05 cta_group::2): 256 rows, each CTA loading its own 128 rows of A
+// and half of B's BN columns, rank 0 issuing M = 256 MMAs that read both
+// CTAs' shared memory and write each CTA's 128 rows into its own TMEM.  Each
+// SM then stages and reads half of B per MMA, which is what bounds the
+// single-SM kernel (its shared-memory port).
+template <int BN_, int STAGES_, int CHUNK_KB_, int EPI_WARPS_, bool PAIR_ = false>
 struct Tf32x3Config {
+    static constexpr bool PAIR = PAIR_;
     static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // rows of C per tile
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // columns of B this CTA loads
     static constexpr int CHUNK_KB = CHUNK_KB_;     // K slices per TMEM accumulator chunk
     // Epilogue warps: 4 lane quarters of TMEM x EPI_WARPS/4 column slabs.
     static constexpr int EPI_WARPS = EPI_WARPS_;
     static constexpr int SLAB = BN / (EPI_WARPS / 4);   // columns per epilogue thread
     static constexpr int A_BYTES = BM * BK * 4;     // one of A_hi / A_lo
-    static constexpr int B_BYTES = BN * BK * 4;     // one of B_hi / B_lo
-    static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int B_BYTES = B_ROWS * BK * 4; // one of B_hi / B_lo
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // per CTA
     // Two accumulators of BN columns; the allocation is a power of two.
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;
@@ -59,30 +68,38 @@ struct Tf32x3Config {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16 + XPOSE_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(BN % 16 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+    static_assert(!PAIR || (BN % 32 == 0 && B_ROWS % 8 == 0), "UMMA N for M = 256 across a pair");
     static_assert(EPI_WARPS % 4 == 0 && SLAB % 32 == 0 && SLAB * (EPI_WARPS / 4) == BN, "epilogue slabs");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM");
     static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
 };
 
-// Work of one CTA as segments, K slices [kb0, kb1) of tile t: whole tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ... below sk_tile0, then an equal
-// contiguous share of the (tile, slice) units of the tiles from sk_tile0 on
-// ("stream-K").  A tile cut between CTAs is finished by the CTA holding its
-// first slice, whose last segment that is; the others (each CTA has at most
-// one such segment, its first) store partial sums.  All three roles of the
-// CTA walk the same sequence.
+// Work of one slot (a CTA, or an SM pair: the cluster) as segments, K
+// slices [kb0, kb1) of tile t: whole tiles slot, slot + slots, ... below
+// sk_tile0, then an equal contiguous share of the (tile, slice) units of the
+// tiles from sk_tile0 on ("stream-K").  A tile cut between slots is
+// finished by the slot holding its first slice, whose last segment that is;
+// the others (each slot has at most one such segment, its first) store
+// partial sums.  All three roles of the CTA (of both CTAs of a pair) walk
+// the same sequence.
+template <bool PAIR>
+__device__ __forceinline__ int tc_slot() { return PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x; }
+template <bool PAIR>
+__device__ __forceinline__ int tc_slots() { return PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x; }
 struct TcSegment {
     int t, kb0, kb1;
 };
 
+template <bool PAIR>
 struct TcWork {
     int t, u, u_end;
     __device__ __forceinline__ void begin(const Tf32x3Args &p) {
-        t = blockIdx.x;
+        const int slot = tc_slot<PAIR>(), slots = tc_slots<PAIR>();
+        t = slot;
         const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
         const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
-        u = (int)(base + (int64_t)blockIdx.x * W / gridDim.x);
-        u_end = (int)(base + (int64_t)(blockIdx.x + 1) * W / gridDim.x);
+        u = (int)(base + (int64_t)slot * W / slots);
+        u_end = (int)(base + (int64_t)(slot + 1) * W / slots);
     }
     __device__ __forceinline__ bool get(const Tf32x3Args &p, TcSegment &s) const {
         if (t < p.sk_tile0) {
@@ -98,16 +115,17 @@ struct TcWork {
         return true;
     }
     __device__ __forceinline__ void advance(const Tf32x3Args &p, const TcSegment &s) {
-        if (t < p.sk_tile0) t += gridDim.x;
+        if (t < p.sk_tile0) t += tc_slots<PAIR>();
         else u += s.kb1 - s.kb0;
     }
 };
 
-// The CTA whose stream-K unit range contains unit u.
-__device__ __forceinline__ int tc_cta_of_unit(int u, const Tf32x3Args &p) {
+// The slot whose stream-K unit range contains unit u.
+template <bool PAIR>
+__device__ __forceinline__ int tc_slot_of_unit(int u, const Tf32x3Args &p) {
     const int64_t base = (int64_t)p.sk_tile0 * p.k_blocks;
     const int64_t W = (int64_t)(p.num_tiles - p.sk_tile0) * p.k_blocks;
-    return (int)((((int64_t)u - base + 1) * gridDim.x - 1) / W);
+    return (int)((((int64_t)u - base + 1) * tc_slots<PAIR>() - 1) / W);
 }
 
 __device__ __forceinline__ void prefetch_l2(const float *p) {
@@ -120,8 +138,10 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
                     const Tf32x3Args p)
 {
+    constexpr bool PAIR = Cfg::PAIR;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
-    constexpr uint32_t IDESC = idesc_tf32(BM, BN);
+    constexpr int TILE_M = Cfg::TILE_M, B_ROWS = Cfg::B_ROWS;
+    constexpr uint32_t IDESC = idesc_tf32(TILE_M, BN);
 
     extern __shared__ unsigned char smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -137,8 +157,15 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Pair: rank 0 issues the MMAs and owns the barriers both CTAs' copies
+    // and epilogues report to (full, tempty); both CTAs' empty and tfull
+    // barriers receive rank 0's MMA completions.
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
-    if (warp == 0) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (warp == 0) {
+        if constexpr (PAIR) tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        else tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    }
     if (threadIdx.x == 32) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -146,7 +173,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], Cfg::EPI_WARPS);
+            mbar_init(&tempty[b], (PAIR ? 2 : 1) * Cfg::EPI_WARPS);
         }
         mbar_init(drain, 1);
         fence_barrier_init();
@@ -163,7 +190,10 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     const bool stream_k = p.sk_tile0 < p.num_tiles;
     if (threadIdx.x == 32 && stream_k) tmem_slot[1] = sk_launch_tag(p.sk_seq);
     tc_fence_before();
-    __syncthreads();
+    // A pair's CTAs signal each other's barriers from here on: both must
+    // have initialised theirs.
+    if constexpr (PAIR) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     const uint32_t sk_tag = stream_k ? reinterpret_cast<volatile uint32_t *>(tmem_slot)[1] : 0u;
@@ -174,45 +204,62 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
-        TcWork w;
+        TcWork<PAIR> w;
         w.begin(p);
         TcSegment seg;
         while (ok && w.get(p, seg)) {
             int bt, tm, tn;
             tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
+            const int ya = tm * TILE_M + (int)rank * BM;      // this CTA's rows of A
+            const int yb = tn * BN + (int)rank * B_ROWS;      // this CTA's columns of B
             for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                 if (p.withhold == kWithholdRefill && issued >= STAGES) {
                     ok = false;     // test hook: stop after one ring fill (drain below)
                     break;
                 }
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                if (!mbar_wait_bounded<PAIR>(&empty[stage], phase ^ 1u, p.timeout_ns)) {
                     record_error(p.err, kSiteProducerEmpty);
                     ok = false;
                     break;
                 }
                 unsigned char *st = smem + stage * Cfg::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                tma_load_3d(st, &tmAhi, &full[stage], kb * BK, tm * BM, bt);
-                tma_load_3d(st + Cfg::A_BYTES, &tmAlo, &full[stage], kb * BK, tm * BM, bt);
-                tma_load_3d(st + 2 * Cfg::A_BYTES, &tmBhi, &full[stage], kb * BK, tn * BN, bt);
-                tma_load_3d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, &full[stage], kb * BK, tn * BN, bt);
+                if constexpr (PAIR) {
+                    // Both CTAs' copies complete on rank 0's barrier, which
+                    // rank 0 arms with the pair's bytes.
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::STAGE_BYTES);
+                    const uint32_t fb = cluster_addr(&full[stage], 0);
+                    tma_load_3d_pair(st, &tmAhi, fb, kb * BK, ya, bt);
+                    tma_load_3d_pair(st + Cfg::A_BYTES, &tmAlo, fb, kb * BK, ya, bt);
+                    tma_load_3d_pair(st + 2 * Cfg::A_BYTES, &tmBhi, fb, kb * BK, yb, bt);
+                    tma_load_3d_pair(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, fb, kb * BK, yb, bt);
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    tma_load_3d(st, &tmAhi, &full[stage], kb * BK, ya, bt);
+                    tma_load_3d(st + Cfg::A_BYTES, &tmAlo, &full[stage], kb * BK, ya, bt);
+                    tma_load_3d(st + 2 * Cfg::A_BYTES, &tmBhi, &full[stage], kb * BK, yb, bt);
+                    tma_load_3d(st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, &tmBlo, &full[stage], kb * BK, yb, bt);
+                }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             w.advance(p, seg);
         }
         if (!ok) {
-            // Let this CTA's own copies land before it can exit.
+            // Let this CTA's own copies land before it can exit.  Rank 1 of
+            // a pair cannot see its copies complete (they count on rank 0's
+            // barrier): it waits for its stages to be released instead,
+            // which happens only after they landed, or for the limit, far
+            // longer than any copy takes.
             const int pending = issued < STAGES ? issued : STAGES;
             for (int back = 1; back <= pending; ++back) {
                 int s = stage - back;
                 uint32_t ph = phase;
                 if (s < 0) { s += STAGES; ph ^= 1u; }
-                mbar_wait_bounded(&full[s], ph, p.timeout_ns);
+                mbar_wait_bounded<PAIR>(rank == 0 ? &full[s] : &empty[s], ph, p.timeout_ns);
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------- MMA issuer (rank 0 of a pair) ----------------
         int stage = 0;
         uint32_t phase = 0;
         int gc = 0;             // chunk counter across segments: TMEM buffer gc & 1
@@ -222,7 +269,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             const int ab = gc & 1;
             const uint32_t use = (uint32_t)(gc >> 1);
             ++gc;
-            if (!mbar_wait_bounded(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
+            if (!mbar_wait_bounded<PAIR>(&tempty[ab], (use & 1u) ^ 1u, p.timeout_ns)) {
                 record_error(p.err, kSiteConsumerFull);
                 ok = false;
                 return;
@@ -230,7 +277,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(&full[stage], phase, downstream_limit(p.timeout_ns))) {
+                if (!mbar_wait_bounded<PAIR>(&full[stage], phase, downstream_limit(p.timeout_ns))) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
                     return;
@@ -250,22 +297,33 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     const uint64_t b_lo = smem_desc_k_sw128(s_blo + off);
                     const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
                     // Small terms first, then the dominant product.
-                    mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
-                    mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
-                    mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
+                    if constexpr (PAIR) {
+                        mma_tf32_pair(d_tmem, a_lo, b_hi, IDESC, acc);
+                        mma_tf32_pair(d_tmem, a_hi, b_lo, IDESC, 1u);
+                        mma_tf32_pair(d_tmem, a_hi, b_hi, IDESC, 1u);
+                    } else {
+                        mma_tf32(d_tmem, a_lo, b_hi, IDESC, acc);
+                        mma_tf32(d_tmem, a_hi, b_lo, IDESC, 1u);
+                        mma_tf32(d_tmem, a_hi, b_hi, IDESC, 1u);
+                    }
                 }
-                if (p.withhold != kWithholdRelease)
-                    mma_commit(&empty[stage]);  // frees the stage once these MMAs are done
+                // Frees the stage (in both CTAs of a pair) once these MMAs are done.
+                if (p.withhold != kWithholdRelease) {
+                    if constexpr (PAIR) mma_commit_pair_mc(&empty[stage], 0x3);
+                    else mma_commit(&empty[stage]);
+                }
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-            mma_commit(&tfull[ab]);             // chunk ready for the epilogue
+            // Chunk ready for the epilogue (of both CTAs).
+            if constexpr (PAIR) mma_commit_pair_mc(&tfull[ab], 0x3);
+            else mma_commit(&tfull[ab]);
         };
         // Whole tiles, then the stream-K segments (the same order as the
         // producer and the epilogue walk).
-        for (int t = blockIdx.x; ok && t < p.sk_tile0; t += gridDim.x)
+        for (int t = tc_slot<PAIR>(); ok && t < p.sk_tile0; t += tc_slots<PAIR>())
             for (int kb0 = 0; ok && kb0 < p.k_blocks; kb0 += Cfg::CHUNK_KB)
                 chunk(kb0, min(p.k_blocks, kb0 + Cfg::CHUNK_KB));
-        TcWork w;
+        TcWork<PAIR> w;
         w.begin(p);
         w.t = p.sk_tile0;                       // whole tiles done above
         TcSegment seg;
@@ -275,7 +333,8 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             w.advance(p, seg);
         }
         // All MMAs this thread issued complete before the CTA tears down.
-        mma_commit(drain);
+        if constexpr (PAIR) mma_commit_pair(drain);
+        else mma_commit(drain);
         mbar_wait_bounded(drain, 0u, p.timeout_ns);
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM chunks -> FP32 sums -> C ----------------
@@ -286,7 +345,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
         const float alpha = p.alpha, beta = p.beta;
         int gc = 0;
         bool ok = true;
-        TcWork w;
+        TcWork<PAIR> w;
         w.begin(p);
         TcSegment seg;
         while (ok && w.get(p, seg)) {
@@ -299,7 +358,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 if (seg.kb0 == 0) {
                     int bt, tm, tn;
                     tile_coords(seg.t, p.tiles_m, p.tiles_n, p.group_m, bt, tm, tn);
-                    const int row = tm * BM + quarter * 32 + lane;
+                    const int row = tm * TILE_M + (int)rank * BM + quarter * 32 + lane;
                     const int c0 = tn * BN + slab0;
                     if (row < p.M && c0 < p.N) {
                         const float *crow = p.C + (int64_t)bt * p.stride_c + (int64_t)row * p.ldc;
@@ -312,7 +371,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
             for (int kb0 = seg.kb0; kb0 < seg.kb1; kb0 += Cfg::CHUNK_KB, ++gc) {
                 const int ab = gc & 1;
                 const uint32_t use = (uint32_t)(gc >> 1);
-                if (!mbar_wait_bounded(&tfull[ab], use & 1u, downstream_limit(p.timeout_ns))) {
+                if (!mbar_wait_bounded<PAIR>(&tfull[ab], use & 1u, downstream_limit(p.timeout_ns))) {
                     record_error(p.err, kSiteConsumerFull);
                     ok = false;
                     break;
@@ -329,7 +388,10 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[ab]);
+                if (lane == 0) {
+                    if constexpr (PAIR) mbar_arrive_cluster(cluster_addr(&tempty[ab], 0));
+                    else mbar_arrive(&tempty[ab]);
+                }
             }
             if (!ok) break;
 
@@ -353,19 +415,23 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                     w.advance(p, seg);
                     continue;
                 }
-                // The tile's first slice: add the partial tiles of the CTAs
-                // that hold its other slices, in CTA order (deterministic).
+                // The tile's first slice: add the partial tiles of the slots
+                // that hold its other slices, in slot order (deterministic);
+                // in a pair, those of the CTA of the same rank.
                 const int tile_u0 = seg.t * p.k_blocks;
-                const int c_first = tc_cta_of_unit(tile_u0 + seg.kb1, p);
-                const int c_last = tc_cta_of_unit(tile_u0 + p.k_blocks - 1, p);
+                const int c_first = tc_slot_of_unit<PAIR>(tile_u0 + seg.kb1, p);
+                const int c_last = tc_slot_of_unit<PAIR>(tile_u0 + p.k_blocks - 1, p);
                 if (lane == 0) {
-                    for (int c = c_first; c <= c_last; ++c)
-                        if (!tag_wait_bounded(&p.flags[c * Cfg::EPI_WARPS + ew], sk_tag, p.timeout_ns))
+                    for (int c = c_first; c <= c_last; ++c) {
+                        const int cta = PAIR ? 2 * c + (int)rank : c;
+                        if (!tag_wait_bounded(&p.flags[cta * Cfg::EPI_WARPS + ew], sk_tag, p.timeout_ns))
                             record_error(p.err, kSiteStreamKFlag);
+                    }
                 }
                 __syncwarp();
                 for (int c = c_first; c <= c_last; ++c) {
-                    const float4 *other = reinterpret_cast<const float4 *>(p.partials + (size_t)c * (BM * BN));
+                    const int cta = PAIR ? 2 * c + (int)rank : c;
+                    const float4 *other = reinterpret_cast<const float4 *>(p.partials + (size_t)cta * (BM * BN));
 #pragma unroll
                     for (int q = 0; q < SLAB / 4; ++q) {
                         const float4 v = __ldcg(&other[(ew * (SLAB / 4) + q) * 32 + lane]);
@@ -384,7 +450,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 // Direct: each lane reads and writes its own row, 16 bytes at
                 // a time; the loads of a group of 16 columns are issued
                 // before its stores so that their latencies overlap.
-                const int row = tm * BM + quarter * 32 + lane;
+                const int row = tm * TILE_M + (int)rank * BM + quarter * 32 + lane;
                 if (row < p.M) {
                     float *crow = cbase + (int64_t)row * p.ldc;
                     constexpr int G = 4;             // float4 columns per group
@@ -433,7 +499,7 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
                 // through shared memory instead, so that lane l handles
                 // column l of one row at a time: 128-byte row segments.
                 float *tb = xpose + ew * (32 * 33);
-                const int row0 = tm * BM + quarter * 32;
+                const int row0 = tm * TILE_M + (int)rank * BM + quarter * 32;
 #pragma unroll
                 for (int b = 0; b < SLAB / 32; ++b) {
                     __syncwarp();
@@ -470,10 +536,16 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
     }
 
     // ---------------- teardown ----------------
+    // In a pair, neither CTA leaves while the other's MMAs, copies or
+    // arrivals may still touch its shared memory or barriers.
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (warp == 0) {
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
     if (threadIdx.x == 32 && stream_k) sk_launch_done(p.sk_seq, sk_tag);
 }
 
@@ -491,8 +563,11 @@ Tf32x3Info make_info() {
     info.fn[3] = reinterpret_cast<const void *>(&sgemm_tf32x3_kernel<Cfg, false, false>);
     info.threads = Cfg::THREADS;
     info.smem = Cfg::SMEM_BYTES;
-    info.bm = Cfg::BM;
+    info.bm = Cfg::TILE_M;
     info.bn = Cfg::BN;
+    info.pair = Cfg::PAIR ? 1 : 0;
+    info.box_a = Cfg::BM;
+    info.box_b = Cfg::B_ROWS;
     info.bk = Cfg::BK;
     info.stages = Cfg::STAGES;
     info.chunk_kb = Cfg::CHUNK_KB;
@@ -501,13 +576,16 @@ Tf32x3Info make_info() {
 }  // namespace
 
 // Tensor-core tile configurations: 1: 128 x 128 (3 stages, 4 epilogue
-// warps), 2: 128 x 192 (2 stages, 8), 3: 128 x 256 (2 stages, 8).  Wider
-// tiles read fewer shared-memory bytes per MMA FLOP.
+// warps), 2: 128 x 192 (2 stages, 8), 3: 128 x 256 (2 stages, 8), 4: 256 x
+// 256 on an SM pair (each CTA 128 rows of A and 128 columns of B per stage,
+// 3 stages, 8 epilogue warps).  Wider tiles read fewer shared-memory bytes
+// per MMA FLOP; the pair halves B's bytes per SM.
 Tf32x3Info tf32x3_info(int config) {
     static const Tf32x3Info infos[kNumTf32x3Configs] = {
         make_info<Tf32x3Config<128, 3, 2, 4>>(),
         make_info<Tf32x3Config<192, 2, 2, 8>>(),
         make_info<Tf32x3Config<256, 2, 2, 8>>(),
+        make_info<Tf32x3Config<256, 3, 2, 8, true>>(),
     };
     if (config < 1 || config > kNumTf32x3Configs) config = 1;
     return infos[config - 1];

@@ -295,11 +295,12 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  *   29 / 30 = 256 x 128 / 128 x 256, K slices of 32, 4 stages, C from
  *   registers.
  * Other numbers up to 30 (configurations measured slower and no longer
- * built) return INVALID_VALUE, here or, for 1..3 set in math mode 0, from
+ * built) return INVALID_VALUE, here or, for 1..4 set in math mode 0, from
  * the product call.  In math mode 1
- * (3xTF32) the values 1..3 pick the tensor-core tile instead: 128 x 128,
- * 128 x 192 or 128 x 256.  Every configuration computes the same result up
- * to summation order.
+ * (3xTF32) the values 1..4 pick the tensor-core tile instead: 128 x 128,
+ * 128 x 192 or 128 x 256 on one SM, or 256 x 256 on an SM pair (a cluster
+ * of two CTAs sharing each MMA).  Every configuration computes the same
+ * result up to summation order.
  */
 sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
 

@@ -140,7 +140,7 @@ def test_null_handle_rejected(lib):
 def test_configurations_not_built_are_rejected(lib):
     # Numbers of tile configurations that are not built (measured slower)
     # are refused before the handle is touched (a fake pointer here).
-    for algo in (4, 9, 11, 15, 22, 25, 26, 31, -1):
+    for algo in (5, 9, 11, 15, 22, 25, 26, 31, -1):
         assert lib.sgemmSetAlgo(F, algo) == _binding.Status.INVALID_VALUE
 
 

@@ -135,7 +135,7 @@ def test_repeated_calls_bitwise_identical(handle):
         assert torch.equal(C.view(torch.int32), first.view(torch.int32))
 
 
-@pytest.mark.parametrize("config", [1, 2, 3])
+@pytest.mark.parametrize("config", [1, 2, 3, 4])
 @pytest.mark.parametrize("shape", [(1000, 1500, 700), (256, 4097, 333), (4096, 4096, 4096)])
 def test_every_tensor_tile_configuration(handle, config, shape):
     M, N, K = shape
@@ -150,22 +150,30 @@ def test_every_tensor_tile_configuration(handle, config, shape):
         handle.set_algo(0)
 
 
-def test_plan_at_4096_is_wide_tiles_with_stream_k(handle):
+def test_plan_at_4096_is_sm_pair_tiles_with_stream_k(handle):
     A = torch.empty((4096, 4096), device="cuda")
     B = torch.empty((4096, 4096), device="cuda")
     C = torch.empty((4096, 4096), device="cuda")
     handle._ensure_workspace(handle.workspace_size(4096, 4096, 4096, A.data_ptr(), 4096, B.data_ptr(), 4096))
     plan = handle.plan(A, B, C)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert plan["tile_n"] == 256
-    # Stream-K when the last wave of whole tiles would be under 3/4 full.
-    waves = (4096 // 128) * (4096 // 256) / sms
+    assert (plan["tile_m"], plan["tile_n"]) == (256, 256)
+    assert plan["ctas"] % 2 == 0 and plan["ctas"] <= sms
+    # Stream-K when the last wave of whole pair tiles would be under half full.
+    waves = (4096 // 256) ** 2 / (plan["ctas"] // 2)
     frac = waves - int(waves)
-    assert plan["stream_k"] == (1 if 0 < frac < 0.75 else 0)
+    assert plan["stream_k"] == (1 if 0 < frac < 0.5 else 0)
+
+
+def test_mid_size_keeps_single_sm_tiles(handle):
+    # 16 pair tiles at 1024^3 would leave most SM pairs idle.
+    A = torch.empty((1024, 1024), device="cuda")
+    plan = handle.plan(A, A, A)
+    assert plan["tile_m"] == 128
 
 
 @pytest.mark.parametrize("schedule", [1, 2])
-@pytest.mark.parametrize("config", [1, 3])
+@pytest.mark.parametrize("config", [1, 3, 4])
 @pytest.mark.parametrize("shape", [(1000, 1500, 700), (257, 255, 4000), (2048, 2048, 2048), (130, 4100, 96)])
 def test_tensor_schedules(handle, schedule, config, shape):
     # schedule 2 cuts tiles between CTAs (stream-K) and adds the partial

@@ -104,13 +104,18 @@ def test_ffma_stream_k_flag_wait_expires_automatic_plan(sg):
     h.close()
 
 
+# Tensor-core kernel: one 128 x 256 tile on one SM (configuration 3), or one
+# 256 x 256 tile on an SM pair (configuration 4: both CTAs' copies report to
+# the first CTA's barriers, and both must release their shared tensor
+# memory allocation).
+@pytest.mark.parametrize("config,M,ctas", [(3, 128, 1), (4, 256, 2)])
 @pytest.mark.parametrize("which,site", [(REFILL, SITE_DATA), (RELEASE, SITE_SLOT)])
-def test_tf32x3_pipeline_waits_expire_and_free_tensor_memory(sg, which, site):
+def test_tf32x3_pipeline_waits_expire_and_free_tensor_memory(sg, which, site, config, M, ctas):
     h = sg.Handle()
     h.set_math_mode(1)
-    h.set_algo(3)
+    h.set_algo(config)
     h.set_schedule(1)
-    _expire_then_recover(sg, h, 128, 256, 1024, which, site, expect_ctas=1)
+    _expire_then_recover(sg, h, M, 256, 1024, which, site, expect_ctas=ctas)
     # Several more launches over every SM: each allocates tensor memory.
     p, A, B = _operands(1024, 1024, 512, seed=5)
     C = torch.zeros((1024, 1024), device="cuda")
@@ -122,12 +127,13 @@ def test_tf32x3_pipeline_waits_expire_and_free_tensor_memory(sg, which, site):
     h.close()
 
 
-def test_tf32x3_stream_k_flag_wait_expires(sg):
+@pytest.mark.parametrize("config,M", [(3, 128), (4, 256)])
+def test_tf32x3_stream_k_flag_wait_expires(sg, config, M):
     h = sg.Handle()
     h.set_math_mode(1)
-    h.set_algo(3)
+    h.set_algo(config)
     h.set_schedule(2)
-    _expire_then_recover(sg, h, 128, 256, 8192, FLAG, SITE_FLAG,
+    _expire_then_recover(sg, h, M, 256, 8192, FLAG, SITE_FLAG,
                          plan_check=lambda pl: pl["stream_k"] == 1 or pytest.fail(str(pl)))
     h.close()
 
