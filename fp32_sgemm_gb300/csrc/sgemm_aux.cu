@@ -168,6 +168,8 @@ sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_
                        int64_t s_dst, int rows, int cols, int batch) {
     __shared__ float t0[64][65];
     __shared__ float t1[SPLIT ? 64 : 1][SPLIT ? 65 : 1];
+    griddep_launch_dependents();
+    griddep_wait();              // the previous kernel may still read dst
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;     // 16 x 16
     const int c0 = blockIdx.x * 64;      // source columns
     const int r0 = blockIdx.y * 64;      // source rows
@@ -239,6 +241,8 @@ sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_
 __global__ void sgemm_split_rows_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
                                         float *__restrict__ hi, float *__restrict__ lo, int64_t ld_dst,
                                         int64_t s_dst, int rows, int cols, int batch) {
+    griddep_launch_dependents();
+    griddep_wait();
     for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
         for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
             const float *sr = src + z * s_src + r * ld_src;
@@ -260,6 +264,8 @@ __global__ void __launch_bounds__(256)
 sgemm_split_rows_vec4_kernel(const float4 *__restrict__ src, int64_t ld4, int64_t s4,
                              float4 *__restrict__ hi, float4 *__restrict__ lo, int64_t ldd4,
                              int64_t sd4, int rows, int cols4, int batch) {
+    griddep_launch_dependents();
+    griddep_wait();
     for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
         for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
             const float4 *sr = src + z * s4 + r * ld4;
@@ -305,6 +311,23 @@ inline int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
 
 namespace {
 unsigned zdim(int batch) { return unsigned(std::min(std::max(batch, 1), 65535)); }
+// Launch with programmatic stream serialisation, as the main kernels are:
+// the kernel's CTAs may be placed while the kernel before it finishes, and
+// wait for it (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 int num_sms() {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -354,7 +377,7 @@ void launch_transpose(const float *src, int64_t ld_src, int64_t s_src, float *ds
                     (batch == 1 || s_dst % 4 == 0) &&
                     (dst2 == nullptr || reinterpret_cast<uintptr_t>(dst2) % 16 == 0);
     auto go = [&](auto kernel) {
-        kernel<<<grid, 256, 0, s>>>(src, ld_src, s_src, dst, dst2, ld_dst, s_dst, rows, cols, batch);
+        launch_chained(kernel, grid, s, src, ld_src, s_src, dst, dst2, ld_dst, s_dst, rows, cols, batch);
     };
     if (dst2 != nullptr) {
         if (vs && vd) go(sgemm_transpose_kernel<true, true, true>);
@@ -374,13 +397,13 @@ void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *h
     if (vec && reinterpret_cast<uintptr_t>(hi) % 16 == 0 && reinterpret_cast<uintptr_t>(lo) % 16 == 0) {
         dim3 grid(unsigned(std::max<int64_t>(1, cdiv(cols / 4, 1024))), unsigned(std::min<int64_t>(rows, 65535)),
                   zdim(batch));
-        sgemm_split_rows_vec4_kernel<<<grid, 256, 0, s>>>(
-            reinterpret_cast<const float4 *>(src), ld_src / 4, s_src / 4, reinterpret_cast<float4 *>(hi),
-            reinterpret_cast<float4 *>(lo), ld_dst / 4, s_dst / 4, rows, cols / 4, batch);
+        launch_chained(sgemm_split_rows_vec4_kernel, grid, s, reinterpret_cast<const float4 *>(src), ld_src / 4,
+                       s_src / 4, reinterpret_cast<float4 *>(hi), reinterpret_cast<float4 *>(lo), ld_dst / 4,
+                       s_dst / 4, rows, cols / 4, batch);
         return;
     }
     dim3 grid(unsigned(std::min<int64_t>(cdiv(cols, 256), 8)), unsigned(std::min<int64_t>(rows, 65535)), zdim(batch));
-    sgemm_split_rows_kernel<<<grid, 256, 0, s>>>(src, ld_src, s_src, hi, lo, ld_dst, s_dst, rows, cols, batch);
+    launch_chained(sgemm_split_rows_kernel, grid, s, src, ld_src, s_src, hi, lo, ld_dst, s_dst, rows, cols, batch);
 }
 
 cudaError_t preload_aux_kernels() {
