@@ -197,6 +197,7 @@ struct PrepArgs {
     PackJob pack[2];
     int npack;
     EdgeJob edge;
+    int edge_pack;       // pack job that is A (one batch entry): the edge products ride on its repack; -1: none
 };
 cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t s);
 // src[r][c] -> dst[c][r]; with dst2 != NULL the TF32 split: dst = hi, dst2 = lo.

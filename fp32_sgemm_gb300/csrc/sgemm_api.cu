@@ -867,10 +867,13 @@ sgemmStatus_t run(sgemmContext *h, const Problem &q, cudaStream_t stream) {
             return SGEMM_STATUS_WORKSPACE_REQUIRED;
         char *ws = static_cast<char *>(h->ws);
         sg::PrepArgs prep{};
+        prep.edge_pack = -1;
         if (pl.prep_a) {
             float *Ap = reinterpret_cast<float *>(ws);
-            if (pl.prep_a == 1)
+            if (pl.prep_a == 1) {
+                if (pl.edge_cols && batch == 1) prep.edge_pack = prep.npack;
                 prep.pack[prep.npack++] = sg::PackJob{q.A, q.lda, q.sa, Ap, pl.lda_p, pl.sa_p, M, K, batch, 0, 0};
+            }
             else
                 sg::launch_transpose(q.A, q.lda, q.sa, Ap, nullptr, pl.lda_p, pl.sa_p, K, M, batch, stream);
             Ause = Ap;

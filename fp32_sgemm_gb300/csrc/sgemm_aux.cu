@@ -23,134 +23,200 @@ __global__ void sgemm_scale_c_kernel(int M, int N, float beta, float *C, int64_t
         }
 }
 
+// Asynchronous 4-byte copy global -> shared (no registers held while it is
+// in flight); completion is awaited with cp_async_wait_all.
+__device__ __forceinline__ void cp_async_4(float *dst_smem, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One repack unit: columns [4 gbase, 4 gbase + 512) of one row, copied into
+// a destination row whose start is 16-byte aligned.  The source is read
+// once, with evict-first loads (measured: 598.5 -> 595.5 us per call at
+// 4095 x 4097 x 1023, where this launch pays for the previous product's C
+// leaving L2).  The source row may
+// start at any 4-byte offset (odd pitch): lane l reads the 16-byte aligned
+// quad that holds the start of its 4-column group and takes the rest from
+// lane l + 1's quad by a shuffle, so the row is read with 16-byte loads; a
+// quad that reaches outside the row (its first or last) is read element by
+// element, so nothing outside the row is touched.  The padding of the last
+// group is written as zeros.  DOT: also add this lane's columns times the
+// staged B columns (bstrip[jj * K + k]) into s[jj], k in ascending order.
+template <bool DOT>
+__device__ __forceinline__ void repack_chunk(const PackJob &j, const float *src, float *dst, int gbase, int lane,
+                                             const float *bstrip, int K, int r, float (&s)[kEdgeMaxCols]) {
+    const int ph = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3u);   // floats past a 16-byte boundary
+    const float *ab = src - ph;                                              // 16-byte aligned
+    const int cols = j.cols;
+    // Quad m of the aligned row holds row elements 4m - ph .. 4m - ph + 3.
+    auto quad = [&](int m) {
+        const int e0 = 4 * m - ph;
+        if (e0 >= 0 && e0 + 3 < cols) return __ldcs(reinterpret_cast<const float4 *>(ab + 4 * m));
+        float4 q;
+        q.x = (e0 >= 0 && e0 < cols) ? __ldcs(ab + 4 * m) : 0.f;
+        q.y = (e0 + 1 >= 0 && e0 + 1 < cols) ? __ldcs(ab + 4 * m + 1) : 0.f;
+        q.z = (e0 + 2 >= 0 && e0 + 2 < cols) ? __ldcs(ab + 4 * m + 2) : 0.f;
+        q.w = (e0 + 3 >= 0 && e0 + 3 < cols) ? __ldcs(ab + 4 * m + 3) : 0.f;
+        return q;
+    };
+    float4 q4[4], n4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int g = gbase + 32 * q + lane;     // this lane's group: row elements 4g .. 4g + 3
+        // (With ph != 0 the quad after the last group may still hold the
+        // last elements of the row.)
+        q4[q] = (g < j.groups || (ph != 0 && g == j.groups)) ? quad(g) : make_float4(0.f, 0.f, 0.f, 0.f);
+        n4[q] = (lane == 31 && ph != 0 && g < j.groups) ? quad(g + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int g = gbase + 32 * q + lane;
+        // The next quad: lane + 1's, or (lane 31) loaded above.
+        float4 nx;
+        nx.x = __shfl_down_sync(0xffffffffu, q4[q].x, 1);
+        nx.y = __shfl_down_sync(0xffffffffu, q4[q].y, 1);
+        nx.z = __shfl_down_sync(0xffffffffu, q4[q].z, 1);
+        if (lane == 31) nx = n4[q];
+        float4 o;
+        if (ph == 0) o = q4[q];
+        else if (ph == 1) o = make_float4(q4[q].y, q4[q].z, q4[q].w, nx.x);
+        else if (ph == 2) o = make_float4(q4[q].z, q4[q].w, nx.x, nx.y);
+        else o = make_float4(q4[q].w, nx.x, nx.y, nx.z);
+        if (g < j.groups) {
+            *reinterpret_cast<float4 *>(dst + 4 * g) = o;
+            if constexpr (DOT) {
+                const int k0 = 4 * g;                // < K; the group's later columns may pass K
+#pragma unroll
+                for (int jj = 0; jj < kEdgeMaxCols; ++jj) {
+                    if (jj < r) {
+                        const float *b = bstrip + jj * K + k0;
+                        s[jj] = fmaf(o.x, b[0], s[jj]);
+                        if (k0 + 1 < K) s[jj] = fmaf(o.y, b[1], s[jj]);
+                        if (k0 + 2 < K) s[jj] = fmaf(o.z, b[2], s[jj]);
+                        if (k0 + 3 < K) s[jj] = fmaf(o.w, b[3], s[jj]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// C[row][n0 + jj] = alpha * s[jj] (+ beta * C) for jj < r, after summing s
+// across the warp by a fixed butterfly (the same result every run).
+__device__ __forceinline__ void edge_finish(const EdgeJob &e, int64_t row, int lane, float (&s)[kEdgeMaxCols]) {
+#pragma unroll
+    for (int jj = 0; jj < kEdgeMaxCols; ++jj)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s[jj] += __shfl_xor_sync(0xffffffffu, s[jj], o);
+    if (lane == 0) {
+        float *c = e.C + row * e.ldc + e.n0;
+#pragma unroll
+        for (int jj = 0; jj < kEdgeMaxCols; ++jj)
+            if (jj < e.r) c[jj] = e.beta == 0.0f ? e.alpha * s[jj] : fmaf(e.beta, c[jj], e.alpha * s[jj]);
+    }
+}
+
 // Operand preparation in one launch (launched with programmatic stream
 // serialisation: it waits for the kernel before it, and lets the main kernel
 // after it be placed as its CTAs finish), one persistent wave of CTAs:
+//   * up to two repack jobs: rows x cols row-major matrices copied into
+//     buffers whose row pitch is a multiple of 4 floats (16-byte aligned
+//     rows), so that TMA can address them; a warp per (row, 512 columns);
 //   * the edge job: the last r <= kEdgeMaxCols columns of C when the main
 //     kernel leaves them out (a last tile column that thin would multiply
-//     mostly padding): one warp per row of C, lanes striding over k with
-//     FP32 FMAs, then a fixed butterfly sum across the warp, so the result
-//     is the same every run.  C = alpha * sum (+ beta * C, C not read when
-//     beta == 0);
-//   * then up to two repack jobs: rows x cols row-major matrices copied
-//     into buffers whose row pitch is a multiple of 4 floats (16-byte
-//     aligned rows), so that TMA can address them; the padding up to the
-//     next multiple of 4 is written as zeros.
-// At most 64 registers (4 CTAs per SM): both roles are bound by the latency
-// of their loads, so each keeps many loads in flight with short chains.
+//     mostly padding): C = alpha * A . B[:, n0 : n0 + r] (+ beta * C, C not
+//     read when beta == 0).  B's r columns are a strided gather (one cache
+//     line per k): every block stages them in shared memory once, by
+//     asynchronous copies issued first and awaited only after the repacks
+//     that do not need them.  When A is repacked in the same launch
+//     (edge_pack), the products are taken from A's values as the repack
+//     moves them: a warp per row of A, each lane summing its own columns in
+//     ascending order with FP32 FMAs, then a fixed butterfly sum across the
+//     warp; A is read once.  Otherwise a pass of its own over A, a warp per
+//     row, lanes striding over k.
+// At most 64 registers (4 CTAs per SM): every role is bound by the latency
+// of its loads, so each keeps many loads in flight with short chains.
 __global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constant__ PrepArgs p) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;                  // warp in block
     const int wpb = blockDim.x >> 5;
-    if (p.edge.r > 0) {
-        // B's columns [n0, n0 + r) are a strided gather (one cache line per
-        // k): every block stages all of them in shared memory once, column
-        // by column so that lanes reading consecutive k hit consecutive
-        // banks; then its warps take rows of C round robin.
-        extern __shared__ float bstrip[];   // [r][K]
-        const EdgeJob &e = p.edge;
+    const int64_t gw = (int64_t)blockIdx.x * wpb + wib;
+    const int64_t warps = (int64_t)gridDim.x * wpb;
+    extern __shared__ float bstrip[];                  // [r][K], the edge job's columns of B
+    const EdgeJob &e = p.edge;
+    const bool edge = e.r > 0;
+    if (edge) {
+        // Column by column, so that lanes reading consecutive k hit
+        // consecutive banks.
         for (int t = threadIdx.x; t < e.K * e.r; t += blockDim.x) {
             const int kk = t / e.r, jj = t - kk * e.r;
-            bstrip[jj * e.K + kk] = e.B[(int64_t)kk * e.ldb + e.n0 + jj];
+            cp_async_4(&bstrip[jj * e.K + kk], &e.B[(int64_t)kk * e.ldb + e.n0 + jj]);
         }
-        __syncthreads();
-        for (int row = blockIdx.x * wpb + wib; row < e.M; row += gridDim.x * wpb) {
-            float s[kEdgeMaxCols];
-#pragma unroll
-            for (int j = 0; j < kEdgeMaxCols; ++j) s[j] = 0.f;
-            const float *a = e.A + (int64_t)row * e.lda;
-            // Sixteen k steps' loads of A in flight per lane; every sum takes
-            // k in ascending order.
-            int k = lane;
-            for (; k + 15 * 32 < e.K; k += 16 * 32) {
-                float av[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) av[u] = a[k + 32 * u];
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-#pragma unroll
-                    for (int j = 0; j < kEdgeMaxCols; ++j)
-                        if (j < e.r) s[j] = fmaf(av[u], bstrip[j * e.K + k + 32 * u], s[j]);
-            }
-            for (; k < e.K; k += 32) {
-                const float av = a[k];
-#pragma unroll
-                for (int j = 0; j < kEdgeMaxCols; ++j)
-                    if (j < e.r) s[j] = fmaf(av, bstrip[j * e.K + k], s[j]);
-            }
-#pragma unroll
-            for (int j = 0; j < kEdgeMaxCols; ++j)
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
-            if (lane == 0) {
-                float *c = e.C + (int64_t)row * e.ldc + e.n0;
-#pragma unroll
-                for (int j = 0; j < kEdgeMaxCols; ++j)
-                    if (j < e.r) c[j] = e.beta == 0.0f ? e.alpha * s[j] : fmaf(e.beta, c[j], e.alpha * s[j]);
-            }
-        }
+        cp_async_commit();
     }
+    float s[kEdgeMaxCols];
 
-    // Repacks: a warp per unit of 512 columns of one row (of either job,
-    // rows of all batch entries in turn).  The source row may start at any
-    // 4-byte offset (odd pitch): lane l reads the 16-byte aligned quad that
-    // holds the start of its 4-column group and takes the rest from lane
-    // l + 1's quad by a shuffle, so the row is read with 16-byte loads; a
-    // quad that reaches outside the row (its first or last) is read element
-    // by element, so nothing outside the row is touched.
-    const int64_t total = p.pack[0].units + p.pack[1].units;   // (row, chunk) units
-    const int64_t warps = (int64_t)gridDim.x * wpb;
-    for (int64_t w = (int64_t)blockIdx.x * wpb + wib; w < total; w += warps) {
-        const bool second = w >= p.pack[0].units;
+    // The repack units of the jobs the edge job does not ride on, rows of
+    // all batch entries in turn.
+    const int fused = edge ? p.edge_pack : -1;
+    const int64_t u0 = fused == 0 ? 0 : p.pack[0].units;
+    const int64_t u1 = fused == 1 ? 0 : p.pack[1].units;
+    for (int64_t w = gw; w < u0 + u1; w += warps) {
+        const bool second = w >= u0;
         const PackJob &j = second ? p.pack[1] : p.pack[0];
-        const int64_t v = second ? w - p.pack[0].units : w;
+        const int64_t v = second ? w - u0 : w;
         const int64_t chunks = (j.groups + 127) / 128;
         const int64_t zr = v / chunks;
         const int gbase = (int)(v - zr * chunks) * 128;
         const int64_t z = zr / j.rows, r = zr - z * j.rows;
-        const float *src = j.src + z * j.s_src + r * j.ld_src;
-        float *dst = j.dst + z * j.s_dst + r * j.ld_dst;
-        const int ph = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3u);   // floats past a 16-byte boundary
-        const float *ab = src - ph;                                              // 16-byte aligned
-        const int cols = j.cols;
-        // Quad m of the aligned row holds row elements 4m - ph .. 4m - ph + 3.
-        auto quad = [&](int m) {
-            const int e0 = 4 * m - ph;
-            if (e0 >= 0 && e0 + 3 < cols) return *reinterpret_cast<const float4 *>(ab + 4 * m);
-            float4 q;
-            q.x = (e0 >= 0 && e0 < cols) ? ab[4 * m] : 0.f;
-            q.y = (e0 + 1 >= 0 && e0 + 1 < cols) ? ab[4 * m + 1] : 0.f;
-            q.z = (e0 + 2 >= 0 && e0 + 2 < cols) ? ab[4 * m + 2] : 0.f;
-            q.w = (e0 + 3 >= 0 && e0 + 3 < cols) ? ab[4 * m + 3] : 0.f;
-            return q;
-        };
-        float4 q4[4], n4[4];
+        repack_chunk<false>(j, j.src + z * j.s_src + r * j.ld_src, j.dst + z * j.s_dst + r * j.ld_dst, gbase,
+                            lane, nullptr, 0, 0, s);
+    }
+    if (!edge) return;
+
+    cp_async_wait_all();
+    __syncthreads();
+    if (fused >= 0) {
+        // A's repack carrying the edge products (one batch entry): a warp per row.
+        const PackJob &j = p.pack[fused];
+        for (int64_t row = gw; row < j.rows; row += warps) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int g = gbase + 32 * q + lane;     // this lane's group: row elements 4g .. 4g + 3
-            // (With ph != 0 the quad after the last group may still hold the
-            // last elements of the row.)
-            q4[q] = (g < j.groups || (ph != 0 && g == j.groups)) ? quad(g) : make_float4(0.f, 0.f, 0.f, 0.f);
-            n4[q] = (lane == 31 && ph != 0 && g < j.groups) ? quad(g + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int jj = 0; jj < kEdgeMaxCols; ++jj) s[jj] = 0.f;
+            const float *src = j.src + row * j.ld_src;
+            float *dst = j.dst + row * j.ld_dst;
+            for (int gbase = 0; gbase < j.groups; gbase += 128)
+                repack_chunk<true>(j, src, dst, gbase, lane, bstrip, e.K, e.r, s);
+            edge_finish(e, row, lane, s);
         }
+        return;
+    }
+    for (int64_t row = gw; row < e.M; row += warps) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int g = gbase + 32 * q + lane;
-            // The next quad: lane + 1's, or (lane 31) loaded above.
-            float4 nx;
-            nx.x = __shfl_down_sync(0xffffffffu, q4[q].x, 1);
-            nx.y = __shfl_down_sync(0xffffffffu, q4[q].y, 1);
-            nx.z = __shfl_down_sync(0xffffffffu, q4[q].z, 1);
-            if (lane == 31) nx = n4[q];
-            float4 o;
-            if (ph == 0) o = q4[q];
-            else if (ph == 1) o = make_float4(q4[q].y, q4[q].z, q4[q].w, nx.x);
-            else if (ph == 2) o = make_float4(q4[q].z, q4[q].w, nx.x, nx.y);
-            else o = make_float4(q4[q].w, nx.x, nx.y, nx.z);
-            if (g < j.groups) *reinterpret_cast<float4 *>(dst + 4 * g) = o;
+        for (int jj = 0; jj < kEdgeMaxCols; ++jj) s[jj] = 0.f;
+        const float *a = e.A + row * e.lda;
+        // Sixteen k steps' loads of A in flight per lane; every sum takes k
+        // in ascending order.
+        int k = lane;
+        for (; k + 15 * 32 < e.K; k += 16 * 32) {
+            float av[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) av[u] = a[k + 32 * u];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+#pragma unroll
+                for (int jj = 0; jj < kEdgeMaxCols; ++jj)
+                    if (jj < e.r) s[jj] = fmaf(av[u], bstrip[jj * e.K + k + 32 * u], s[jj]);
         }
+        for (; k < e.K; k += 32) {
+            const float av = a[k];
+#pragma unroll
+            for (int jj = 0; jj < kEdgeMaxCols; ++jj)
+                if (jj < e.r) s[jj] = fmaf(av, bstrip[jj * e.K + k], s[jj]);
+        }
+        edge_finish(e, row, lane, s);
     }
 }
 
@@ -343,15 +409,20 @@ void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t str
 
 cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t s) {
     int64_t units = 0;
+    if (p.edge.r == 0 || p.edge_pack >= p.npack) p.edge_pack = -1;
     for (int i = 0; i < 2; ++i) {
         PackJob &j = p.pack[i];
         if (i >= p.npack) j = PackJob{};
         j.groups = (j.cols + 3) / 4;
-        j.units = (int64_t)j.batch * j.rows * cdiv(j.groups, 128);   // (row, 512-column chunk)
-        units += j.units;
+        if (i == p.edge_pack) {
+            j.units = j.rows;                                         // rows (one batch entry)
+        } else {
+            j.units = (int64_t)j.batch * j.rows * cdiv(j.groups, 128);   // (row, 512-column chunk)
+            units += j.units;
+        }
     }
     // One persistent wave: four CTAs of eight warps per SM, every warp takes
-    // edge rows and then repack units in turn.
+    // repack units and then edge rows in turn.
     const int64_t warps_needed = std::max<int64_t>(units, p.edge.r > 0 ? p.edge.M : 0);
     const int blocks = (int)std::min<int64_t>(cdiv(warps_needed, 8), 4 * (int64_t)sms);
     if (blocks == 0) return cudaSuccess;

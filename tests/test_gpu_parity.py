@@ -637,6 +637,7 @@ def test_tma_store_epilogue_batched(sg, handle):
     (2048, 2048 + 3, 1100, 1101, 2051, 2053, 0.5, 0.25),      # both repacked, C read
     (1500, 1024 + 8, 1500, None, 1040, 1036, 1.0, -1.0),      # C 16-byte aligned, read
     (3000, 512 + 5, 800, 801, None, None, 2.0, 0.0),
+    (2100, 640 + 7, 1001, 1003, None, None, 1.0, 0.5),        # K mod 4 = 1, products ride on A's repack
     (1500, 1024 + 8, 2048, None, 1040, 1036, 1.0, -1.0),      # K x r too large: full tiles
 ])
 def test_edge_columns_split_off(sg, handle, M, N, K, lda, ldb, ldc, alpha, beta):
