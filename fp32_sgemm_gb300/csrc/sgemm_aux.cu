@@ -31,14 +31,20 @@ __device__ __forceinline__ void cp_async_4(float *dst_smem, const float *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// One repack unit: columns [4 gbase, 4 gbase + 512) of one row, copied into
-// a destination row whose start is 16-byte aligned.  The source is read
+// Quads (16-byte groups of 4 columns) per lane in one repack unit: a unit is
+// 32 * kPackQuads groups of one row, all its loads issued before any store.
+constexpr int kPackQuads = 8;
+constexpr int kPackGroups = 32 * kPackQuads;
+
+// One repack unit: columns [4 gbase, 4 (gbase + kPackGroups)) of one row,
+// copied into a destination row whose start is 16-byte aligned.  The source is read
 // once, with evict-first loads (measured: 598.5 -> 595.5 us per call at
 // 4095 x 4097 x 1023, where this launch pays for the previous product's C
 // leaving L2).  The source row may
 // start at any 4-byte offset (odd pitch): lane l reads the 16-byte aligned
 // quad that holds the start of its 4-column group and takes the rest from
-// lane l + 1's quad by a shuffle, so the row is read with 16-byte loads; a
+// lane l + 1's quad by a shuffle (lane 31 from lane 0's next quad), so the
+// row is read with 16-byte loads; a
 // quad that reaches outside the row (its first or last) is read element by
 // element, so nothing outside the row is touched.  The padding of the last
 // group is written as zeros.  DOT: also add this lane's columns times the
@@ -60,24 +66,33 @@ __device__ __forceinline__ void repack_chunk(const PackJob &j, const float *src,
         q.w = (e0 + 3 >= 0 && e0 + 3 < cols) ? __ldcs(ab + 4 * m + 3) : 0.f;
         return q;
     };
-    float4 q4[4], n4[4];
+    float4 q4[kPackQuads];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kPackQuads; ++q) {
         const int g = gbase + 32 * q + lane;     // this lane's group: row elements 4g .. 4g + 3
         // (With ph != 0 the quad after the last group may still hold the
         // last elements of the row.)
         q4[q] = (g < j.groups || (ph != 0 && g == j.groups)) ? quad(g) : make_float4(0.f, 0.f, 0.f, 0.f);
-        n4[q] = (lane == 31 && ph != 0 && g < j.groups) ? quad(g + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // The quad after the unit's last one, for lane 31 (the others take it from lane 0).
+    const int g_last = gbase + 32 * (kPackQuads - 1) + 31;
+    const float4 after = (lane == 31 && ph != 0 && g_last < j.groups) ? quad(g_last + 1)
+                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kPackQuads; ++q) {
         const int g = gbase + 32 * q + lane;
-        // The next quad: lane + 1's, or (lane 31) loaded above.
-        float4 nx;
+        // The next quad: lane + 1's; for lane 31, lane 0's next one (or the
+        // one loaded above).
+        float4 nx, wrap = after;
         nx.x = __shfl_down_sync(0xffffffffu, q4[q].x, 1);
         nx.y = __shfl_down_sync(0xffffffffu, q4[q].y, 1);
         nx.z = __shfl_down_sync(0xffffffffu, q4[q].z, 1);
-        if (lane == 31) nx = n4[q];
+        if (q + 1 < kPackQuads) {
+            wrap.x = __shfl_sync(0xffffffffu, q4[q + 1].x, 0);
+            wrap.y = __shfl_sync(0xffffffffu, q4[q + 1].y, 0);
+            wrap.z = __shfl_sync(0xffffffffu, q4[q + 1].z, 0);
+        }
+        if (lane == 31) nx = wrap;
         float4 o;
         if (ph == 0) o = q4[q];
         else if (ph == 1) o = make_float4(q4[q].y, q4[q].z, q4[q].w, nx.x);
@@ -122,7 +137,7 @@ __device__ __forceinline__ void edge_finish(const EdgeJob &e, int64_t row, int l
 // after it be placed as its CTAs finish), one persistent wave of CTAs:
 //   * up to two repack jobs: rows x cols row-major matrices copied into
 //     buffers whose row pitch is a multiple of 4 floats (16-byte aligned
-//     rows), so that TMA can address them; a warp per (row, 512 columns);
+//     rows), so that TMA can address them; a warp per (row, 1024 columns);
 //   * the edge job: the last r <= kEdgeMaxCols columns of C when the main
 //     kernel leaves them out (a last tile column that thin would multiply
 //     mostly padding): C = alpha * A . B[:, n0 : n0 + r] (+ beta * C, C not
@@ -135,9 +150,13 @@ __device__ __forceinline__ void edge_finish(const EdgeJob &e, int64_t row, int l
 //     ascending order with FP32 FMAs, then a fixed butterfly sum across the
 //     warp; A is read once.  Otherwise a pass of its own over A, a warp per
 //     row, lanes striding over k.
-// At most 64 registers (4 CTAs per SM): every role is bound by the latency
-// of its loads, so each keeps many loads in flight with short chains.
-__global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constant__ PrepArgs p) {
+// Every role is bound by the latency of its loads, so each keeps many loads
+// in flight with short chains: a repack unit's 8 quads per lane are all
+// loaded before any is stored, in two CTAs per SM of up to 128 registers a
+// thread (measured per call, 2048 x 2051 x 1100 with odd pitches: 177.9 us,
+// against 183.5 with 4 quads per lane and four CTAs per SM; 8 quads in 64
+// registers spilled, 190.7).
+__global__ void __launch_bounds__(256, 2) sgemm_prep_kernel(const __grid_constant__ PrepArgs p) {
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -168,9 +187,9 @@ __global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constan
         const bool second = w >= u0;
         const PackJob &j = second ? p.pack[1] : p.pack[0];
         const int64_t v = second ? w - u0 : w;
-        const int64_t chunks = (j.groups + 127) / 128;
+        const int64_t chunks = (j.groups + kPackGroups - 1) / kPackGroups;
         const int64_t zr = v / chunks;
-        const int gbase = (int)(v - zr * chunks) * 128;
+        const int gbase = (int)(v - zr * chunks) * kPackGroups;
         const int64_t z = zr / j.rows, r = zr - z * j.rows;
         repack_chunk<false>(j, j.src + z * j.s_src + r * j.ld_src, j.dst + z * j.s_dst + r * j.ld_dst, gbase,
                             lane, nullptr, 0, 0, s);
@@ -187,7 +206,7 @@ __global__ void __launch_bounds__(256, 4) sgemm_prep_kernel(const __grid_constan
             for (int jj = 0; jj < kEdgeMaxCols; ++jj) s[jj] = 0.f;
             const float *src = j.src + row * j.ld_src;
             float *dst = j.dst + row * j.ld_dst;
-            for (int gbase = 0; gbase < j.groups; gbase += 128)
+            for (int gbase = 0; gbase < j.groups; gbase += kPackGroups)
                 repack_chunk<true>(j, src, dst, gbase, lane, bstrip, e.K, e.r, s);
             edge_finish(e, row, lane, s);
         }
@@ -417,14 +436,14 @@ cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t s) {
         if (i == p.edge_pack) {
             j.units = j.rows;                                         // rows (one batch entry)
         } else {
-            j.units = (int64_t)j.batch * j.rows * cdiv(j.groups, 128);   // (row, 512-column chunk)
+            j.units = (int64_t)j.batch * j.rows * cdiv(j.groups, kPackGroups);   // (row, chunk)
             units += j.units;
         }
     }
-    // One persistent wave: four CTAs of eight warps per SM, every warp takes
+    // One persistent wave: two CTAs of eight warps per SM, every warp takes
     // repack units and then edge rows in turn.
     const int64_t warps_needed = std::max<int64_t>(units, p.edge.r > 0 ? p.edge.M : 0);
-    const int blocks = (int)std::min<int64_t>(cdiv(warps_needed, 8), 4 * (int64_t)sms);
+    const int blocks = (int)std::min<int64_t>(cdiv(warps_needed, 8), 2 * (int64_t)sms);
     if (blocks == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)blocks);
