@@ -377,27 +377,43 @@ int64_t stream_k_ctas(int64_t tiles, int64_t k_blocks, int64_t slots, bool even_
 
 int choose_tf32x3_config(const sgemmContext *h, const Problem &q) {
     if (h->algo >= 1 && h->algo <= sg::kNumTf32x3Configs) return h->algo;
-    // The SM-pair tile (256 x 256, each SM staging and reading half of B)
-    // wins once its tiles occupy at least half of the pairs; measured main
-    // kernel against the 128 x 256 tile: 4096^3 450.8 / 516.5 us, 8192^3
-    // 3467 / 3836 us, 2048^3 (64 tiles) 71.3 / 76.2 us, but 1024^3 (16
-    // tiles) 36.4 / 32.4 us.
-    if (4 * ceil_div(q.M, 256) * ceil_div(q.N, 256) * q.batch >= h->sm_count && ceil_div(q.K, 32) >= 4)
-        return 4;
-    // With stream-K evening out the last wave, the widest tile wins as soon
-    // as it fills the chip once: it reads the fewest shared-memory bytes per
-    // MMA, the resource this kernel is bound by.
-    if (h->schedule != 1 && ceil_div(q.M, 128) * ceil_div(q.N, 256) * q.batch >= h->sm_count &&
-        ceil_div(q.K, 32) >= 4)
-        return 3;
+    // Among the tiles whose count fills the chip (with stream-K evening out
+    // the last wave), the least padded tile area per element of C over the
+    // tile's relative speed wins.  Speeds from the measured main kernels:
+    // 128 x 128 0.86, 128 x 256 0.91 (fewer shared-memory bytes per MMA,
+    // the resource this kernel is bound by), 256 x 256 on an SM pair 1.04
+    // (4096^3: 516.5 us for 128 x 256, 450.8 us for the pair tile).  The
+    // padding matters for batches of small matrices (300 x 64 x 64 x 512:
+    // 81.0 us with 128 x 128 tiles, 95.8 with 128 x 256, 121.0 with the pair
+    // tile).  The pair tile counts as filling the chip at half of the pairs
+    // (2048^3, 64 tiles: 71.3 us against 76.2 for 128 x 256; 1024^3, 16
+    // tiles: 36.4 against 32.4).
+    const int64_t sms = h->sm_count;
+    const bool deep = ceil_div(q.K, 32) >= 4;
+    auto tiles = [&](int64_t bm, int64_t bn) { return ceil_div(q.M, bm) * ceil_div(q.N, bn) * q.batch; };
+    auto cost = [&](int64_t bm, int64_t bn, double speed) {
+        return double(ceil_div(q.M, bm) * bm) * double(ceil_div(q.N, bn) * bn) /
+               (double(q.M) * double(q.N) * speed);
+    };
+    int pick = 0;
+    double pick_cost = 0.0;
+    auto consider = [&](int cfg, double c) {
+        if (pick == 0 || c < pick_cost) { pick = cfg; pick_cost = c; }
+    };
+    if (deep && 4 * tiles(256, 256) >= sms) consider(4, cost(256, 256, 1.04));
+    if (deep && h->schedule != 1 && tiles(128, 256) >= sms) consider(3, cost(128, 256, 0.91));
+    if (pick != 0) {
+        if (tiles(128, 128) >= sms) consider(1, cost(128, 128, 0.86));
+        return pick;
+    }
     const double width[2] = {128.0, 256.0};
     const double eff[2] = {0.86, 0.91};
     const int cfg[2] = {1, 3};
     int best = 1;
     double best_t = 0.0;
     for (int i = 0; i < 2; ++i) {
-        const int64_t tiles = ceil_div(q.M, 128) * ceil_div(q.N, int64_t(width[i])) * q.batch;
-        const double t = double(ceil_div(tiles, h->sm_count)) * width[i] / eff[i];
+        const int64_t t_i = ceil_div(q.M, 128) * ceil_div(q.N, int64_t(width[i])) * q.batch;
+        const double t = double(ceil_div(t_i, sms)) * width[i] / eff[i];
         if (i == 0 || t < best_t) { best_t = t; best = cfg[i]; }
     }
     return best;
