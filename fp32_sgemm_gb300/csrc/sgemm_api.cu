@@ -313,20 +313,33 @@ int choose_algo(const sgemmContext *h, const Problem &q) {
     if (q.N <= 32) return 19 - 1;
     if (q.M <= 64 && q.M <= q.N) return 16 - 1;
     if (q.N <= 64) return 17 - 1;
+    // Tile shape: the least padded area per element of C over the tile's
+    // relative speed, 256 x 128 and 128 x 256 1.0, 128 x 128 (configuration
+    // 10: four warps, two CTAs per SM) 0.88 (measured on batches: 100 x
+    // 200 x 300 x 400, equal padding, 129.7 / 148.5 us; 40 x 300 x 300 x
+    // 1024, padding 2.18 / 1.64: 257.2 / 215.5 us).  Between the first two,
+    // equal padding goes to 128 x 256 under 256 rows or for products more
+    // than twice as wide as tall.
+    const int64_t tall_area = ceil_div(q.M, 256) * 256 * ceil_div(q.N, 128) * 128;
+    const int64_t wide_area = ceil_div(q.M, 128) * 128 * ceil_div(q.N, 256) * 256;
+    const int64_t square_area = ceil_div(q.M, 128) * 128 * ceil_div(q.N, 128) * 128;
+    const bool wide = tall_area == wide_area ? (q.M < 256 || q.N > 2 * q.M) : wide_area < tall_area;
+    const bool short_k = q.K <= 64 && q.K % 32 != 0;   // slices no deeper than needed (below)
+    if (!short_k && double(square_area) / 0.88 < double(std::min(tall_area, wide_area))) return 10 - 1;
     // Staging-area epilogues: TMA stores (beta == 0, aligned C) or row runs
     // (C not 16-byte aligned; 4095 x 4097 x 1023 with beta = 0.25:
     // 669 -> 617 us).  Aligned C with beta != 0 keeps the register epilogue.
     if (c_vector_ok(q) ? q.beta == 0.0f : true) {
-        if (q.M < 256 || q.N > 2 * q.M) return kWideStoreTmaAlgo - 1;
+        if (wide) return kWideStoreTmaAlgo - 1;
         // Short K: the K slice that divides K (32, 16, else 8 deep).
-        if (q.K <= 64 && q.K % 32 != 0) return (q.K % 16 == 0 ? 23 : 24) - 1;
+        if (short_k) return (q.K % 16 == 0 ? 23 : 24) - 1;
         return kStoreTmaAlgo - 1;
     }
-    if (q.M < 256 || q.N > 2 * q.M) return kWideAlgo - 1;
+    if (wide) return kWideAlgo - 1;
     // Short K (writing C bounds the product): slices no deeper than needed,
     // so that little zero padding is multiplied (measured at 16384^2: K = 8
     // 393 -> 213 us with 8-deep slices, K = 16 393 -> 278 us with 16-deep).
-    if (q.K <= 64 && q.K % 32 != 0) return (q.K % 16 == 0 || q.K > 32 ? 20 : 21) - 1;
+    if (short_k) return (q.K % 16 == 0 || q.K > 32 ? 20 : 21) - 1;
     return kDefaultAlgo - 1;
 }
 

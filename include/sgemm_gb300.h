@@ -275,13 +275,16 @@ sgemmStatus_t sgemmQueryPlan(sgemmHandle_t handle, int64_t M, int64_t N,
  * Pin the main kernel's tile configuration for calls on this handle:
  * 0 = automatic choice by shape (default: 10 when both sides are at most
  * 128, 18 / 19 for large products of 17 to 32 rows / columns, 16 for at
- * most 64 rows, 17 for at most 64 columns; then, when beta == 0 and C is
- * 16-byte aligned or when C is not 16-byte aligned (C through a
- * shared-memory staging area), 27 under 256 rows or for products more than
- * twice as wide as tall, 23 / 24 for K of at most 64 that is a multiple of
- * 16 / not a multiple of 16 (multiples of 32 excepted), else 28; otherwise
- * 30 under 256 rows or for wide products, 20 / 21 for K of at most 64 that
- * is not a multiple of 32, else 29).  Fixed configurations (every one
+ * most 64 rows, 17 for at most 64 columns; otherwise the tile shape with
+ * the least padded area per element of C over its relative speed (256 x 128
+ * and 128 x 256: 1, 128 x 128 of configuration 10: 0.88, not for the short
+ * K below), a tie between the first two going to 128 x 256 under 256 rows
+ * or for products more than twice as wide as tall; then, when beta == 0 and
+ * C is 16-byte aligned or when C is not 16-byte aligned (C through a
+ * shared-memory staging area), 27 for 128 x 256, 23 / 24 for K of at most
+ * 64 that is a multiple of 16 / not a multiple of 16 (multiples of 32
+ * excepted), else 28; otherwise 30 for 128 x 256, 20 / 21 for K of at most
+ * 64 that is not a multiple of 32, else 29).  Fixed configurations (every one
  * but 10 is eight warps in one CTA per SM; fp32_sgemm_gb300/csrc/
  * sgemm_algo*.cu):
  *   10 = 128 x 128, four warps, two CTAs per SM;
