@@ -672,3 +672,18 @@ def test_edge_columns_only_in_the_automatic_setting(sg, handle):
     handle.set_algo(0)
     assert plan["edge_cols"] == 0
     np.testing.assert_array_equal(_gpu(sg, handle, p, algo=28).astype(np.float64), _ref(p))
+
+
+@pytest.mark.parametrize("M,N,K,want", [
+    (4096, 4096, 4096, (256, 128)),
+    (300, 300, 4096, (128, 128)),    # 128 x 128 pads 1.64x, the 256-wide tiles 2.18x
+    (200, 4096, 512, (128, 256)),    # equal padding, under 256 rows
+    (4095, 4097, 1023, (256, 128)),
+])
+def test_tile_shape_follows_padding(sg, handle, M, N, K, want):
+    handle.set_algo(0)
+    A = torch.empty((M, K), device="cuda")
+    B = torch.empty((K, N), device="cuda")
+    C = torch.empty((M, N), device="cuda")
+    plan = handle.plan(A, B, C)
+    assert plan["kind"] == 1 and (plan["tile_m"], plan["tile_n"]) == want, plan
