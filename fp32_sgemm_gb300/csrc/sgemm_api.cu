@@ -765,20 +765,37 @@ sgemmStatus_t run_tf32x3(sgemmContext *h, const Plan &pl, const Problem &q, cuda
     const int M = int(q.M), N = int(q.N), K = int(q.K), batch = int(q.batch);
     const int64_t sa_d = q.M * pl.kp, sb_d = q.N * pl.kp;
     // A_hi / A_lo as [batch][M][kp] and B_hi / B_lo as [batch][N][kp]: K
-    // contiguous for both, whatever the stored layout.
-    if (q.opA == 0) sg::launch_split_rows(q.A, q.lda, q.sa, a_hi, a_lo, pl.kp, sa_d, M, K, batch, stream);
+    // contiguous for both, whatever the stored layout.  The high part is the
+    // operand itself (the MMA reads its TF32 bits), so an operand stored K
+    // contiguous that TMA can address is read in place as its high part and
+    // only its residual is written: the split of A moves 128 instead of 192
+    // MB at 4096^3 (516.0 -> 504.5 us per call).  Only up to 64 MB of
+    // operand: a larger one read in place did not pay (8192^3: 3577 -> 3608
+    // us per call; 6144^3 no gain).
+    const int64_t kDirectMaxBytes = int64_t(64) << 20;
+    const bool a_direct = q.opA == 0 && tma_ok_batched(q.A, q.lda, q.sa, q.batch) &&
+                          q.batch * q.M * q.K * 4 <= kDirectMaxBytes;
+    const bool b_direct = q.opB == 1 && tma_ok_batched(q.B, q.ldb, q.sb, q.batch) &&
+                          q.batch * q.N * q.K * 4 <= kDirectMaxBytes;
+    if (q.opA == 0)
+        sg::launch_split_rows(q.A, q.lda, q.sa, a_direct ? nullptr : a_hi, a_lo, pl.kp, sa_d, M, K, batch, stream);
     else sg::launch_transpose(q.A, q.lda, q.sa, a_hi, a_lo, pl.kp, sa_d, K, M, batch, stream);
     if (q.opB == 0) sg::launch_transpose(q.B, q.ldb, q.sb, b_hi, b_lo, pl.kp, sb_d, K, N, batch, stream);
-    else sg::launch_split_rows(q.B, q.ldb, q.sb, b_hi, b_lo, pl.kp, sb_d, N, K, batch, stream);
+    else sg::launch_split_rows(q.B, q.ldb, q.sb, b_direct ? nullptr : b_hi, b_lo, pl.kp, sb_d, N, K, batch, stream);
     if (last_launch() != SGEMM_STATUS_SUCCESS) return SGEMM_STATUS_LAUNCH_FAILED;
 
     CUtensorMap tm[4];
-    const float *ptrs[4] = {a_hi, a_lo, b_hi, b_lo};
+    const float *ptrs[4] = {a_direct ? q.A : a_hi, a_lo, b_direct ? q.B : b_hi, b_lo};
     for (int i = 0; i < 4; ++i) {
         const bool is_a = i < 2;
-        sgemmStatus_t st = encode_3d(&tm[i], ptrs[i], q.K, is_a ? q.M : q.N, q.batch, pl.kp,
-                                     is_a ? sa_d : sb_d, info.bk, is_a ? info.box_a : info.box_b,
-                                     CU_TENSOR_MAP_SWIZZLE_128B);
+        const bool direct = i == 0 ? a_direct : i == 2 ? b_direct : false;
+        int64_t ld = pl.kp, bstride = is_a ? sa_d : sb_d;
+        if (direct) {
+            ld = is_a ? q.lda : q.ldb;
+            bstride = q.batch == 1 ? ld * (is_a ? q.M : q.N) : (is_a ? q.sa : q.sb);
+        }
+        sgemmStatus_t st = encode_3d(&tm[i], ptrs[i], q.K, is_a ? q.M : q.N, q.batch, ld, bstride, info.bk,
+                                     is_a ? info.box_a : info.box_b, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != SGEMM_STATUS_SUCCESS) return st;
     }
     sg::Tf32x3Args args{};

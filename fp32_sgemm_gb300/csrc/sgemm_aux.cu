@@ -245,7 +245,12 @@ __global__ void __launch_bounds__(256, 2) sgemm_prep_kernel(const __grid_constan
 // destination row segments (VEC_DST).  Row pitch 65 keeps shared-memory
 // accesses at most two-way conflicted.
 //   SPLIT = false: plain copy (operands given transposed, for the FFMA path);
-//   SPLIT = true : dst gets tf32(x), dst2 gets tf32(x - tf32(x)) (3xTF32 path).
+//   SPLIT = true : dst gets tf32_trunc(x) (the TF32 part the MMA would read
+//                  of x), dst2 the residual tf32_rna(x - tf32_trunc(x))
+//                  (3xTF32 path).  The high part is stored with its low bits
+//                  cleared: the same products, but the tensor cores ran
+//                  slower on operands whose dropped bits were not zero
+//                  (8192^3 main kernel 3369 us against 3412-3430).
 template <bool SPLIT, bool VEC_SRC, bool VEC_DST>
 __global__ void __launch_bounds__(256)
 sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
@@ -279,9 +284,8 @@ sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if constexpr (SPLIT) {
-                    const float xh = tf32_rna(x[i][e]);
-                    t0[ty + 16 * i][4 * tx + e] = xh;
-                    t1[ty + 16 * i][4 * tx + e] = tf32_rna(x[i][e] - xh);
+                    t0[ty + 16 * i][4 * tx + e] = tf32_trunc(x[i][e]);
+                    t1[ty + 16 * i][4 * tx + e] = tf32_rna(x[i][e] - tf32_trunc(x[i][e]));
                 } else {
                     t0[ty + 16 * i][4 * tx + e] = x[i][e];
                 }
@@ -322,7 +326,9 @@ sgemm_transpose_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_
     }
 }
 
-// Row-major split into TF32 hi / lo parts (3xTF32 path), scalar.
+// Row-major split into hi / lo parts (3xTF32 path), scalar: hi =
+// tf32_trunc(x), lo = tf32_rna(x - tf32_trunc(x)).  hi == nullptr: only lo
+// is written (the MMA reads hi from the operand in place).
 __global__ void sgemm_split_rows_kernel(const float *__restrict__ src, int64_t ld_src, int64_t s_src,
                                         float *__restrict__ hi, float *__restrict__ lo, int64_t ld_dst,
                                         int64_t s_dst, int rows, int cols, int batch) {
@@ -331,20 +337,20 @@ __global__ void sgemm_split_rows_kernel(const float *__restrict__ src, int64_t l
     for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
         for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
             const float *sr = src + z * s_src + r * ld_src;
-            float *h = hi + z * s_dst + r * ld_dst;
+            float *h = hi != nullptr ? hi + z * s_dst + r * ld_dst : nullptr;
             float *l = lo + z * s_dst + r * ld_dst;
             for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x) {
                 const float x = sr[c];
-                const float xh = tf32_rna(x);
-                h[c] = xh;
-                l[c] = tf32_rna(x - xh);
+                if (hi != nullptr) h[c] = tf32_trunc(x);
+                l[c] = tf32_rna(x - tf32_trunc(x));
             }
         }
 }
 
 // Same, 16 bytes at a time (src and dst 16-byte aligned; pitches, batch
 // strides and cols multiples of 4 floats).  A block covers 1024 float4 of a
-// row; each thread issues its four loads before any store.
+// row; each thread issues its four loads before any store.  The source is
+// read evict-first unless the main kernel reads it again (hi == nullptr).
 __global__ void __launch_bounds__(256)
 sgemm_split_rows_vec4_kernel(const float4 *__restrict__ src, int64_t ld4, int64_t s4,
                              float4 *__restrict__ hi, float4 *__restrict__ lo, int64_t ldd4,
@@ -354,22 +360,22 @@ sgemm_split_rows_vec4_kernel(const float4 *__restrict__ src, int64_t ld4, int64_
     for (int64_t z = blockIdx.z; z < batch; z += gridDim.z)
         for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
             const float4 *sr = src + z * s4 + r * ld4;
-            float4 *h = hi + z * sd4 + r * ldd4;
+            float4 *h = hi != nullptr ? hi + z * sd4 + r * ldd4 : nullptr;
             float4 *l = lo + z * sd4 + r * ldd4;
             const int c = blockIdx.x * 1024 + threadIdx.x;
             float4 x[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if (c + 256 * i < cols4) x[i] = __ldcs(&sr[c + 256 * i]);
+                if (c + 256 * i < cols4) x[i] = hi != nullptr ? __ldcs(&sr[c + 256 * i]) : sr[c + 256 * i];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 if (c + 256 * i < cols4) {
-                    float4 xh, xl;
-                    xh.x = tf32_rna(x[i].x); xl.x = tf32_rna(x[i].x - xh.x);
-                    xh.y = tf32_rna(x[i].y); xl.y = tf32_rna(x[i].y - xh.y);
-                    xh.z = tf32_rna(x[i].z); xl.z = tf32_rna(x[i].z - xh.z);
-                    xh.w = tf32_rna(x[i].w); xl.w = tf32_rna(x[i].w - xh.w);
-                    h[c + 256 * i] = xh;
+                    float4 xl;
+                    xl.x = tf32_rna(x[i].x - tf32_trunc(x[i].x));
+                    xl.y = tf32_rna(x[i].y - tf32_trunc(x[i].y));
+                    xl.z = tf32_rna(x[i].z - tf32_trunc(x[i].z));
+                    xl.w = tf32_rna(x[i].w - tf32_trunc(x[i].w));
+                    if (hi != nullptr) h[c + 256 * i] = make_float4(tf32_trunc(x[i].x), tf32_trunc(x[i].y), tf32_trunc(x[i].z), tf32_trunc(x[i].w));
                     l[c + 256 * i] = xl;
                 }
             }
@@ -484,7 +490,7 @@ void launch_split_rows(const float *src, int64_t ld_src, int64_t s_src, float *h
                        int64_t ld_dst, int64_t s_dst, int rows, int cols, int batch, cudaStream_t s) {
     const bool vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && ld_src % 4 == 0 && cols % 4 == 0 &&
                      ld_dst % 4 == 0 && (batch == 1 || (s_src % 4 == 0 && s_dst % 4 == 0));
-    if (vec && reinterpret_cast<uintptr_t>(hi) % 16 == 0 && reinterpret_cast<uintptr_t>(lo) % 16 == 0) {
+    if (vec && reinterpret_cast<uintptr_t>(hi) % 16 == 0 && reinterpret_cast<uintptr_t>(lo) % 16 == 0) {   // (hi may be null)
         dim3 grid(unsigned(std::max<int64_t>(1, cdiv(cols / 4, 1024))), unsigned(std::min<int64_t>(rows, 65535)),
                   zdim(batch));
         launch_chained(sgemm_split_rows_vec4_kernel, grid, s, reinterpret_cast<const float4 *>(src), ld_src / 4,

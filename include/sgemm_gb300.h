@@ -312,13 +312,17 @@ sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
  * 0 = FP32 FFMA on the CUDA cores (default): every product and sum in FP32.
  * 1 = error-compensated 3xTF32 on the 5th-generation tensor cores
  *     (tcgen05): each operand is split into a TF32 part and a TF32 residual
- *     (x = hi + lo, both rounded to nearest) and C = alpha * (A_hi.B_hi +
- *     A_hi.B_lo + A_lo.B_hi) + beta * C with FP32 accumulation.  The omitted
- *     A_lo.B_lo term and the rounding of lo bound the extra relative error
- *     per product near 2^-21; integer-valued inputs of magnitude < 2^11 give
- *     bit-exact results.  Needs a workspace of 2 * (M + N) * round_up(K, 4)
- *     floats (rounded up to 256 bytes per part) for the split operands;
- *     the split runs as two extra kernels before the product.
+ *     (x = hi + lo: hi is x with its low 13 mantissa bits dropped, which is
+ *     what the tensor core reads of an FP32 operand, lo = x - hi rounded to
+ *     nearest TF32) and C = alpha * (A_hi.B_hi + A_hi.B_lo + A_lo.B_hi) +
+ *     beta * C with FP32 accumulation.  The omitted A_lo.B_lo term and the
+ *     rounding of lo bound the extra relative error per product near 2^-21;
+ *     integer-valued inputs of magnitude < 2^11 give bit-exact results.
+ *     Needs a workspace of 2 * (M + N) * round_up(K, 4) floats (rounded up
+ *     to 256 bytes per part) for the split operands; the split runs as two
+ *     extra kernels before the product (an operand of at most 64 MB stored
+ *     K contiguous, 16-byte aligned, is read in place as its own high part
+ *     and only its residual is written).
  * The pages treat TF32 only as a different contest; the splitting follows
  * Ootomo & Yokota, "Recovering single precision accuracy from Tensor Cores
  * while surpassing the FP32 theoretical peak performance" (2022).
