@@ -1,6 +1,7 @@
 // FP32 SGEMM on the 5th-generation tensor cores, error-compensated 3xTF32:
 //
-//   x = x_hi + x_lo,  x_hi = tf32(x), x_lo = tf32(x - x_hi)   (round to nearest)
+//   x = x_hi + x_lo,  x_hi = x truncated to TF32 (what the MMA reads of an
+//                     FP32 operand), x_lo = x - x_hi rounded to nearest TF32
 //   A.B ~= A_hi.B_hi + A_hi.B_lo + A_lo.B_hi                  (FP32 accumulation)
 //
 // The dropped term A_lo.B_lo and the rounding of x_lo leave a relative
@@ -11,16 +12,18 @@
 // Ootomo & Yokota (2022).  Integer-valued inputs up to 2^11 in magnitude are
 // exact in TF32 (x_lo = 0), so those products stay bit exact.
 //
-// Two kernels:
-//   * split: A -> A_hi, A_lo (row major, K contiguous) and B -> B_hi^T, B_lo^T
-//     (N x K, K contiguous), so both tensor-core operands are K-major and can
-//     be staged with TMA's 128-byte swizzle, the layout the MMA descriptors
-//     name;
-//   * main: persistent CTAs of 6 warps.  Warp 0 lane 0 streams the four
-//     operand tiles of each 32-wide K slice into a shared-memory ring (TMA);
-//     warp 1 lane 0 issues tcgen05.mma (M=128, N=BN, K=8, kind::tf32) into
-//     TMEM; warps 2..5 read TMEM back (tcgen05.ld, each warp its 32-lane
-//     quarter) and write C = alpha*acc (+ beta*C).
+// Two kinds of kernel:
+//   * split (sgemm_aux.cu): A -> A_hi, A_lo (row major, K contiguous) and
+//     B -> B_hi^T, B_lo^T (N x K, K contiguous), so both tensor-core operands
+//     are K-major and can be staged with TMA's 128-byte swizzle, the layout
+//     the MMA descriptors name; an operand already stored that way is read
+//     in place as its own high part;
+//   * main: persistent CTAs (or SM pairs) of 2 + EPI_WARPS warps.  Warp 0
+//     lane 0 streams the four operand tiles of each 32-wide K slice into a
+//     shared-memory ring (TMA); warp 1 lane 0 (of rank 0 in a pair) issues
+//     tcgen05.mma (K=8, kind::tf32) into TMEM; the epilogue warps read TMEM
+//     back (tcgen05.ld, each warp a 32-lane quarter and a column slab) and
+//     write C = alpha*acc (+ beta*C).
 //
 // Chunked accumulation.  The tensor core's FP32 accumulation does not round
 // to nearest: summing all of K into one TMEM accumulator, whose sign and
