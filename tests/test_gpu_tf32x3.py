@@ -208,3 +208,23 @@ def test_stream_k_repeatable_bitwise(handle):
         handle.set_schedule(0)
     assert handle.device_error() == 0
     _close(first.cpu().numpy(), _ref(p))
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 1500, 700), (512, 384, 260)])
+def test_operand_read_in_place_matches_its_copy_bitwise(handle, M, N, K):
+    # With lda = K (16-byte aligned rows) A is read in place as its own high
+    # part; with lda = K + 1 its truncated high part is copied first.  The
+    # tensor core sees the same TF32 values either way.
+    p = inputs.make_problem(M, N, K, seed=M + K, alpha=0.75, beta=0.0)
+    A = _dev(p.A)
+    B = _dev(p.B)
+    A_odd = torch.empty((M, K + 1), device="cuda")
+    A_odd[:, :K] = A
+    C1 = torch.empty((M, N), device="cuda")
+    C2 = torch.empty((M, N), device="cuda")
+    handle.gemm(A, B, C1, 0.75)
+    handle.gemm(A_odd[:, :K], B, C2, 0.75)
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+    _close(C1.cpu().numpy(), _ref(p))
