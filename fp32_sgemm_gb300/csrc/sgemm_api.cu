@@ -130,10 +130,8 @@ struct Problem {
     int64_t ldc = 0, sc = 0;
     int64_t batch = 1;
 
-    int64_t a_rows() const { return opA ? K : M; }   // stored A
-    int64_t a_cols() const { return opA ? M : K; }
-    int64_t b_rows() const { return opB ? N : K; }   // stored B
-    int64_t b_cols() const { return opB ? K : N; }
+    int64_t a_cols() const { return opA ? M : K; }   // stored A: columns
+    int64_t b_cols() const { return opB ? K : N; }   // stored B: columns
     bool empty() const { return M == 0 || N == 0 || batch == 0; }
 };
 

@@ -419,11 +419,6 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, cudaStream_t s, 
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
-int num_sms() {
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return sms;
-}
 }  // namespace
 
 void launch_scale_c(int M, int N, float beta, float *C, int64_t ldc, int64_t stride_c, int batch,

@@ -555,8 +555,6 @@ sgemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_cons
 // ---------------------------------------------------------------- launches
 
 namespace {
-inline int64_t cdiv(int64_t x, int64_t a) { return (x + a - 1) / a; }
-
 template <class Cfg>
 Tf32x3Info make_info() {
     Tf32x3Info info;
