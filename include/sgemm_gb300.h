@@ -318,8 +318,10 @@ sgemmStatus_t sgemmSetAlgo(sgemmHandle_t handle, int algo);
  *     beta * C with FP32 accumulation.  The omitted A_lo.B_lo term and the
  *     rounding of lo bound the extra relative error per product near 2^-21;
  *     integer-valued inputs of magnitude < 2^11 give bit-exact results.
- *     Needs a workspace of 2 * (M + N) * round_up(K, 4) floats (rounded up
- *     to 256 bytes per part) for the split operands; the split runs as two
+ *     Needs a workspace of 2 * (M + N) * round_up(K, 32) floats (rounded
+ *     up to 256 bytes per part; B stored N x K or K x N alike) for the
+ *     split operands, plus the stream-K partial tiles when they are used
+ *     (sgemmGetWorkspaceSize gives the exact figure); the split runs as two
  *     extra kernels before the product (an operand of at most 64 MB stored
  *     K contiguous, 16-byte aligned, is read in place as its own high part
  *     and only its residual is written).
@@ -425,8 +427,9 @@ sgemmStatus_t sgemmSelfTestWaitTimeout(sgemmHandle_t handle,
  *     no later call loads code or commits memory.  Make that first call
  *     before any stream capture and outside any allocator hook.
  *   - Every call shares the one array per device and the array keeps the
- *     last call's contents; what must start at zero (the stream-K flags) is
- *     cleared on the stream before each launch.  Calls whose work overlaps
+ *     last call's contents; the stream-K partial-tile flags carry a tag per
+ *     launch, kept in the array's control block (zero when the module
+ *     loads), so nothing is cleared between calls.  Calls whose work overlaps
  *     on the GPU (different streams, or different host threads without
  *     ordering) race on the array: order them on one stream.
  *   - Operands that need repacking (base not 16-byte aligned or row pitch not
