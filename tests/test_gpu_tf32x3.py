@@ -228,3 +228,34 @@ def test_operand_read_in_place_matches_its_copy_bitwise(handle, M, N, K):
     assert handle.device_error() == 0
     assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
     _close(C1.cpu().numpy(), _ref(p))
+
+
+@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("opA,opB", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_sm_pair_tile_on_batches_and_transposes(handle, opA, opB, schedule):
+    # Configuration 4 (256 x 256 on SM pairs) pinned: three matrices per
+    # call, every operand form, whole tiles and stream-K (the K range of a
+    # tile cut between pairs, partial tiles added by the rank-matched CTA).
+    M, N, K, batch = 300, 520, 700, 3
+    ar, ac = (K, M) if opA else (M, K)
+    br, bc = (N, K) if opB else (K, N)
+    seed = 31 + 2 * opA + opB + 5 * schedule
+    A = inputs.draw(seed, 0, batch * ar * ac, "integer").reshape(batch, ar, ac)
+    B = inputs.draw(seed + 1, 0, batch * br * bc, "integer").reshape(batch, br, bc)
+    C0 = inputs.draw(seed + 2, 0, batch * M * N, "integer").reshape(batch, M, N)
+    dA, dB, dC = _dev(A), _dev(B), _dev(C0)
+    handle.set_algo(4)
+    handle.set_schedule(schedule)
+    try:
+        handle.gemm_batched(dA, dB, dC, 0.5, -1.25, trans_a=bool(opA), trans_b=bool(opB))
+        torch.cuda.synchronize()
+    finally:
+        handle.set_algo(0)
+        handle.set_schedule(0)
+    assert handle.device_error() == 0
+    got = dC.cpu().numpy()
+    for z in range(batch):
+        opa = np.ascontiguousarray(A[z].T if opA else A[z])
+        opb = np.ascontiguousarray(B[z].T if opB else B[z])
+        ref = oracle.sgemm_ref(M, N, K, 0.5, opa, opb, -1.25, np.ascontiguousarray(C0[z]))
+        np.testing.assert_array_equal(got[z].astype(np.float64), ref, err_msg=f"batch {z}")
