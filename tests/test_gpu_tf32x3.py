@@ -259,3 +259,17 @@ def test_sm_pair_tile_on_batches_and_transposes(handle, opA, opB, schedule):
         opb = np.ascontiguousarray(B[z].T if opB else B[z])
         ref = oracle.sgemm_ref(M, N, K, 0.5, opa, opb, -1.25, np.ascontiguousarray(C0[z]))
         np.testing.assert_array_equal(got[z].astype(np.float64), ref, err_msg=f"batch {z}")
+
+
+@pytest.mark.parametrize("config", [0, 4])
+def test_deep_k_stays_inside_the_bound(handle, config):
+    # 64 accumulator chunks of 256 K each, summed in FP32 registers: the
+    # tensor core's own accumulation error must not pile up across K.
+    M, N, K = 512, 512, 16384
+    p = inputs.make_problem(M, N, K, seed=K + config)
+    handle.set_algo(config)
+    try:
+        got = _run(handle, p)
+    finally:
+        handle.set_algo(0)
+    assert _close(got, _ref(p)) < 0.5
